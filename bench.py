@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the low-bit KV cache on GB300.
+
+One step = for every layer: append one new token per sequence
+(kv_quant_append, which flushes the fp16 window into packed groups when it
+fills) and attend one query token per (sequence, query head) over the whole
+cache (kv_decode_attn).  Inputs (new K/V tokens, queries) and the cache are
+resident in HBM; the cache of all layers together is far larger than L2, so
+every layer's read comes from HBM.
+
+Metric: decode-attention context tokens/s/layer = sum over sequences of the
+tokens attended, divided by the time of one layer (step time / layers).  The
+JSON line also carries the roofline of the decode-attention call (algorithmic
+bytes / CUDA-event time against the measured HBM copy bandwidth), the CPU
+oracle's throughput on a bounded sample, and an end-to-end number through the
+same C ABI with host buffers copied in and out every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (times the CPU oracle instead)
+"""
+
+import os
+
+# the CPU oracle runs single-threaded so its core count is exact
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import dataclasses  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_02_gb300 import synth  # noqa: E402
+
+METRIC = "decode-attn context tokens/s/layer"
+UNIT = "context tokens/s/layer"
+DEFAULT_WORKLOAD = "llama2_7b_mha"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- setup
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def decode_bytes(lengths, w):
+    """Algorithmic HBM bytes of one layer's decode attention: every packed
+    group block (K/V codes + fp32 metadata) once, every fp16 sink/window
+    token (K and V) once, the query and the output."""
+    from bit_kv_cache_02_gb300.kvq import block_bytes
+    bb = block_bytes(w.bits)
+    total = 0
+    for L in lengths:
+        ns = min(L, w.num_sink)
+        n = L - ns
+        r = n % w.residual
+        total += w.kv_heads * ((n - r) // 32 * bb + (r + ns) * 2 * 128 * 2)
+    total += len(lengths) * w.q_heads * 128 * 2 * 2
+    return total
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "kvq_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_kv_cache_02_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per decode-attention call from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_attn_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_call:\s*([0-9]+)\s+source_hash:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.file = None
+        self.window = None
+
+    def mark(self, t0, t1):
+        """Wall-clock bounds of the timed region (samples outside are dropped)."""
+        self.window = (t0, t1)
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        import datetime
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if self.window and not (self.window[0] - 0.05 <= ts <= self.window[1] + 0.05):
+                    continue
+                rows.append(parts[1:])
+        os.unlink(self.file.name)
+        sm = [float(r[1]) for r in rows if _num(r[1])]
+        mx = [float(r[2]) for r in rows if _num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _num(s):
+    try:
+        float(s)
+        return True
+    except ValueError:
+        return False
+
+
+# ---------------------------------------------------------- our arm (GPU)
+
+def prefill_lengths(w, steps, warmup):
+    """Prefilled tokens per sequence: the workload's context lengths, less
+    half the timed steps and the warm-up steps, so that the context averaged
+    over the timed steps equals the workload's."""
+    base = synth.context_lengths(w)
+    shift = warmup + steps // 2
+    return np.maximum(base - shift, 1).astype(np.int64)
+
+
+def build_caches(kvq, w, layers, pre, capacity, device):
+    caches = []
+    for layer in range(layers):
+        c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
+                        pre_rope=w.pre_rope, device=device)
+        T = int(pre.max())
+        k, v = synth.kv_tokens(w, layer, T, device=device)
+        kvq.kv_quant_append(c, k.contiguous(), v.contiguous(),
+                            torch.as_tensor(pre.astype(np.int32), device=device), T)
+        del k, v
+        caches.append(c)
+    torch.cuda.synchronize()
+    for c in caches:
+        if int(c.status.item()) != 0:
+            raise RuntimeError(f"prefill reported device status {int(c.status.item())}")
+    return caches
+
+
+def run_ours(args, w, layers, rank, world, local):
+    from bit_kv_cache_02_gb300 import build
+    build.build()
+    from bit_kv_cache_02_gb300 import kvq
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    K, W = args.steps, args.warmup
+    pre = prefill_lengths(w, K, W)
+    capacity = int(pre.max()) + K + W + 32   # room for the end-to-end steps too
+    caches = build_caches(kvq, w, layers, pre, capacity, device)
+
+    S, H, Hq = w.seqs, w.kv_heads, w.q_heads
+    pool = max(1, min(4, K + W))
+    k_new = [[synth.kv_tokens(w, l, 1, device=device, stream_id=1 + p) for l in range(layers)] for p in range(pool)]
+    qs = [[synth.queries(w, l, p, device=device) for l in range(layers)] for p in range(pool)]
+    ones = torch.ones(S, dtype=torch.int32, device=device)
+    outs = [torch.empty((S, Hq, 128), dtype=torch.float16, device=device) for _ in range(layers)]
+    lens_at = [pre + 1 + i for i in range(K + W + 1)]        # lengths attended at step i
+    ws_bytes = max(kvq.kv_decode_workspace_bytes(caches[0], Hq, int(l.max())) for l in lens_at)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i, ev=None):
+        p = i % pool
+        max_len = int(lens_at[i].max())
+        for l in range(layers):
+            kn, vn = k_new[p][l]
+            kvq.kv_quant_append(caches[l], kn, vn, ones, 1, stream=stream)
+            if ev is not None:
+                ev[l][0].record(stream)
+            kvq.kv_decode_attn(caches[l], qs[p][l], outs[l], ws, max_len, stream=stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    launches0 = kvq.launch_count()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(layers)]
+           for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(K):
+        step(W + i, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(wall0, time.time())
+    barrier(world)
+    launches = kvq.launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t0.elapsed_time(t1)
+    attn_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(layers)]
+    for c in caches:
+        if int(c.status.item()) != 0:
+            raise RuntimeError(f"device status {int(c.status.item())} after the timed steps")
+
+    tokens_per_layer_step = [int(lens_at[W + i].sum()) for i in range(K)]
+    local_tokens = float(sum(tokens_per_layer_step)) * layers      # context tokens attended, all layers
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+    total_tokens = sum_over_ranks(local_tokens, world, device)
+    value = total_tokens / (elapsed_ms / 1e3) / layers
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    bytes_avg = statistics.mean(decode_bytes(lens_at[W + i], w) for i in range(K))
+    attn_tokens_per_s = statistics.mean(tokens_per_layer_step) / attn_avg_s
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, W, stream, world, device)
+
+    return dict(value=value, elapsed_ms=elapsed_ms, attn_avg_s=attn_avg_s, bytes_avg=bytes_avg,
+                attn_tokens_per_s=attn_tokens_per_s, clocks=clocks, launches=launches,
+                mean_ctx=float(np.mean([lens_at[W + i].mean() for i in range(K)])), e2e=e2e,
+                cache_bytes=sum(c.blocks.numel() + 4 * c.k_res.numel() for c in caches))
+
+
+def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, W, stream, world, device):
+    """Same steps through the same C ABI, but every step's inputs start in
+    pinned host memory and every output is read back to pinned host memory
+    inside the timed region.  The caches continue from where the device-only
+    run left them (they keep growing by one token per step)."""
+    pool = len(k_new)
+    h_k = [[(k.cpu().pin_memory(), v.cpu().pin_memory()) for (k, v) in row] for row in k_new]
+    h_q = [[q.cpu().pin_memory() for q in row] for row in qs]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    d_k = [torch.empty_like(k_new[0][0][0]) for _ in range(layers)]
+    d_v = [torch.empty_like(k_new[0][0][1]) for _ in range(layers)]
+    d_q = [torch.empty_like(qs[0][0]) for _ in range(layers)]
+    base = K + W   # steps already appended
+    n_steps = min(K, 20)
+    lens = [pre + 1 + base + i for i in range(n_steps)]
+    need = max(kvq.kv_decode_workspace_bytes(caches[0], w.q_heads, int(l.max())) for l in lens)
+    if need > ws.numel():
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+    h2d = d2h = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        p = i % pool
+        for l in range(layers):
+            d_k[l].copy_(h_k[p][l][0], non_blocking=True)
+            d_v[l].copy_(h_k[p][l][1], non_blocking=True)
+            d_q[l].copy_(h_q[p][l], non_blocking=True)
+            kvq.kv_quant_append(caches[l], d_k[l], d_v[l], ones, 1, stream=stream)
+            kvq.kv_decode_attn(caches[l], d_q[l], outs[l], ws, int(lens[i].max()), stream=stream)
+            h_out[l].copy_(outs[l], non_blocking=True)
+            if i == 0:
+                h2d += 2 * d_k[l].numel() * 2 + d_q[l].numel() * 2
+                d2h += outs[l].numel() * 2
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    elapsed = max_over_ranks(elapsed, world, device)
+    tokens = sum_over_ranks(float(sum(int(l.sum()) for l in lens)) * layers, world, device)
+    return {"value": tokens / elapsed / layers, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n_steps, "timer": "host perf_counter around enqueue + synchronize"}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: n (sequence, KV
+    head) pairs of layer 0 prefilled (untimed) to the workload's mean
+    context; each step appends one token per pair and runs the oracle's
+    attention for all query heads of those KV heads.  The step time is
+    scaled linearly from n pairs to the whole layer (S x Hkv pairs)."""
+
+    def __init__(self, w, seconds_per_step):
+        import oracle
+        self.w = w
+        self.ctx = int(synth.context_lengths(w).mean())
+        self.gq = w.q_heads // w.kv_heads
+        self.pairs = w.seqs * w.kv_heads
+        probe = self._make(oracle, 1, 4)
+        t = time.perf_counter()
+        self._step(probe, 0)
+        per_pair = max(time.perf_counter() - t, 1e-4)
+        self.n = int(max(1, min(self.pairs, seconds_per_step / per_pair)))
+        self.state = self._make(oracle, self.n, 256)
+        self.i = 0
+
+    def _make(self, oracle, n, extra):
+        ws = dataclasses.replace(self.w, seqs=n, kv_heads=1, q_heads=self.gq, ragged_min=0, ctx=self.ctx)
+        k, v = synth.kv_tokens(ws, 0, self.ctx + extra)
+        k, v = k.numpy(), v.numpy()
+        c = oracle.OracleCache(n, 1, self.ctx + extra, self.w.bits, residual=self.w.residual,
+                               num_sink=self.w.num_sink)
+        c.append(k[:, :, :self.ctx], v[:, :, :self.ctx], [self.ctx] * n)
+        return ws, k, v, c
+
+    def _step(self, state, i):
+        ws, k, v, c = state
+        j = self.ctx + i
+        c.append(k[:, :, j:j + 1], v[:, :, j:j + 1], [1] * c.S)
+        c.attention(synth.queries(ws, 0, i).numpy(), pre_rope=self.w.pre_rope)
+        return int(c.seq_len.mean())
+
+    def step(self):
+        """One timed step: (context tokens of the whole layer, scaled seconds)."""
+        t = time.perf_counter()
+        L = self._step(self.state, self.i % 250)
+        dt = time.perf_counter() - t
+        self.i += 1
+        return L * self.w.seqs, dt * self.pairs / self.n
+
+    def describe(self, steps):
+        return (f"{self.n} of {self.pairs} (sequence, KV head) pairs of layer 0 at context {self.ctx}, "
+                f"{steps} steps of append + attention ({self.gq} query heads per KV head), "
+                f"step time scaled linearly to all pairs")
+
+
+def oracle_throughput(w, budget_s):
+    """(tokens/s/layer, description) of the oracle over about budget_s."""
+    smp = OracleSample(w, budget_s / 8)
+    tok = sec = 0.0
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < 8 and (steps == 0 or time.perf_counter() - t0 < budget_s):
+        a, b = smp.step()
+        tok, sec, steps = tok + a, sec + b, steps + 1
+    return tok / sec, smp.describe(steps)
+
+
+def cpu_cores_used():
+    return 1
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    w = synth.WORKLOADS[args.workload]
+    layers = args.layers or w.layers
+    config = {"workload": w.name, "layers": layers, "seqs_per_gpu": w.seqs, "q_heads": w.q_heads,
+              "kv_heads": w.kv_heads, "head_dim": 128, "ctx": w.ctx, "bits": w.bits, "group": 32,
+              "residual": w.residual, "num_sink": w.num_sink, "pre_rope": w.pre_rope,
+              "ragged": bool(w.ragged_min), "parallelism": f"replicas{world}",
+              "l2": "inputs larger than L2: each layer's packed cache is streamed once per step"}
+
+    if args.impl == "reference":
+        init_dist(world, "gloo")
+        if rank != 0:
+            barrier(world)
+            return
+        per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+        smp = OracleSample(w, per_step)
+        for _ in range(args.warmup):
+            smp.step()
+        t0 = time.perf_counter()
+        tok = sec = 0.0
+        for _ in range(args.steps):
+            a, b = smp.step()
+            tok, sec = tok + a, sec + b
+        total = time.perf_counter() - t0
+        value = tok / sec
+        desc = smp.describe(args.steps)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        barrier(world)
+        return
+
+    init_dist(world, "nccl")
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc = oracle_throughput(w, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle", "sample": desc}
+    r = run_ours(args, w, layers, rank, world, local)
+    if rank != 0:
+        return
+    peaks, which = measured_peaks()
+    achieved = r["bytes_avg"] / r["attn_avg_s"] / 1e9
+    peak = float(peaks["hbm_gbs"])
+    traffic = ncu_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["elapsed_ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": f"u{w.bits}-codes/f32-accum",
+        "data": "synthetic", "config": dict(config, mean_ctx_timed=r["mean_ctx"]),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "kv_decode_attn (split + merge)", "peak_source": which,
+                     "algorithmic_bytes_per_call": r["bytes_avg"], "call_us": r["attn_avg_s"] * 1e6},
+        "attn_only": {"value": r["attn_tokens_per_s"], "unit": UNIT},
+        "cpu_baseline": cpu,
+        "e2e": r["e2e"],
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

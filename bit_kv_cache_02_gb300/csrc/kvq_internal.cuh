@@ -1,0 +1,164 @@
+// Internal definitions shared by the kernels of the low-bit KV-cache library.
+//
+// Packed block (one group of 32 tokens of one (sequence, KV head)):
+//   [K codes 32*D*b/8][V codes 32*D*b/8][K scale f32 D][K min f32 D]
+//   [V scale f32 32][V min f32 32]
+// A code tile is 32 lanes x W 32-bit words.  Element (row, col) (keys: row =
+// token, col = channel; values: row = channel, col = token) sits in lane
+// 4*(row%8) + (col%8)/2, word w = (P*KT + kt)*(4/nu) + tau/nu, bit
+// 16*(col%2) + 8*((col/8)%2) + b*(tau%nu), where mt = row/16, tau =
+// 2*(mt%2) + (row/8)%2, P = mt/2, kt = col/16, KT = cols/16, nu = 8/b.  Word
+// w of lane l is at byte ((w/4)*32 + l)*16 + (w%4)*4.  With this order one
+// 32-bit word yields, under a single AND mask, a half2 register of the
+// m16n8k16 A fragment whose two fp16 values are (code << b*u) * 2^-24 (fp16
+// subnormals), which the tensor core multiplies exactly.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kD = 128;       // head dimension
+constexpr int kG = 32;        // tokens per group
+
+__host__ __device__ constexpr int code_tile_bytes(int bits) { return kG * kD * bits / 8; }
+__host__ __device__ constexpr int block_bytes(int bits) { return 2 * code_tile_bytes(bits) + 8 * kD + 8 * kG; }
+__host__ __device__ constexpr int off_kc(int) { return 0; }
+__host__ __device__ constexpr int off_vc(int bits) { return code_tile_bytes(bits); }
+__host__ __device__ constexpr int off_ks(int bits) { return 2 * code_tile_bytes(bits); }
+__host__ __device__ constexpr int off_km(int bits) { return off_ks(bits) + 4 * kD; }
+__host__ __device__ constexpr int off_vs(int bits) { return off_km(bits) + 4 * kD; }
+__host__ __device__ constexpr int off_vm(int bits) { return off_vs(bits) + 4 * kG; }
+
+// Cache geometry and buffers as the kernels see them.
+struct Geo {
+  int S, H, R, ns, bits, pre_rope;
+  float theta;
+  int capacity;
+  int max_groups;
+  uint8_t *blocks;
+  __half *k_res, *v_res, *k_sink, *v_sink;
+  int *seq_len;
+  int *status;
+};
+
+// Stream bookkeeping of a sequence holding L tokens.
+struct Split {
+  int nsink;  // tokens in the sink
+  int Lq;     // quantized stream tokens
+  int r;      // tokens in the window
+};
+
+__host__ __device__ inline Split split_len(int L, int ns, int R) {
+  Split sp;
+  sp.nsink = L < ns ? L : ns;
+  int n = L - sp.nsink;
+  sp.r = n % R;
+  sp.Lq = n - sp.r;
+  return sp;
+}
+
+__device__ inline void set_status(int *status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ inline uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ inline void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`, giving up after about two seconds of SM
+// clock; returns false (and the caller records KVQ_STATUS_TIMEOUT) on timeout.
+__device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > 4000000000LL) return false;
+  }
+  return true;
+}
+
+// One-dimensional bulk copy global -> shared, completing on `bar`.
+__device__ inline void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ inline void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ inline uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// Split (x0, x1) into fp16 hi + lo parts: hi = fp16(x), lo = fp16(x - hi).
+// Returns lo when `want_lo`, else hi.
+__device__ inline uint32_t hi_or_lo(float x0, float x1, bool want_lo) {
+  __half2 hi = __floats2half2_rn(x0, x1);
+  float2 hf = __half22float2(hi);
+  __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  return want_lo ? h2_as_u32(lo) : h2_as_u32(hi);
+}
+
+// ------------------------------------------------------- host-side launchers
+
+// Workspace plan of one decode call: groups per split, splits per (sequence,
+// query head), RoPE base rows, and the byte offsets of the workspace regions
+// (partial outputs, partial (max, sum), RoPE tables), each 256-byte aligned.
+struct DecodePlan {
+  int chunk, nsp, n_base;
+  size_t off_ml, off_base, off_off, bytes;
+};
+
+cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
+                                int max_new, cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_dequant(const Geo &geo, float *k_out, float *v_out, cudaStream_t stream, uint64_t *launches);
+DecodePlan plan_decode(const Geo &geo, int Hq, int max_len);
+cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
+                          void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
+                          uint64_t *launches);
+int set_decode_chunk(int groups);
+
+}  // namespace kvq

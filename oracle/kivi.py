@@ -22,7 +22,7 @@ Method, by source (page title, section):
 * First token kept in fp16 (attention sink): "KV cache quantization",
   "What they report" (KVQuant paragraph).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 min/max and scale in fp32, scale = (max - min) / (2^b - 1) by one IEEE
 division, code = round-half-even of (x - min) / scale by one IEEE
 subtraction and one IEEE division, scale == 0 gives code 0; one (scale, min)

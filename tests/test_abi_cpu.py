@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/kvq.h declares, sizes buffers as the
+packed format says, and rejects bad arguments before launching anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from bit_kv_cache_02_gb300 import build
+    build.build()
+    from bit_kv_cache_02_gb300 import kvq as mod
+    return mod
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq?_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(kvq):
+    names = _declared()
+    assert {"kv_quant_append", "kv_decode_attn", "kv_dequant", "kv_decode_workspace_bytes"} <= set(names)
+    lib = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kvq.EXPORTED) == set(names)
+
+
+def _struct(kvq, **kw):
+    d = dict(num_seqs=2, num_kv_heads=3, head_dim=128, bits=2, group=32, residual=128, num_sink=1,
+             pre_rope=0, rope_theta=10000.0, capacity=1000)
+    d.update(kw)
+    st = kvq.CacheStruct()
+    for k, v in d.items():
+        setattr(st, k, v)
+    return st
+
+
+def test_sizes(kvq):
+    assert kvq.lib.kvq_block_bytes(2, 128) == 3328 and kvq.lib.kvq_block_bytes(4, 128) == 5376
+    assert kvq.lib.kvq_block_bytes(3, 128) == 0 and kvq.lib.kvq_block_bytes(2, 64) == 0
+    st = _struct(kvq)
+    # (1000 - 1) // 128 * 128 = 896 quantized tokens -> 28 groups
+    assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == 28
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_BLOCKS) == 2 * 3 * 28 * 3328
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_K_RES) == 2 * 3 * 128 * 128 * 2
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_K_SINK) == 2 * 3 * 1 * 128 * 2
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_SEQ_LEN) == 8
+    st0 = _struct(kvq, num_sink=0)
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st0), kvq.BUF_K_SINK) == 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 64, -2), ("bits", 3, -2), ("group", 16, -2), ("residual", 100, -2),
+    ("residual", 256, -2), ("num_sink", 2, -2), ("num_seqs", 0, -1), ("capacity", 0, -1),
+])
+def test_bad_geometry_rejected(kvq, field, value, code):
+    st = _struct(kvq, **{field: value})
+    assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == -1
+    assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 3, 10) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == code
+
+
+def test_workspace_sizing(kvq):
+    st = _struct(kvq)
+    n = kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 6, 1000)
+    assert n > 0 and n % 256 == 0
+    assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 5, 1000) == -1   # not a multiple of Hkv
+    assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 24, 1000) == -1  # group of 8 unsupported
+    assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 6, 1001) == -1   # past capacity
+
+
+def test_null_and_misaligned_buffers_rejected_before_launch(kvq):
+    st = _struct(kvq)
+    base = 1 << 30
+    st.blocks, st.k_res, st.v_res = base, base + 4096, base + 8192
+    st.k_sink, st.v_sink, st.seq_len = base + 12288, base + 16384, base + 20480
+    p = ctypes.byref(st)
+    kn = ctypes.c_void_p(base + (1 << 24))
+    nl = ctypes.c_void_p(base + (1 << 25))
+    assert kvq.lib.kv_quant_append(p, None, kn, nl, 4, None) == -1          # null k_new
+    assert kvq.lib.kv_quant_append(p, kn, kn, None, 4, None) == -1          # null new_len
+    assert kvq.lib.kv_quant_append(p, kn, kn, nl, 1001, None) == -3         # max_new > capacity
+    assert kvq.lib.kv_quant_append(p, ctypes.c_void_p(base + 2), kn, nl, 4, None) == -5
+    st.blocks = base + 64                                                     # blocks need 128 B
+    assert kvq.lib.kv_quant_append(p, kn, kn, nl, 4, None) == -5
+    st.blocks = base
+    st.k_sink = None                                                          # sink needed when num_sink=1
+    assert kvq.lib.kv_quant_append(p, kn, kn, nl, 4, None) == -1
+    st.k_sink = base + 12288
+    q = ctypes.c_void_p(base + (1 << 26))
+    ws = ctypes.c_void_p(base + (1 << 27))
+    need = kvq.lib.kv_decode_workspace_bytes(p, 6, 1000)
+    assert kvq.lib.kv_decode_attn(p, 6, q, 0.0, q, ws, need - 1, 1000, None) == -4
+    assert kvq.lib.kv_decode_attn(p, 6, q, 0.0, q, None, need, 1000, None) == -4
+    assert kvq.lib.kv_decode_attn(p, 6, q, 0.0, q, ctypes.c_void_p(base + (1 << 27) + 16), need, 1000, None) == -5
+    assert kvq.lib.kv_decode_attn(p, 6, q, 0.0, q, ws, need, 1001, None) == -3
+    assert kvq.lib.kv_decode_attn(p, 24, q, 0.0, q, ws, need, 1000, None) == -2
+    assert kvq.lib.kv_decode_attn(p, 6, None, 0.0, q, ws, need, 1000, None) == -1
+    assert kvq.lib.kv_dequant(p, None, q, None) == -1
+    assert kvq.lib.kvq_set_decode_chunk(6) == -1 and kvq.lib.kvq_set_decode_chunk(0) == 0
+    assert kvq.lib.kvq_strerror(-4) == b"workspace missing or too small"

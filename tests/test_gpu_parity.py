@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.
+
+Packed codes, scales, mins, the fp16 window, the sink and seq_len must match
+byte for byte; dequantized values within 1 fp32 ulp; attention outputs within
+|gpu - oracle| <= 2e-3 + 1e-2 * |oracle| per element (fp16 outputs)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_kv_cache_02_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_kv_cache_02_gb300 import build
+    build.build()
+    from bit_kv_cache_02_gb300 import kvq as mod
+    return mod
+
+
+def _rand_kv(S, H, T, seed, outliers=(3, 17, 64, 101), mult=15.0):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((S, H, T, 128), dtype=np.float32)
+    v = rng.standard_normal((S, H, T, 128), dtype=np.float32)
+    k[..., list(outliers)] *= mult
+    return k.astype(np.float16), v.astype(np.float16)
+
+
+def _rand_q(S, Hq, seed):
+    return np.random.default_rng(seed).standard_normal((S, Hq, 128), dtype=np.float32).astype(np.float16)
+
+
+def _compare_state(cache, orc, heads=None):
+    """Byte-compare the valid parts of the device state with the oracle's."""
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    sl = cache.seq_len.cpu().numpy()
+    np.testing.assert_array_equal(sl, orc.seq_len)
+    blocks = cache.blocks_view().cpu().numpy()
+    kres, vres = cache.k_res.cpu().numpy(), cache.v_res.cpu().numpy()
+    ksink, vsink = cache.k_sink.cpu().numpy(), cache.v_sink.cpu().numpy()
+    for s in range(orc.S):
+        ns, Lq, r = orc.split(s)
+        ng = Lq // 32
+        np.testing.assert_array_equal(blocks[s, :, :ng], orc.blocks[s, :, :ng], err_msg=f"blocks seq {s}")
+        np.testing.assert_array_equal(kres[s, :, :r].view(np.uint16), orc.k_res[s, :, :r].view(np.uint16))
+        np.testing.assert_array_equal(vres[s, :, :r].view(np.uint16), orc.v_res[s, :, :r].view(np.uint16))
+        if ns:
+            np.testing.assert_array_equal(ksink[s, :, :ns].view(np.uint16), orc.k_sink[s, :, :ns].view(np.uint16))
+            np.testing.assert_array_equal(vsink[s, :, :ns].view(np.uint16), orc.v_sink[s, :, :ns].view(np.uint16))
+
+
+def _attn_close(got, want):
+    got = got.astype(np.float64)
+    want = want.astype(np.float64)
+    err = np.abs(got - want)
+    bad = err > ATOL + RTOL * np.abs(want)
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance, max abs err {err.max():.3e}"
+    return float(err.max())
+
+
+def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128):
+    cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope)
+    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns)
+    return cache, orc
+
+
+def _append(kvq, cache, orc, k, v, lens):
+    dk = torch.from_numpy(np.ascontiguousarray(k)).cuda()
+    dv = torch.from_numpy(np.ascontiguousarray(v)).cuda()
+    nl = torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    kvq.kv_quant_append(cache, dk, dv, nl, k.shape[2])
+    orc.append(k, v, lens)
+
+
+def _attend(kvq, cache, q, max_len):
+    dq = torch.from_numpy(q).cuda()
+    out = torch.empty_like(dq)
+    ws = kvq.alloc_workspace(cache, q.shape[1], max_len)
+    kvq.kv_decode_attn(cache, dq, out, ws, max_len)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+# ------------------------------------------------------------------- Tiny
+
+def test_tiny_full(kvq):
+    w = synth.WORKLOADS["tiny"]
+    k, v = synth.kv_tokens(w, 0, w.ctx)
+    k, v = k.numpy(), v.numpy()
+    cache, orc = _build(kvq, 1, 1, 512, 2)
+    _append(kvq, cache, orc, k, v, [256])
+    _compare_state(cache, orc)
+    q = synth.queries(w, 0).numpy()
+    got = _attend(kvq, cache, q, 256)
+    _attn_close(got, orc.attention(q))
+    # dequant within one fp32 ulp
+    K = torch.full((1, 1, 512, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    np.testing.assert_array_max_ulp(K.cpu().numpy()[:, :, :256], Ko[:, :, :256].astype(np.float32), maxulp=1)
+    np.testing.assert_array_max_ulp(V.cpu().numpy()[:, :, :256], Vo[:, :, :256].astype(np.float32), maxulp=1)
+    assert torch.isnan(K[:, :, 256:]).all()
+
+
+# ------------------------------------------------------------ boundary sweep
+
+LENS = [1, 2, 31, 32, 33, 127, 128, 129, 255, 256, 257]
+
+
+@pytest.mark.parametrize("pre_rope", [False, True])
+@pytest.mark.parametrize("ns", [0, 1])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_boundary_sweep(kvq, bits, ns, pre_rope):
+    S, H, gq = len(LENS), 2, 2
+    T = max(LENS)
+    k, v = _rand_kv(S, H, T, seed=100 + bits + 10 * ns)
+    cache, orc = _build(kvq, S, H, 300, bits, ns=ns, pre_rope=pre_rope)
+    _append(kvq, cache, orc, k, v, LENS)
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=7)
+    got = _attend(kvq, cache, q, T)
+    _attn_close(got, orc.attention(q, pre_rope=pre_rope))
+    K = torch.full((S, H, 300, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    Kg, Vg = K.cpu().numpy(), V.cpu().numpy()
+    for s, L in enumerate(LENS):
+        np.testing.assert_array_max_ulp(Kg[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
+        np.testing.assert_array_max_ulp(Vg[s, :, :L], Vo[s, :, :L].astype(np.float32), maxulp=1)
+        assert np.isnan(Kg[s, :, L:]).all()
+
+
+@pytest.mark.parametrize("gq", [1, 2, 4])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_gqa_group_sizes(kvq, gq, bits):
+    S, H, T = 3, 2, 700
+    k, v = _rand_kv(S, H, T, seed=31 + gq)
+    cache, orc = _build(kvq, S, H, 800, bits)
+    _append(kvq, cache, orc, k, v, [700, 333, 129])
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=gq)
+    _attn_close(_attend(kvq, cache, q, 700), orc.attention(q))
+
+
+# ------------------------------------------------------------- streaming
+
+@pytest.mark.parametrize("ns", [0, 1])
+def test_streaming_appends_match_prefill(kvq, ns):
+    """One-token appends, ragged chunks and one prefill all leave the oracle's
+    bytes, across several window flushes."""
+    S, H, T = 3, 2, 300
+    k, v = _rand_kv(S, H, T, seed=5)
+    lens = np.array([300, 257, 128 + ns])
+    caches = []
+    for mode in ("prefill", "tokens", "chunks"):
+        cache, orc = _build(kvq, S, H, 320, 2, ns=ns)
+        if mode == "prefill":
+            _append(kvq, cache, orc, k, v, lens)
+        elif mode == "tokens":
+            for t in range(T):
+                _append(kvq, cache, orc, k[:, :, t:t + 1], v[:, :, t:t + 1], (t < lens).astype(np.int32))
+        else:
+            pos = 0
+            for step in (1, 126, 2, 64, 107):
+                sl = np.clip(lens - pos, 0, step).astype(np.int32)
+                _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+                pos += step
+        _compare_state(cache, orc)
+        caches.append(cache)
+    b0 = caches[0].blocks.cpu()
+    for c in caches[1:]:
+        assert torch.equal(c.blocks.cpu(), b0)
+
+
+def test_decode_step_flush_then_attend(kvq):
+    """A window holding R-1 tokens plus one appended token flushes; attention
+    then reads only quantized groups."""
+    S, H, T = 2, 2, 256
+    k, v = _rand_kv(S, H, T, seed=9)
+    cache, orc = _build(kvq, S, H, 300, 2)
+    _append(kvq, cache, orc, k[:, :, :255], v[:, :, :255], [255, 255])
+    assert orc.split(0) == (0, 128, 127)
+    _append(kvq, cache, orc, k[:, :, 255:], v[:, :, 255:], [1, 1])
+    assert orc.split(0) == (0, 256, 0)
+    _compare_state(cache, orc)
+    q = _rand_q(S, 2 * H, seed=3)
+    _attn_close(_attend(kvq, cache, q, 256), orc.attention(q))
+
+
+# ------------------------------------------------------ edge and error cases
+
+def test_empty_cache_outputs_zero(kvq):
+    cache, orc = _build(kvq, 2, 1, 64, 2)
+    q = _rand_q(2, 1, seed=1)
+    got = _attend(kvq, cache, q, 64)
+    assert (got == 0).all()
+
+
+def test_capacity_overflow_sets_status_and_skips(kvq):
+    cache, orc = _build(kvq, 2, 1, 160, 2)
+    k, v = _rand_kv(2, 1, 150, seed=2)
+    _append(kvq, cache, orc, k, v, [150, 20])
+    k2, v2 = _rand_kv(2, 1, 20, seed=3)
+    before = cache.blocks.clone()
+    dk, dv = torch.from_numpy(k2).cuda(), torch.from_numpy(v2).cuda()
+    kvq.kv_quant_append(cache, dk, dv, torch.tensor([20, 5], dtype=torch.int32, device="cuda"), 20)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) & kvq.KVQ_STATUS_CAPACITY
+    assert cache.seq_len.cpu().tolist() == [150, 25]          # seq 0 skipped, seq 1 appended
+    assert torch.equal(cache.blocks[: before.numel() // 2], before[: before.numel() // 2])
+
+
+def test_bad_new_len_sets_status(kvq):
+    cache, _ = _build(kvq, 1, 1, 64, 2)
+    k, v = _rand_kv(1, 1, 4, seed=2)
+    kvq.kv_quant_append(cache, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                        torch.tensor([9], dtype=torch.int32, device="cuda"), 4)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) & kvq.KVQ_STATUS_BAD_LEN
+    assert cache.seq_len.item() == 0
+
+
+def test_workspace_too_small_raises(kvq):
+    cache, _ = _build(kvq, 1, 1, 64, 2)
+    q = torch.zeros((1, 1, 128), dtype=torch.float16, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kv_decode_attn(cache, q, torch.empty_like(q), ws, 64)
+    assert e.value.code == -4
+
+
+@pytest.mark.parametrize("chunk", [4, 8, 64])
+def test_split_sizes_agree(kvq, chunk):
+    """The answer does not depend on how the token axis is split."""
+    S, H, T = 2, 2, 1500
+    k, v = _rand_kv(S, H, T, seed=12)
+    cache, orc = _build(kvq, S, H, 1600, 2, ns=1)
+    _append(kvq, cache, orc, k, v, [1500, 1100])
+    q = _rand_q(S, 4 * H, seed=4)
+    want = orc.attention(q)
+    try:
+        kvq.set_decode_chunk(chunk)
+        _attn_close(_attend(kvq, cache, q, 1500), want)
+    finally:
+        kvq.set_decode_chunk(0)
