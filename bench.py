@@ -207,6 +207,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def _json_default(o):
+    if hasattr(o, "item"):
+        return o.item()
+    raise TypeError(f"not JSON serializable: {type(o).__name__}")
+
+
 def _num(s):
     try:
         float(s)
@@ -315,7 +321,8 @@ def run_ours(args, w, layers, rank, world, local):
     local_tokens = float(sum(tokens_per_layer_step)) * layers      # context tokens attended, all layers
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     total_tokens = sum_over_ranks(local_tokens, world, device)
-    value = total_tokens / (elapsed_ms / 1e3) / layers
+    # tokens/s/layer = (tokens one layer attends) / (step time / layers)
+    value = total_tokens / (elapsed_ms / 1e3)
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     bytes_avg = statistics.mean(decode_bytes(lens_at[W + i], w) for i in range(K))
     attn_tokens_per_s = statistics.mean(tokens_per_layer_step) / attn_avg_s
@@ -368,7 +375,7 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, 
     elapsed = time.perf_counter() - t0
     elapsed = max_over_ranks(elapsed, world, device)
     tokens = sum_over_ranks(float(sum(int(l.sum()) for l in lens)) * layers, world, device)
-    return {"value": tokens / elapsed / layers, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    return {"value": tokens / elapsed, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n_steps, "timer": "host perf_counter around enqueue + synchronize"}
 
 
@@ -478,7 +485,7 @@ def main():
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
                                  "sample": desc},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        print(json.dumps(line, default=_json_default))
         barrier(world)
         return
 
@@ -509,7 +516,7 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
-    print(json.dumps(line))
+    print(json.dumps(line, default=_json_default))
 
 
 if __name__ == "__main__":
