@@ -194,6 +194,36 @@ int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    void *stream);
 
 /*
+ * kv_decode_attn_noalloc -- kv_decode_attn for callers that cannot allocate
+ * device memory.
+ *
+ * The pages describe no such interface; it has no counterpart in the method.
+ * It exists for callers that cannot hand the library a workspace: code
+ * running inside a host program whose device memory is owned and planned by
+ * another runtime (a plugin in an inference server or engine with a fixed
+ * memory budget), and paths where a cudaMalloc is not allowed because it can
+ * synchronize the device.
+ *
+ * Same arguments and results as kv_decode_attn, minus the workspace.  The
+ * scratch is a 16 MiB array compiled into this library (every GPU that loads
+ * the library keeps it until the process exits).  A call whose
+ * kv_decode_workspace_bytes(cache, num_q_heads, max_len) exceeds 16 MiB
+ * returns KVQ_ERR_WORKSPACE and enqueues nothing.  Nothing is allocated: no
+ * cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture.  All calls on a device share the one array and it keeps
+ * the previous call's contents (this path needs none of them zeroed): calls
+ * whose work overlaps on the GPU (different streams, or different host
+ * threads without ordering) race on the scratch and must be serialized by
+ * the caller.
+ */
+int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_heads,
+                           const uint16_t *q, float softmax_scale,
+                           uint16_t *out, int32_t max_len, void *stream);
+
+/*
  * kv_dequant -- test aid: write the dequantized cache.
  *
  *   k_out, v_out  [S][Hkv][capacity][D] fp32.  For every stored position p <
