@@ -232,22 +232,47 @@ def prefill_lengths(w, steps, warmup):
     return np.maximum(base - shift, 1).astype(np.int64)
 
 
+def prefill_bytes(lengths, w):
+    """Algorithmic bytes of a prefill: quantized tokens read fp16 K and V and
+    write their share of the packed blocks; window and sink tokens are read
+    and written as fp16."""
+    from bit_kv_cache_02_gb300.kvq import block_bytes
+    bb = block_bytes(w.bits)
+    total = 0
+    for L in lengths:
+        L = int(L)
+        ns = min(L, w.num_sink)
+        n = L - ns
+        r = n % w.residual
+        total += w.kv_heads * ((n - r) * (2 * 128 * 2 + bb // 32) + (r + ns) * 2 * 2 * 128 * 2)
+    return total
+
+
 def build_caches(kvq, w, layers, pre, capacity, device):
-    caches = []
+    """Prefill every layer's cache (kv_quant_append of the whole context);
+    returns the caches and the per-layer prefill times (CUDA events)."""
+    caches, times = [], []
+    stream = torch.cuda.current_stream(device)
     for layer in range(layers):
         c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
                         pre_rope=w.pre_rope, device=device)
         T = int(pre.max())
         k, v = synth.kv_tokens(w, layer, T, device=device)
-        kvq.kv_quant_append(c, k.contiguous(), v.contiguous(),
-                            torch.as_tensor(pre.astype(np.int32), device=device), T)
+        k, v = k.contiguous(), v.contiguous()
+        nl = torch.as_tensor(pre.astype(np.int32), device=device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kvq.kv_quant_append(c, k, v, nl, T, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
         del k, v
         caches.append(c)
     torch.cuda.synchronize()
     for c in caches:
         if int(c.status.item()) != 0:
             raise RuntimeError(f"prefill reported device status {int(c.status.item())}")
-    return caches
+    return caches, times
 
 
 def run_ours(args, w, layers, rank, world, local):
@@ -260,7 +285,8 @@ def run_ours(args, w, layers, rank, world, local):
     K, W = args.steps, args.warmup
     pre = prefill_lengths(w, K, W)
     capacity = int(pre.max()) + K + W + 32   # room for the end-to-end steps too
-    caches = build_caches(kvq, w, layers, pre, capacity, device)
+    caches, prefill_s = build_caches(kvq, w, layers, pre, capacity, device)
+    prefill = {"seconds_per_layer": statistics.median(prefill_s), "bytes_per_layer": prefill_bytes(pre, w)}
 
     S, H, Hq = w.seqs, w.kv_heads, w.q_heads
     pool = max(1, min(4, K + W))
@@ -333,7 +359,7 @@ def run_ours(args, w, layers, rank, world, local):
 
     return dict(value=value, elapsed_ms=elapsed_ms, attn_avg_s=attn_avg_s, bytes_avg=bytes_avg,
                 attn_tokens_per_s=attn_tokens_per_s, clocks=clocks, launches=launches,
-                mean_ctx=float(np.mean([lens_at[W + i].mean() for i in range(K)])), e2e=e2e,
+                mean_ctx=float(np.mean([lens_at[W + i].mean() for i in range(K)])), e2e=e2e, prefill=prefill,
                 cache_bytes=sum(c.blocks.numel() + 4 * c.k_res.numel() for c in caches))
 
 
@@ -511,6 +537,12 @@ def main():
                      "kernel": "kv_decode_attn (split + merge)", "peak_source": which,
                      "algorithmic_bytes_per_call": r["bytes_avg"], "call_us": r["attn_avg_s"] * 1e6},
         "attn_only": {"value": r["attn_tokens_per_s"], "unit": UNIT},
+        "quantize": {"kernel": "kv_quant_append (prefill of one layer)",
+                     "achieved": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9,
+                     "unit": "GB/s", "peak": peak,
+                     "frac": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9 / peak,
+                     "algorithmic_bytes": r["prefill"]["bytes_per_layer"],
+                     "us": r["prefill"]["seconds_per_layer"] * 1e6},
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
         "gpu_launches": r["launches"],

@@ -146,10 +146,11 @@ __device__ inline uint32_t hi_or_lo(float x0, float x1, bool want_lo) {
 
 // Workspace plan of one decode call: groups per split, splits per (sequence,
 // query head), RoPE base rows, and the byte offsets of the workspace regions
-// (partial outputs, partial (max, sum), RoPE tables), each 256-byte aligned.
+// (partial outputs, partial (max, sum), per-(sequence, KV head) split
+// counters, RoPE tables), each 256-byte aligned.
 struct DecodePlan {
   int chunk, nsp, n_base;
-  size_t off_ml, off_base, off_off, bytes;
+  size_t off_ml, off_cnt, off_base, off_off, bytes;
 };
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,

@@ -177,7 +177,8 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  *   out     [S][Hq][D] fp16, written for every row (zeros when seq_len is 0).
  *   workspace, workspace_bytes  device scratch of at least
  *           kv_decode_workspace_bytes(cache, num_q_heads, max_len) bytes,
- *           256-byte aligned; no contents need to be preserved between calls.
+ *           256-byte aligned; no contents need to be preserved between calls
+ *           (the call zeroes its split counters itself).
  *   max_len host bound on every seq_len (sizes the split-K grid); a
  *           sequence longer than max_len gets a zero output row and sets
  *           KVQ_STATUS_MAX_LEN.
@@ -185,8 +186,9 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  * Keys are k_hat = code * scale + min (pre-RoPE keys then rotated by
  * rotate-half RoPE at their absolute position); values likewise.  The kernel
  * dequantizes in registers, forms scores, runs an online softmax per split of
- * the token axis and merges the splits (log-sum-exp).  Enqueues one to three
- * kernels (a RoPE table kernel only when pre_rope).
+ * the token axis, and the last split to finish merges them (log-sum-exp).
+ * Enqueues a memset of the split counters and one kernel (plus a RoPE table
+ * kernel when pre_rope).
  */
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    const uint16_t *q, float softmax_scale, uint16_t *out,
@@ -214,7 +216,8 @@ int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
  * stream capture.  All calls on a device share the one array and it keeps
- * the previous call's contents (this path needs none of them zeroed): calls
+ * the previous call's contents (each call clears the part that must start
+ * at zero, on its own stream, before using it): calls
  * whose work overlaps on the GPU (different streams, or different host
  * threads without ordering) race on the scratch and must be serialized by
  * the caller.
