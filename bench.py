@@ -60,6 +60,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--chunk", type=int, default=0, help="groups per decode work item (0: library's choice)")
     return p.parse_args()
 
 
@@ -225,8 +226,8 @@ def _num(s):
 
 def prefill_lengths(w, steps, warmup):
     """Prefilled tokens per sequence: the workload's context lengths, less
-    half the timed steps and the warm-up steps, so that the context averaged
-    over the timed steps equals the workload's."""
+    half the timed steps and the untimed steps before them, so that the
+    context averaged over the timed steps equals the workload's."""
     base = synth.context_lengths(w)
     shift = warmup + steps // 2
     return np.maximum(base - shift, 1).astype(np.int64)
@@ -282,46 +283,58 @@ def run_ours(args, w, layers, rank, world, local):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.chunk:
+        kvq.set_decode_chunk(args.chunk)
     K, W = args.steps, args.warmup
-    pre = prefill_lengths(w, K, W)
-    capacity = int(pre.max()) + K + W + 32   # room for the end-to-end steps too
+    pool = max(1, min(4, K))
+    pre = prefill_lengths(w, K, max(W, 1) + pool)
+    capacity = int(pre.max()) + max(W, 1) + pool + K + 32   # room for the end-to-end steps too
     caches, prefill_s = build_caches(kvq, w, layers, pre, capacity, device)
     prefill = {"seconds_per_layer": statistics.median(prefill_s), "bytes_per_layer": prefill_bytes(pre, w)}
 
-    S, H, Hq = w.seqs, w.kv_heads, w.q_heads
-    pool = max(1, min(4, K + W))
+    S, Hq = w.seqs, w.q_heads
     k_new = [[synth.kv_tokens(w, l, 1, device=device, stream_id=1 + p) for l in range(layers)] for p in range(pool)]
     qs = [[synth.queries(w, l, p, device=device) for l in range(layers)] for p in range(pool)]
     ones = torch.ones(S, dtype=torch.int32, device=device)
     outs = [torch.empty((S, Hq, 128), dtype=torch.float16, device=device) for _ in range(layers)]
-    lens_at = [pre + 1 + i for i in range(K + W + 1)]        # lengths attended at step i
-    ws_bytes = max(kvq.kv_decode_workspace_bytes(caches[0], Hq, int(l.max())) for l in lens_at)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
+    # The decode grid is sized for the cache capacity, so one captured graph
+    # serves every step (the kernel reads the actual lengths on the device).
+    max_len = capacity
+    ws = torch.empty(kvq.kv_decode_workspace_bytes(caches[0], Hq, max_len), dtype=torch.uint8, device=device)
 
-    def step(i, ev=None):
-        p = i % pool
-        max_len = int(lens_at[i].max())
+    def step_calls(p, append=True):
         for l in range(layers):
-            kn, vn = k_new[p][l]
-            kvq.kv_quant_append(caches[l], kn, vn, ones, 1, stream=stream)
-            if ev is not None:
-                ev[l][0].record(stream)
-            kvq.kv_decode_attn(caches[l], qs[p][l], outs[l], ws, max_len, stream=stream)
-            if ev is not None:
-                ev[l][1].record(stream)
+            if append:
+                kn, vn = k_new[p][l]
+                kvq.kv_quant_append(caches[l], kn, vn, ones, 1)
+            kvq.kv_decode_attn(caches[l], qs[p][l], outs[l], ws, max_len)
 
-    for i in range(W):
-        step(i)
+    # eager warm-up, then one CUDA graph per input set: a step launches ~3
+    # kernels per layer, too many to issue from Python at the GPU's pace
+    for i in range(max(W, 1)):
+        step_calls(i % pool)
     torch.cuda.synchronize()
-    barrier(world)
+    n0 = kvq.launch_count()
+    graphs = []
+    for p in range(pool):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step_calls(p)
+        graphs.append(g)
+    launches_per_step = (kvq.launch_count() - n0) // pool
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph):
+        step_calls(0, append=False)
+    for p in range(pool):                 # first replays upload the graphs
+        graphs[p].replay()
+    torch.cuda.synchronize()
+    done = max(W, 1) + pool                # steps appended so far
+    lens_at = [pre + 1 + done + i for i in range(K)]   # lengths attended in timed step i
+    stream = torch.cuda.current_stream(device)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    launches0 = kvq.launch_count()
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(layers)]
-           for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -329,45 +342,56 @@ def run_ours(args, w, layers, rank, world, local):
     wall0 = time.time()
     t0.record(stream)
     for i in range(K):
-        step(W + i, evs[i])
+        graphs[i % pool].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark(wall0, time.time())
     barrier(world)
-    launches = kvq.launch_count() - launches0
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t0.elapsed_time(t1)
-    attn_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(K) for l in range(layers)]
+
+    # decode attention alone: the same calls without the appends, replayed
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    dgraph.replay()
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for _ in range(K):
+        dgraph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    attn_avg_s = d0.elapsed_time(d1) / 1e3 / (K * layers)
+    final_lens = pre + done + K
     for c in caches:
         if int(c.status.item()) != 0:
             raise RuntimeError(f"device status {int(c.status.item())} after the timed steps")
 
-    tokens_per_layer_step = [int(lens_at[W + i].sum()) for i in range(K)]
+    tokens_per_layer_step = [int(l.sum()) for l in lens_at]
     local_tokens = float(sum(tokens_per_layer_step)) * layers      # context tokens attended, all layers
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     total_tokens = sum_over_ranks(local_tokens, world, device)
     # tokens/s/layer = (tokens one layer attends) / (step time / layers)
     value = total_tokens / (elapsed_ms / 1e3)
-    attn_avg_s = statistics.mean(attn_ms) / 1e3
-    bytes_avg = statistics.mean(decode_bytes(lens_at[W + i], w) for i in range(K))
-    attn_tokens_per_s = statistics.mean(tokens_per_layer_step) / attn_avg_s
+    bytes_avg = decode_bytes(final_lens, w)
+    attn_tokens_per_s = float(final_lens.sum()) / attn_avg_s
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, W, stream, world, device)
+        e2e = run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, max_len, final_lens, world, device)
 
     return dict(value=value, elapsed_ms=elapsed_ms, attn_avg_s=attn_avg_s, bytes_avg=bytes_avg,
-                attn_tokens_per_s=attn_tokens_per_s, clocks=clocks, launches=launches,
-                mean_ctx=float(np.mean([lens_at[W + i].mean() for i in range(K)])), e2e=e2e, prefill=prefill,
+                attn_tokens_per_s=attn_tokens_per_s, clocks=clocks, launches=launches_per_step * K,
+                mean_ctx=float(np.mean([l.mean() for l in lens_at])), e2e=e2e, prefill=prefill,
                 cache_bytes=sum(c.blocks.numel() + 4 * c.k_res.numel() for c in caches))
 
 
-def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, W, stream, world, device):
-    """Same steps through the same C ABI, but every step's inputs start in
-    pinned host memory and every output is read back to pinned host memory
-    inside the timed region.  The caches continue from where the device-only
-    run left them (they keep growing by one token per step)."""
+def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, max_len, lens0, world, device):
+    """The same steps through the same C ABI, called eagerly as a user would,
+    with every step's inputs (new K/V token and query of every layer) copied
+    from pinned host memory and every output copied back to pinned host
+    memory inside the timed region.  The caches continue from their current
+    state (one more token per step)."""
     pool = len(k_new)
     h_k = [[(k.cpu().pin_memory(), v.cpu().pin_memory()) for (k, v) in row] for row in k_new]
     h_q = [[q.cpu().pin_memory() for q in row] for row in qs]
@@ -375,12 +399,8 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, 
     d_k = [torch.empty_like(k_new[0][0][0]) for _ in range(layers)]
     d_v = [torch.empty_like(k_new[0][0][1]) for _ in range(layers)]
     d_q = [torch.empty_like(qs[0][0]) for _ in range(layers)]
-    base = K + W   # steps already appended
-    n_steps = min(K, 20)
-    lens = [pre + 1 + base + i for i in range(n_steps)]
-    need = max(kvq.kv_decode_workspace_bytes(caches[0], w.q_heads, int(l.max())) for l in lens)
-    if need > ws.numel():
-        ws = torch.empty(need, dtype=torch.uint8, device=device)
+    n_steps = 20
+    lens = [lens0 + 1 + i for i in range(n_steps)]
     h2d = d2h = 0
     barrier(world)
     torch.cuda.synchronize()
@@ -391,8 +411,8 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, 
             d_k[l].copy_(h_k[p][l][0], non_blocking=True)
             d_v[l].copy_(h_k[p][l][1], non_blocking=True)
             d_q[l].copy_(h_q[p][l], non_blocking=True)
-            kvq.kv_quant_append(caches[l], d_k[l], d_v[l], ones, 1, stream=stream)
-            kvq.kv_decode_attn(caches[l], d_q[l], outs[l], ws, int(lens[i].max()), stream=stream)
+            kvq.kv_quant_append(caches[l], d_k[l], d_v[l], ones, 1)
+            kvq.kv_decode_attn(caches[l], d_q[l], outs[l], ws, max_len)
             h_out[l].copy_(outs[l], non_blocking=True)
             if i == 0:
                 h2d += 2 * d_k[l].numel() * 2 + d_q[l].numel() * 2
@@ -402,7 +422,7 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, lens_at, pre, K, 
     elapsed = max_over_ranks(elapsed, world, device)
     tokens = sum_over_ranks(float(sum(int(l.sum()) for l in lens)) * layers, world, device)
     return {"value": tokens / elapsed, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n_steps, "timer": "host perf_counter around enqueue + synchronize"}
+            "steps": n_steps, "timer": "host perf_counter around eager calls + copies + synchronize"}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -534,7 +554,8 @@ def main():
         "data": "synthetic", "config": dict(config, mean_ctx_timed=r["mean_ctx"]),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "kv_decode_attn (split + merge)", "peak_source": which,
+                     "kernel": "decode_kernel (one per kv_decode_attn call)", "peak_source": which,
+                     "timing": "CUDA events around K replays of a graph of 32 kv_decode_attn calls",
                      "algorithmic_bytes_per_call": r["bytes_avg"], "call_us": r["attn_avg_s"] * 1e6},
         "attn_only": {"value": r["attn_tokens_per_s"], "unit": UNIT},
         "quantize": {"kernel": "kv_quant_append (prefill of one layer)",
@@ -546,6 +567,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
         "gpu_launches": r["launches"],
+        "timing": "CUDA events around K replays of CUDA graphs, one graph per decode step",
         "clocks": r["clocks"],
     }
     print(json.dumps(line, default=_json_default))

@@ -6,13 +6,16 @@
 // dequantization); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV
 // Cache", second and third paragraphs (what the groups and the window hold).
 //
-// One CTA handles one split (a run of `chunk` groups, or the sink + window
-// tail) of one (sequence, KV head) for all query heads of that KV head.  A
-// producer warp streams the split's blocks into a shared-memory ring with
-// bulk copies; four consumer warps take one group each per stage.  The CTA
-// that finishes last for a (sequence, KV head) merges every split's
-// (max, sum, output) with a log-sum-exp and writes the fp16 output, so one
-// call is one kernel (plus a RoPE table kernel for pre-RoPE keys).
+// The kernel is persistent and every warp is its own streaming engine: a
+// warp takes work items (a run of `chunk` packed groups of one (sequence, KV
+// head), or that pair's fp16 sink + window tokens) from a global counter,
+// keeps a small ring of group blocks in flight with one-dimensional bulk
+// copies completing on per-slot mbarriers, and already fetches the next
+// item's first groups while it finishes the current one.  Each item leaves a
+// partial (max, sum, unnormalized output) per query head; the warp that
+// finishes the last item of a (sequence, KV head) merges them with a
+// log-sum-exp and writes the fp16 output.  No CTA-wide synchronization
+// happens after start-up.
 //
 // Scores over a group use mma.sync m16n8k16 with the 32 tokens as M, the
 // channels as K and the query as N: the A operand comes straight from the
@@ -33,11 +36,8 @@
 
 namespace kvq {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStageGroups = kConsumerWarps;  // one group per consumer warp per stage
-constexpr int kRopeOffStride = 65;            // padded row of the in-group rotation table
-constexpr int kMergeChunk = 512;              // split weights staged per pass of the final merge
+constexpr int kWarps = 4;              // independent warps per CTA
+constexpr int kRopeOffStride = 65;     // padded row of the in-group rotation table
 constexpr unsigned kFull = 0xffffffffu;
 
 struct DecodeArgs {
@@ -48,33 +48,35 @@ struct DecodeArgs {
   float zscale;             // softmax scale * log2(e)
   float *part_o;            // [S][Hq][nsp][D]
   float2 *part_ml;          // [S][Hq][nsp] (max, sum) in log2 units
-  int *counters;            // [S][Hkv] splits finished, zeroed before the launch
-  int nsp;
-  int chunk;                // groups per split
-  int max_len;              // host bound on seq_len the grid and tables were sized for
+  int *counters;            // [S][Hkv] items finished, zeroed before the launch
+  int *work;                // next work item, zeroed before the launch
+  int items;                // S * Hkv * nsp
+  int nsp;                  // items per (sequence, KV head): window passes + chunks
+  int tail_passes;          // window/sink items per (sequence, KV head), 32 tokens each
+  int chunk;                // groups per item
+  int max_len;              // host bound on seq_len the plan was sized for
   const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
   const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
 };
 
-template <int BITS>
-struct Stages {
-  static constexpr int n = BITS == 2 ? 4 : 2;
-};
+// Shared memory of one warp: a ring of NS group blocks, one mbarrier per
+// slot, and the query of the current item (fp32, up to 4 heads).
+// Ring slots (group blocks in flight) per warp.
+#ifndef KVQ_DECODE_RING_2BIT
+#define KVQ_DECODE_RING_2BIT 3
+#endif
+#ifndef KVQ_DECODE_RING_4BIT
+#define KVQ_DECODE_RING_4BIT 2
+#endif
 
-template <int BITS, int NSTAGES>
-struct DecSmem {
+template <int BITS>
+struct WarpSmem {
   static constexpr int BB = block_bytes(BITS);
-  static constexpr int STAGE = kStageGroups * BB;
-  static constexpr int BAR_OFF = NSTAGES * STAGE;
-  static constexpr int Q_OFF = BAR_OFF + 2 * NSTAGES * 8;
-  static constexpr int RED_OFF = Q_OFF + 4 * kD * 4;  // q for up to 4 heads
-  static constexpr int ROPE_OFF = RED_OFF + 16 * 4;   // block-reduction scratch + flag
-  static constexpr int BYTES_NOROPE = ROPE_OFF;
-  static constexpr int BYTES_ROPE = ROPE_OFF + kG * kRopeOffStride * 8;
-  // aliases of the ring once every stage is consumed: per-warp states, then
-  // the merge weights
-  static constexpr int MRG_BYTES = kConsumerWarps * 4 * (2 + kD) * 4;
-  static_assert(STAGE * NSTAGES >= MRG_BYTES + kMergeChunk * 4, "merge area does not fit the ring");
+  static constexpr int NS = BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT;
+  static constexpr int BAR_OFF = NS * BB;
+  static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
+  static constexpr int BYTES = (Q_OFF + 4 * kD * 4 + 127) / 128 * 128;
+  static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
 };
 
 // Post-scale of a key score row tau (0..3 = token 8*tau + g) and of a value
@@ -278,463 +280,547 @@ __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, int kt, i
   return reinterpret_cast<const uint32_t *>(kc)[((w >> 2) * 32 + lane) * 4 + (w & 3)];
 }
 
-// Block-wide max / sum over the CTA's threads (red: 8 floats of smem).
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float o = __shfl_xor_sync(kFull, v, off);
-    v = is_max ? fmaxf(v, o) : v + o;
+// Per-warp decode work item of one (sequence, KV head).  Its items are
+// numbered split = 0 .. nsp-1: the first `tail_passes` cover the fp16 sink +
+// window tokens 32 at a time (scheduled first: they are the slowest per
+// byte), the rest are runs of `chunk` packed groups.  kind: 1 = groups
+// [g0, g0+ng); 2 = window/sink tokens [32*split, 32*split + 32); 3 = zero the
+// output rows (empty sequence, or length out of range); 0 = nothing to do;
+// -1 = past the end.  nparts = partial results the (sequence, KV head)
+// produces in total.
+struct Item {
+  int s, h, split, kind, g0, ng, tparts, nparts;
+  Split spl;
+};
+
+__device__ __forceinline__ Item item_of(const DecodeArgs &a, int it) {
+  Item x;
+  x.kind = -1;
+  x.s = x.h = x.split = x.g0 = x.ng = x.tparts = x.nparts = 0;
+  x.spl.nsink = x.spl.Lq = x.spl.r = 0;
+  if (it >= a.items) return x;
+  const int per_s = a.geo.H * a.nsp;
+  x.s = it / per_s;
+  const int rem = it - x.s * per_s;
+  x.h = rem / a.nsp;
+  x.split = rem - x.h * a.nsp;
+  const int L = a.geo.seq_len[x.s];
+  x.kind = 0;
+  if (L <= 0 || L > a.geo.capacity || L > a.max_len) {
+    if (x.split == 0) x.kind = 3;
+    return x;
   }
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  v = red[0];
-  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-  return v;
+  x.spl = split_len(L, a.geo.ns, a.geo.R);
+  const int ng_all = x.spl.Lq / kG;
+  const int nchunks = (ng_all + a.chunk - 1) / a.chunk;
+  x.tparts = (x.spl.nsink + x.spl.r + 31) / 32;
+  x.nparts = x.tparts + nchunks;
+  if (x.split < a.tail_passes) {
+    if (x.split < x.tparts) x.kind = 2;
+  } else {
+    const int c = x.split - a.tail_passes;
+    if (c < nchunks) {
+      x.kind = 1;
+      x.g0 = c * a.chunk;
+      x.ng = min(a.chunk, ng_all - x.g0);
+    }
+  }
+  return x;
 }
 
-template <int BITS, int GQ, bool ROPE, int NSTAGES>
-__global__ void __launch_bounds__(kDecThreads, ROPE ? 2 : (GQ == 4 ? 3 : 4)) decode_split_kernel(DecodeArgs a) {
-  using SM = DecSmem<BITS, NSTAGES>;
-  constexpr int BB = SM::BB;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *ring = smem;
-  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + SM::BAR_OFF);
-  uint64_t *empty_bar = full_bar + NSTAGES;
-  float *q_s = reinterpret_cast<float *>(smem + SM::Q_OFF);           // [GQ][D]
-  float *red = reinterpret_cast<float *>(smem + SM::RED_OFF);         // [16]
-  float2 *roff_s = reinterpret_cast<float2 *>(smem + SM::ROPE_OFF);   // [32][65]
-  float *mrg_m = reinterpret_cast<float *>(smem);                      // [4][GQ]
-  float *mrg_l = mrg_m + kConsumerWarps * GQ;                          // [4][GQ]
-  float *mrg_o = mrg_l + kConsumerWarps * GQ;                          // [4][GQ][D]
-  float *wts = reinterpret_cast<float *>(smem + SM::MRG_BYTES);        // [kMergeChunk]
+// Scores of one packed group for this lane: z[tau] = log2-domain logit of
+// token 8*tau + g for query head q.
+template <int BITS, int GQ>
+__device__ __forceinline__ void group_scores(const uint8_t *blk, const QkOperand<GQ> &qo, const float (&kfac)[4],
+                                             int lane, float (&z)[4]) {
+  uint32_t bq[8][2];
+  float beta;
+  qo.build(reinterpret_cast<const float *>(blk + off_ks(BITS)), reinterpret_cast<const float *>(blk + off_km(BITS)),
+           lane, bq, beta);
+  float acc[2][4];
+  qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) z[2 * mt + hh] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[2 * mt + hh], beta);
+}
 
-  const Geo &geo = a.geo;
-  const int s = blockIdx.z, h = blockIdx.y, sp = blockIdx.x;
-  const int L = geo.seq_len[s];
-  const size_t orow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * kD;
-  if (L < 0 || L > geo.capacity || L > a.max_len) {
-    if (sp == 0) {
-      for (int i = threadIdx.x; i < GQ * kD; i += blockDim.x) a.out[orow0 + i] = __float2half_rn(0.f);
-      if (L > a.max_len && h == 0 && threadIdx.x == 0) set_status(geo.status, KVQ_STATUS_MAX_LEN);
+// o += values of one group weighted by ps (score layout: token 8*tau + g,
+// head q).  The value mma's B column h carries head h's p_t * scale_t as one
+// fp16 (its rounding error, at most 2^-11 relative per weight, enters the
+// output linearly); o columns 2q and 2q+1 of this lane are heads 2q, 2q+1.
+template <int BITS>
+__device__ __forceinline__ void group_values(const uint8_t *blk, const float (&ps)[4], int lane, float (&o)[8][4]) {
+  const int q = lane & 3, gcol = lane >> 2;
+  uint32_t bp[2][2];
+#pragma unroll
+  for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + gcol) & 31);
+      const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + gcol) & 31);
+      bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
     }
-    return;
-  }
-  const Split spl = split_len(L, geo.ns, geo.R);
-  const int ng = spl.Lq / kG;
-  const int nchunks = (ng + a.chunk - 1) / a.chunk;
-  if (sp > nchunks) return;
-  const bool tail = (sp == nchunks);
+  pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
+}
 
+// Scale the o columns of heads 2q and 2q+1 by their softmax rescale factors.
+__device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_hi) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    o[i][0] *= a_lo;
+    o[i][1] *= a_hi;
+    o[i][2] *= a_lo;
+    o[i][3] *= a_hi;
+  }
+}
+
+template <int BITS, int GQ, bool ROPE>
+__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) decode_kernel(DecodeArgs a) {
+  using WS = WarpSmem<BITS>;
+  constexpr int NS = WS::NS, BB = WS::BB;
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
+  uint8_t *ring = smem + warp * WS::BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + WS::BAR_OFF);
+  float *q_s = reinterpret_cast<float *>(ring + WS::Q_OFF);              // [GQ][D]
+  float2 *roff_s = reinterpret_cast<float2 *>(smem + kWarps * WS::BYTES);  // [32][65]
+  const Geo &geo = a.geo;
 
-  for (int i = threadIdx.x; i < GQ * kD; i += blockDim.x) q_s[i] = __half2float(a.q[orow0 + i]);
   if (ROPE) {
     for (int i = threadIdx.x; i < kG * 64; i += blockDim.x)
       roff_s[(i >> 6) * kRopeOffStride + (i & 63)] = a.rope_off[i];
   }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGES; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], kConsumerWarps);
-    }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  __syncthreads();  // the only CTA-wide barrier: from here each warp runs alone
 
-  // Running softmax state of this lane: query head q of the output layout.
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f, mu_run = 0.f;
   const bool head_valid = q < GQ;
-  const float col_lo = static_cast<float>(g & 1);  // B column g: low part when odd
-  const int hc = g >> 1;                           // B column g: query head
+    uint32_t fseq = 0, cseq = 0;                     // ring groups issued / consumed
+  bool ok = true;
 
-  if (!tail) {
-    const int g0 = sp * a.chunk;
-    const int ngr = min(ng, g0 + a.chunk) - g0;
-    const int nst = (ngr + kStageGroups - 1) / kStageGroups;
-    const uint8_t *src = geo.blocks + ((static_cast<size_t>(s) * geo.H + h) * geo.max_groups + g0) * BB;
-    if (warp == kConsumerWarps) {
-      // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        int issued = 0;
-        for (int k = 0; k < nst; ++k) {
-          const int slot = k % NSTAGES;
-          if (k >= NSTAGES && !mbar_wait_bounded(&empty_bar[slot], ((k / NSTAGES) - 1) & 1)) {
-            set_status(geo.status, KVQ_STATUS_TIMEOUT);
-            break;
-          }
-          const int cnt = min(kStageGroups, ngr - k * kStageGroups);
-          mbar_arrive_expect_tx(&full_bar[slot], cnt * BB);
-          bulk_g2s(ring + slot * SM::STAGE, src + static_cast<size_t>(k) * SM::STAGE, cnt * BB, &full_bar[slot]);
-          issued = k + 1;
-        }
-        // let every copy still in flight land before the ring is reused
-        for (int k = max(0, issued - NSTAGES); k < issued; ++k)
-          if (!mbar_wait_bounded(&full_bar[k % NSTAGES], (k / NSTAGES) & 1)) set_status(geo.status, KVQ_STATUS_TIMEOUT);
+#ifndef KVQ_DECODE_STATIC
+#define KVQ_DECODE_STATIC 0
+#endif
+  int k_static = 0;
+  auto grab = [&]() {
+    int it = 0;
+    if (KVQ_DECODE_STATIC) {
+      it = (blockIdx.x * kWarps + warp) + (k_static++) * static_cast<int>(gridDim.x * kWarps);
+    } else if (lane == 0) {
+      it = atomicAdd(a.work, 1);
+    }
+    return it;
+  };
+  Item cur = item_of(a, __shfl_sync(kFull, grab(), 0)), nxt;
+  int cur_fetched = 0, nxt_fetched = 0;
+  bool have_nxt = false;
+  int nid = 0;
+
+  // issue the next group of `it` into the next ring slot (lane 0 issues)
+  auto issue = [&](const Item &it, int gidx) {
+    if (lane == 0) {
+      const uint32_t slot = fseq % NS;
+      const uint8_t *src =
+          geo.blocks + ((static_cast<size_t>(it.s) * geo.H + it.h) * geo.max_groups + it.g0 + gidx) * BB;
+      fence_proxy_async();  // generic reads of the slot before the async write
+      mbar_arrive_expect_tx(&full[slot], BB);
+      bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
+    }
+    ++fseq;
+  };
+  auto top_up = [&]() {
+    while (fseq - cseq < static_cast<uint32_t>(NS)) {
+      if (cur.kind == 1 && cur_fetched < cur.ng) {
+        issue(cur, cur_fetched++);
+      } else if (have_nxt && nxt.kind == 1 && nxt_fetched < nxt.ng) {
+        issue(nxt, nxt_fetched++);
+      } else {
+        break;
       }
-    } else if (!ROPE) {
-      // ------------------------------------------- consumer, tensor-core path
-      QkOperand<GQ> qo;
-      qo.init(q_s, lane, a.zscale);
-      float kfac[4];
-#pragma unroll
-      for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
+    }
+  };
+  top_up();
+  // the next item is claimed at the start of the current one and resolved
+  // (its lengths read, its first groups fetched) once the first groups of
+  // the current item are under way, so the claim's latency stays hidden
+  auto resolve = [&]() {
+    if (!have_nxt) {
+      nxt = item_of(a, __shfl_sync(kFull, nid, 0));
+      nxt_fetched = 0;
+      have_nxt = true;
+      top_up();
+    }
+  };
 
-      for (int k = 0; k < nst; ++k) {
-        const int slot = k % NSTAGES;
-        const int gi = k * kStageGroups + warp;
-        if (gi < ngr) {
-          if (!mbar_wait_bounded(&full_bar[slot], (k / NSTAGES) & 1)) {
-            set_status(geo.status, KVQ_STATUS_TIMEOUT);
-            break;
-          }
-          const uint8_t *blk = ring + slot * SM::STAGE + warp * BB;
-          const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
-          const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
-          uint32_t bq[8][2];
-          float beta;
-          qo.build(reinterpret_cast<const float *>(blk + off_ks(BITS)),
-                   reinterpret_cast<const float *>(blk + off_km(BITS)), lane, bq, beta);
-          float acc[2][4];
-          qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
-          float z[4];
+  while (cur.kind != -1) {
+    nid = grab();
+    if (cur.kind != 1 || ROPE) resolve();
+    const size_t orow0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ) * kD;
+    const size_t prow0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ) * a.nsp + cur.split;
+    if (cur.kind == 3) {
+      for (int i = lane; i < GQ * kD; i += 32) a.out[orow0 + i] = __float2half_rn(0.f);
+      if (lane == 0 && cur.h == 0 && geo.seq_len[cur.s] > a.max_len) set_status(geo.status, KVQ_STATUS_MAX_LEN);
+    } else if (cur.kind == 1 || cur.kind == 2) {
+      __syncwarp();  // the previous item's reads of q_s are done
+      for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
+      __syncwarp();
+      if (cur.kind == 1) {
+        // ---------------------------------------------------- quantized groups
+        float o[8][4];
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f, mu_run = 0.f;
+        if (!ROPE) {
+          QkOperand<GQ> qo;
+          qo.init(q_s, lane, a.zscale);
+          float kfac[4];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              z[2 * mt + hh] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[2 * mt + hh], beta);
-
-          // online softmax over the group's 32 tokens (8 lanes share head q)
-          float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-          const float m_new = fmaxf(m_run, mx);
-          const float alpha = exp2f(m_run - m_new);
-          float ps[4], psum = 0.f, mus = 0.f;
-#pragma unroll
-          for (int tau = 0; tau < 4; ++tau) {
-            const float p = exp2f(z[tau] - m_new);
-            psum += p;
-            ps[tau] = p * vs[8 * tau + g];
-            mus = fmaf(p, vm[8 * tau + g], mus);
-          }
-          l_run = fmaf(l_run, alpha, psum);
-          mu_run = fmaf(mu_run, alpha, mus);
-          m_run = m_new;
-          if (__any_sync(kFull, head_valid && alpha != 1.f)) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              o[i][0] *= alpha; o[i][1] *= alpha; o[i][2] *= alpha; o[i][3] *= alpha;
+          for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
+          // two groups (64 tokens) per iteration: independent score mmas, one
+          // softmax update, two value mmas
+          for (int gi = 0; gi < cur.ng; gi += 2) {
+            const bool two = gi + 1 < cur.ng;
+            const uint32_t sa = cseq % NS, sb = (cseq + 1) % NS;
+            if (!mbar_wait_bounded(&full[sa], (cseq / NS) & 1) ||
+                (two && !mbar_wait_bounded(&full[sb], ((cseq + 1) / NS) & 1))) {
+              ok = false;
+              break;
             }
-          }
-          // B operand of the value mma: tokens 16kt + 8j + 2q + e, head hc
-          uint32_t bp[2][2];
-#pragma unroll
-          for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + hc) & 31);
-              const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + hc) & 31);
-              bp[kt][j] = split_part(v0, v1, col_lo);
+            const uint8_t *ba = ring + sa * BB, *bb = ring + sb * BB;
+            float za[4], zb[4];
+            group_scores<BITS, GQ>(ba, qo, kfac, lane, za);
+            if (two) {
+              group_scores<BITS, GQ>(bb, qo, kfac, lane, zb);
+            } else {
+              zb[0] = zb[1] = zb[2] = zb[3] = -INFINITY;
             }
-          pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-      }
-    } else {
-      // ---------------------------------------- consumer, pre-RoPE keys path
-      // one lane per token: dequantize, rotate at the token's position, dot
-      float m_all[GQ];
+            float mx = fmaxf(fmaxf(fmaxf(za[0], za[1]), fmaxf(za[2], za[3])),
+                             fmaxf(fmaxf(zb[0], zb[1]), fmaxf(zb[2], zb[3])));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = fast_exp2(m_run - m_new);
+            const float *vsa = reinterpret_cast<const float *>(ba + off_vs(BITS));
+            const float *vma = reinterpret_cast<const float *>(ba + off_vm(BITS));
+            const float *vsb = reinterpret_cast<const float *>(bb + off_vs(BITS));
+            const float *vmb = reinterpret_cast<const float *>(bb + off_vm(BITS));
+            float psa[4], psb[4], psum = 0.f, mus = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
-      for (int k = 0; k < nst; ++k) {
-        const int slot = k % NSTAGES;
-        const int gi = k * kStageGroups + warp;
-        if (gi < ngr) {
-          if (!mbar_wait_bounded(&full_bar[slot], (k / NSTAGES) & 1)) {
-            set_status(geo.status, KVQ_STATUS_TIMEOUT);
-            break;
+            for (int tau = 0; tau < 4; ++tau) {
+              const float pa = fast_exp2(za[tau] - m_new);
+              psum += pa;
+              psa[tau] = pa * vsa[8 * tau + g];
+              mus = fmaf(pa, vma[8 * tau + g], mus);
+            }
+            if (two) {
+#pragma unroll
+              for (int tau = 0; tau < 4; ++tau) {
+                const float pb = fast_exp2(zb[tau] - m_new);
+                psum += pb;
+                psb[tau] = pb * vsb[8 * tau + g];
+                mus = fmaf(pb, vmb[8 * tau + g], mus);
+              }
+            }
+            l_run = fmaf(l_run, alpha, psum);
+            mu_run = fmaf(mu_run, alpha, mus);
+            m_run = m_new;
+            if (__any_sync(kFull, head_valid && alpha != 1.f))
+              rescale_o(o, __shfl_sync(kFull, alpha, (2 * q) & 31), __shfl_sync(kFull, alpha, (2 * q + 1) & 31));
+            group_values<BITS>(ba, psa, lane, o);
+            if (two) group_values<BITS>(bb, psb, lane, o);
+            resolve();
+            __syncwarp();
+            cseq += two ? 2 : 1;
+            top_up();
           }
-          const uint8_t *blk = ring + slot * SM::STAGE + warp * BB;
-          const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
-          const float *km = reinterpret_cast<const float *>(blk + off_km(BITS));
-          const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
-          const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
-          const uint8_t *kc = blk + off_kc(BITS);
-          const float2 *base = a.rope_base + static_cast<size_t>(g0 + gi) * 64;
-          const int t = lane;
-          const int u = (t >> 3) % (8 / BITS);
-          float dot[GQ];
+        } else {
+          // pre-RoPE keys: one lane per token, dequantize, rotate, dot
+          float m_all[GQ];
 #pragma unroll
-          for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
+          for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
+          for (int gi = 0; gi < cur.ng; ++gi) {
+            const uint32_t slot = cseq % NS;
+            if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1)) {
+              ok = false;
+              break;
+            }
+            const uint8_t *blk = ring + slot * BB;
+            const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
+            const float *km = reinterpret_cast<const float *>(blk + off_km(BITS));
+            const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
+            const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
+            const uint8_t *kc = blk + off_kc(BITS);
+            const float2 *base = a.rope_base + static_cast<size_t>(cur.g0 + gi) * 64;
+            const int t = lane;
+            const int u = (t >> 3) % (8 / BITS);
+            float dot[GQ];
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
 #pragma unroll 1
-          for (int kt = 0; kt < 4; ++kt) {
+            for (int kt = 0; kt < 4; ++kt) {
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const uint32_t wa = key_word<BITS>(kc, t, kt, qq);
-              const uint32_t wb = key_word<BITS>(kc, t, kt + 4, qq);
+              for (int qq = 0; qq < 4; ++qq) {
+                const uint32_t wa = key_word<BITS>(kc, t, kt, qq);
+                const uint32_t wb = key_word<BITS>(kc, t, kt + 4, qq);
 #pragma unroll
-              for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int ch = 16 * kt + 8 * j + 2 * qq + e;
-                  const int sh = 16 * e + 8 * j + BITS * u;
-                  const float ca = static_cast<float>((wa >> sh) & ((1u << BITS) - 1u));
-                  const float cb = static_cast<float>((wb >> sh) & ((1u << BITS) - 1u));
-                  const float k1 = fmaf(ca, ks[ch], km[ch]);
-                  const float k2 = fmaf(cb, ks[ch + 64], km[ch + 64]);
-                  const float2 bs = base[ch];
-                  const float2 of = roff_s[t * kRopeOffStride + ch];
+                  for (int e = 0; e < 2; ++e) {
+                    const int ch = 16 * kt + 8 * j + 2 * qq + e;
+                    const int sh = 16 * e + 8 * j + BITS * u;
+                    const float ca = static_cast<float>((wa >> sh) & ((1u << BITS) - 1u));
+                    const float cb = static_cast<float>((wb >> sh) & ((1u << BITS) - 1u));
+                    const float k1 = fmaf(ca, ks[ch], km[ch]);
+                    const float k2 = fmaf(cb, ks[ch + 64], km[ch + 64]);
+                    const float2 bs = base[ch];
+                    const float2 of = roff_s[t * kRopeOffStride + ch];
+                    const float cs = bs.x * of.x - bs.y * of.y;
+                    const float sn = bs.y * of.x + bs.x * of.y;
+                    const float r1 = k1 * cs - k2 * sn;
+                    const float r2 = k2 * cs + k1 * sn;
+#pragma unroll
+                    for (int hh = 0; hh < GQ; ++hh)
+                      dot[hh] = fmaf(q_s[hh * kD + ch], r1, fmaf(q_s[hh * kD + ch + 64], r2, dot[hh]));
+                  }
+              }
+            }
+            const float vsc = vs[t], vmn = vm[t];
+            float ps[GQ];
+            float alpha_q = 1.f, psum_q = 0.f, mus_q = 0.f, m_q = m_run, a_lo = 1.f, a_hi = 1.f;
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              const float zz = dot[hh] * a.zscale;
+              float mx = zz;
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+              const float m_new = fmaxf(m_all[hh], mx);
+              const float alpha = fast_exp2(m_all[hh] - m_new);
+              m_all[hh] = m_new;
+              const float p = fast_exp2(zz - m_new);
+              ps[hh] = p * vsc;
+              float pl = p, pm = p * vmn;
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) {
+                pl += __shfl_xor_sync(kFull, pl, off);
+                pm += __shfl_xor_sync(kFull, pm, off);
+              }
+              if (hh == q) {
+                alpha_q = alpha;
+                psum_q = pl;
+                mus_q = pm;
+                m_q = m_new;
+              }
+              if (hh == 2 * q) a_lo = alpha;
+              if (hh == 2 * q + 1) a_hi = alpha;
+            }
+            l_run = fmaf(l_run, alpha_q, g == 0 ? psum_q : 0.f);
+            mu_run = fmaf(mu_run, alpha_q, g == 0 ? mus_q : 0.f);
+            m_run = m_q;
+            rescale_o(o, a_lo, a_hi);
+            uint32_t bp[2][2];
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                  const float a0 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q);
+                  const float a1 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q + 1);
+                  if (hh == g) {
+                    v0 = a0;
+                    v1 = a1;
+                  }
+                }
+                bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
+              }
+            pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
+            resolve();
+            __syncwarp();
+            ++cseq;
+            top_up();
+          }
+        }
+        if (!ok) break;
+        // this item's partial state per query head
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          l_run += __shfl_xor_sync(kFull, l_run, off);
+          mu_run += __shfl_xor_sync(kFull, mu_run, off);
+        }
+        {
+          const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            if (2 * q + c < GQ) {
+              float *po = a.part_o + (prow0 + static_cast<size_t>(2 * q + c) * a.nsp) * kD;
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                  po[16 * mt + 8 * rr + g] = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
+            }
+          }
+          if (head_valid && g == 0) a.part_ml[prow0 + static_cast<size_t>(q) * a.nsp] = make_float2(m_run, l_run);
+        }
+      } else {
+        // ------------------ 32 sink / window tokens, CUDA cores, one per lane
+        const int T = cur.spl.nsink + cur.spl.r;
+        const int t0 = 32 * cur.split;
+        const int nt = min(32, T - t0);
+        const size_t sh = static_cast<size_t>(cur.s) * geo.H + cur.h;
+        const int i = t0 + lane;
+        const bool valid = lane < nt;
+        float dot[GQ];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
+        if (valid) {
+          int pos;
+          const __half *kp;
+          if (i < cur.spl.nsink) {
+            pos = i;
+            kp = geo.k_sink + (sh * geo.ns + i) * kD;
+          } else {
+            const int slot = i - cur.spl.nsink;
+            pos = cur.spl.nsink + cur.spl.Lq + slot;
+            kp = geo.k_res + (sh * geo.R + slot) * kD;
+          }
+          const int sidx = pos - geo.ns;  // stream index (negative for the sink)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint4 ra[4], rb[4];  // channels 32*half + 8c.. and 64 + 32*half + 8c..
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              ra[c] = *reinterpret_cast<const uint4 *>(kp + 32 * half + 8 * c);
+              rb[c] = *reinterpret_cast<const uint4 *>(kp + 64 + 32 * half + 8 * c);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const __half *ha = reinterpret_cast<const __half *>(&ra[c]);
+              const __half *hb = reinterpret_cast<const __half *>(&rb[c]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int ch = 32 * half + 8 * c + e;
+                float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
+                if (ROPE && sidx >= 0) {
+                  const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
+                  const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
                   const float cs = bs.x * of.x - bs.y * of.y;
                   const float sn = bs.y * of.x + bs.x * of.y;
-                  const float r1 = k1 * cs - k2 * sn;
-                  const float r2 = k2 * cs + k1 * sn;
-#pragma unroll
-                  for (int hh = 0; hh < GQ; ++hh)
-                    dot[hh] = fmaf(q_s[hh * kD + ch], r1, fmaf(q_s[hh * kD + ch + 64], r2, dot[hh]));
+                  const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
+                  k1 = r1;
+                  k2 = r2;
                 }
-            }
-          }
-          const float vsc = vs[t], vmn = vm[t];
-          float ps[GQ];
-          float alpha_q = 1.f, psum_q = 0.f, mus_q = 0.f, m_q = m_run;
 #pragma unroll
-          for (int hh = 0; hh < GQ; ++hh) {
-            const float z = dot[hh] * a.zscale;
-            float mx = z;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-            const float m_new = fmaxf(m_all[hh], mx);
-            const float alpha = exp2f(m_all[hh] - m_new);
-            m_all[hh] = m_new;
-            const float p = exp2f(z - m_new);
-            ps[hh] = p * vsc;
-            float pl = p, pm = p * vmn;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-              pl += __shfl_xor_sync(kFull, pl, off);
-              pm += __shfl_xor_sync(kFull, pm, off);
-            }
-            if (hh == q) {
-              alpha_q = alpha;
-              psum_q = pl;
-              mus_q = pm;
-              m_q = m_new;
-            }
-          }
-          l_run = fmaf(l_run, alpha_q, g == 0 ? psum_q : 0.f);
-          mu_run = fmaf(mu_run, alpha_q, g == 0 ? mus_q : 0.f);
-          m_run = m_q;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            o[i][0] *= alpha_q; o[i][1] *= alpha_q; o[i][2] *= alpha_q; o[i][3] *= alpha_q;
-          }
-          uint32_t bp[2][2];
-#pragma unroll
-          for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-              for (int hh = 0; hh < GQ; ++hh) {
-                const float a0 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q);
-                const float a1 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q + 1);
-                if (hh == hc) {
-                  v0 = a0;
-                  v1 = a1;
-                }
+                for (int hh = 0; hh < GQ; ++hh)
+                  dot[hh] = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, dot[hh]));
               }
-              bp[kt][j] = split_part(v0, v1, col_lo);
             }
-          pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-      }
-    }
-  }
-  __syncthreads();  // ring free from here on: the merge area aliases it
-
-  if (!tail) {
-    if (warp < kConsumerWarps) {
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        l_run += __shfl_xor_sync(kFull, l_run, off);
-        mu_run += __shfl_xor_sync(kFull, mu_run, off);
-      }
-      if (head_valid) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int ch = 16 * mt + 8 * hh + g;
-            mrg_o[(warp * GQ + q) * kD + ch] =
-                fmaf(o[mt][2 * hh] + o[mt][2 * hh + 1], val_row_scale<BITS>(mt, hh), mu_run);
           }
-        if (g == 0) {
-          mrg_m[warp * GQ + q] = m_run;
-          mrg_l[warp * GQ + q] = l_run;
         }
-      }
-    }
-  } else if (warp < kConsumerWarps) {
-    // ------------------------------------------- sink + window, CUDA cores
-    const int T = spl.nsink + spl.r;
-    const int i = kG * warp + lane;
-    const bool valid = i < T;
-    const size_t sh = static_cast<size_t>(s) * geo.H + h;
-    int pos = 0;
-    const __half *kp = nullptr;
-    if (valid) {
-      if (i < spl.nsink) {
-        pos = i;
-        kp = geo.k_sink + (sh * geo.ns + i) * kD;
-      } else {
-        const int slot = i - spl.nsink;
-        pos = spl.nsink + spl.Lq + slot;
-        kp = geo.k_res + (sh * geo.R + slot) * kD;
-      }
-    }
-    float dot[GQ];
+        float p[GQ], mh[GQ], lh[GQ], acc[GQ][4];
 #pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
-    if (valid) {
-      const int sidx = pos - geo.ns;  // stream index (negative for the sink)
-#pragma unroll 1
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint4 ra = *reinterpret_cast<const uint4 *>(kp + c8 * 8);
-        const uint4 rb = *reinterpret_cast<const uint4 *>(kp + 64 + c8 * 8);
-        const __half *ha = reinterpret_cast<const __half *>(&ra);
-        const __half *hb = reinterpret_cast<const __half *>(&rb);
+        for (int hh = 0; hh < GQ; ++hh) {
+          const float zz = valid ? dot[hh] * a.zscale : -INFINITY;
+          float mx = zz;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int ch = c8 * 8 + e;
-          float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
-          if (ROPE && sidx >= 0) {
-            const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
-            const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
-            const float cs = bs.x * of.x - bs.y * of.y;
-            const float sn = bs.y * of.x + bs.x * of.y;
-            const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
-            k1 = r1;
-            k2 = r2;
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+          p[hh] = valid ? fast_exp2(zz - mx) : 0.f;
+          float sum = p[hh];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+          mh[hh] = mx;
+          lh[hh] = sum;
+          acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+        }
+        // values: lane holds channels 4*lane .. 4*lane+3; eight rows in flight
+        for (int tb = 0; tb < nt; tb += 8) {
+          uint2 raw[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int it = t0 + tb + u;
+            raw[u] = make_uint2(0u, 0u);
+            if (tb + u < nt) {
+              const __half *vp = it < cur.spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
+                                                    : geo.v_res + (sh * geo.R + (it - cur.spl.nsink)) * kD;
+              raw[u] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
+            }
           }
 #pragma unroll
-          for (int hh = 0; hh < GQ; ++hh)
-            dot[hh] = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, dot[hh]));
+          for (int u = 0; u < 8; ++u) {
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u].x));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u].y));
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              const float pt = __shfl_sync(kFull, p[hh], (tb + u) & 31);
+              acc[hh][0] = fmaf(pt, v01.x, acc[hh][0]);
+              acc[hh][1] = fmaf(pt, v01.y, acc[hh][1]);
+              acc[hh][2] = fmaf(pt, v23.x, acc[hh][2]);
+              acc[hh][3] = fmaf(pt, v23.y, acc[hh][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+          float *po = a.part_o + (prow0 + static_cast<size_t>(hh) * a.nsp) * kD;
+          *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+          if (lane == 0) a.part_ml[prow0 + static_cast<size_t>(hh) * a.nsp] = make_float2(mh[hh], lh[hh]);
         }
       }
-    }
-    float p[GQ], mh[GQ], lh[GQ];
+      // the last item of this (sequence, KV head) to finish merges them all;
+      // lane 0's acq_rel add publishes the warp's partial (ordered before it
+      // by the warp barrier) and observes every earlier item's
+      __syncwarp();
+      int last = 0;
+      if (lane == 0)
+        last = atom_add_acq_rel(&a.counters[static_cast<size_t>(cur.s) * geo.H + cur.h], 1) == cur.nparts - 1;
+      if (__shfl_sync(kFull, last, 0)) {
+        __threadfence();
+        for (int hh = 0; hh < GQ; ++hh) {
+          const size_t r0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ + hh) * a.nsp;
+          // partial i lives at split i (window passes) or tail_passes + i - tparts (chunks)
+          auto split_of = [&](int i) { return i < cur.tparts ? i : a.tail_passes + i - cur.tparts; };
+          float M = -INFINITY;
+          for (int i = lane; i < cur.nparts; i += 32) M = fmaxf(M, __ldcg(&a.part_ml[r0 + split_of(i)]).x);
 #pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) {
-      const float zz = valid ? dot[hh] * a.zscale : -INFINITY;
-      float mx = zz;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-      p[hh] = valid ? exp2f(zz - mx) : 0.f;
-      float sum = p[hh];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-      mh[hh] = mx;
-      lh[hh] = sum;
-    }
-    float acc[GQ][4];
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
-    const int nt = min(kG, T - kG * warp);
-    for (int t = 0; t < nt; ++t) {
-      const int it = kG * warp + t;
-      const __half *vp = it < spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
-                                        : geo.v_res + (sh * geo.R + (it - spl.nsink)) * kD;
-      const uint2 raw = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
-      const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-      const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) {
-        const float pt = __shfl_sync(kFull, p[hh], t);
-        acc[hh][0] = fmaf(pt, v01.x, acc[hh][0]);
-        acc[hh][1] = fmaf(pt, v01.y, acc[hh][1]);
-        acc[hh][2] = fmaf(pt, v23.x, acc[hh][2]);
-        acc[hh][3] = fmaf(pt, v23.y, acc[hh][3]);
-      }
-    }
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) {
-      *reinterpret_cast<float4 *>(&mrg_o[(warp * GQ + hh) * kD + 4 * lane]) =
-          make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-      if (lane == 0) {
-        mrg_m[warp * GQ + hh] = mh[hh];
-        mrg_l[warp * GQ + hh] = lh[hh];
-      }
-    }
-  }
-  __syncthreads();
-
-  // this split's (max, sum, unnormalized output) per query head
-  const size_t prow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * a.nsp;
-  for (int idx = threadIdx.x; idx < GQ * kD; idx += blockDim.x) {
-    const int hh = idx / kD, ch = idx % kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * GQ + hh]);
-    float Ls = 0.f, Os = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = mrg_m[w * GQ + hh];
-        if (mw != -INFINITY) {
-          const float f = exp2f(mw - M);
-          Ls = fmaf(mrg_l[w * GQ + hh], f, Ls);
-          Os = fmaf(mrg_o[(w * GQ + hh) * kD + ch], f, Os);
-        }
-      }
-    }
-    const size_t row = prow0 + static_cast<size_t>(hh) * a.nsp + sp;
-    a.part_o[row * kD + ch] = Os;
-    if (ch == 0) a.part_ml[row] = make_float2(M, Ls);
-  }
-
-  // the last split of this (sequence, KV head) to finish merges them all
-  __threadfence();
-  __syncthreads();
-  int *flag = reinterpret_cast<int *>(red + 8);
-  if (threadIdx.x == 0) *flag = atomicAdd(&a.counters[static_cast<size_t>(s) * geo.H + h], 1) == nchunks;
-  __syncthreads();
-  if (!*flag) return;
-  __threadfence();
-  const int nsplit = nchunks + 1;
-  for (int hh = 0; hh < GQ; ++hh) {
-    const size_t r0 = prow0 + static_cast<size_t>(hh) * a.nsp;
-    float M = -INFINITY;
-    for (int i = threadIdx.x; i < nsplit; i += blockDim.x) M = fmaxf(M, __ldcg(&a.part_ml[r0 + i]).x);
-    M = block_reduce(M, true, red);
-    float lpart = 0.f, acc = 0.f;
-    for (int c0 = 0; c0 < nsplit; c0 += kMergeChunk) {
-      const int n = min(kMergeChunk, nsplit - c0);
-      __syncthreads();  // the previous chunk's weights are consumed
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const float2 ml = __ldcg(&a.part_ml[r0 + c0 + i]);
-        const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-        wts[i] = wgt;
-        lpart = fmaf(ml.y, wgt, lpart);
-      }
-      __syncthreads();
-      if (threadIdx.x < kD) {
-        const float *po = a.part_o + (r0 + c0) * kD + threadIdx.x;
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (M != -INFINITY) {
 #pragma unroll 4
-        for (int i = 0; i < n; ++i) acc = fmaf(__ldcg(po + static_cast<size_t>(i) * kD), wts[i], acc);
+            for (int i = 0; i < cur.nparts; ++i) {
+              const size_t r = r0 + split_of(i);
+              const float2 ml = __ldcg(&a.part_ml[r]);
+              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + r * kD) + lane);
+              const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+              Ls = fmaf(ml.y, wgt, Ls);
+              acc.x = fmaf(ov.x, wgt, acc.x);
+              acc.y = fmaf(ov.y, wgt, acc.y);
+              acc.z = fmaf(ov.z, wgt, acc.z);
+              acc.w = fmaf(ov.w, wgt, acc.w);
+            }
+          }
+          const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
+          __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
+          op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+          op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        }
       }
     }
-    const float Ls = block_reduce(lpart, false, red);
-    if (threadIdx.x < kD)
-      a.out[orow0 + static_cast<size_t>(hh) * kD + threadIdx.x] = __float2half_rn(M == -INFINITY ? 0.f : acc / Ls);
+    resolve();
+    cur = nxt;
+    cur_fetched = nxt_fetched;
+    have_nxt = false;
+  }
+  if (!ok) {
+    set_status(geo.status, KVQ_STATUS_TIMEOUT);
+    // let this warp's copies still in flight land before it exits
+    for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
   }
 }
 
@@ -759,38 +845,47 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 // ---------------------------------------------------------------- host side
 
 template <int BITS, int GQ, bool ROPE>
-static cudaError_t launch_split_t(const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
-  constexpr int NST = Stages<BITS>::n;
-  using SM = DecSmem<BITS, NST>;
-  constexpr int bytes = ROPE ? SM::BYTES_ROPE : SM::BYTES_NOROPE;
-  auto kern = decode_split_kernel<BITS, GQ, ROPE, NST>;
-  static unsigned long long attr_set = 0;  // per instantiation: one bit per device ordinal
+static cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
+  using WS = WarpSmem<BITS>;
+  constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
+  auto kern = decode_kernel<BITS, GQ, ROPE>;
+  // per instantiation and device ordinal: attributes set, resident CTAs per SM
+  static int resident[64] = {};
+  static int sms[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set >> dev & 1ULL)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set |= 1ULL << dev;
+  int per_sm = dev < 64 ? resident[dev] : 0, n_sm = dev < 64 ? sms[dev] : 0;
+  if (per_sm == 0) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, bytes)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    per_sm = max(per_sm, 1);
+    if (dev < 64) {
+      resident[dev] = per_sm;
+      sms[dev] = n_sm;
+    }
   }
-  kern<<<grid, kDecThreads, bytes, stream>>>(a);
+  const long long want = (static_cast<long long>(a.items) + kWarps - 1) / kWarps;
+  const int grid = static_cast<int>(min(want, static_cast<long long>(n_sm) * per_sm));
+  kern<<<grid, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <int BITS, int GQ>
-static cudaError_t launch_split_g(const DecodeArgs &a, dim3 grid, cudaStream_t stream) {
-  return a.geo.pre_rope ? launch_split_t<BITS, GQ, true>(a, grid, stream)
-                        : launch_split_t<BITS, GQ, false>(a, grid, stream);
+static cudaError_t launch_g(const DecodeArgs &a, cudaStream_t stream) {
+  return a.geo.pre_rope ? launch_t<BITS, GQ, true>(a, stream) : launch_t<BITS, GQ, false>(a, stream);
 }
 
 template <int BITS>
-static cudaError_t launch_split_b(const DecodeArgs &a, int gq, dim3 grid, cudaStream_t stream) {
+static cudaError_t launch_b(const DecodeArgs &a, int gq, cudaStream_t stream) {
   switch (gq) {
-    case 1: return launch_split_g<BITS, 1>(a, grid, stream);
-    case 2: return launch_split_g<BITS, 2>(a, grid, stream);
-    default: return launch_split_g<BITS, 4>(a, grid, stream);
+    case 1: return launch_g<BITS, 1>(a, stream);
+    case 2: return launch_g<BITS, 2>(a, stream);
+    default: return launch_g<BITS, 4>(a, stream);
   }
 }
 
@@ -807,22 +902,28 @@ int set_decode_chunk(int groups) {
 DecodePlan plan_decode(const Geo &geo, int Hq, int max_len) {
   DecodePlan p;
   const Split sp = split_len(max_len, geo.ns, geo.R);
-  const int ng_max = sp.Lq / kG;
+  const long long ng_max = sp.Lq / kG;
   int chunk = g_chunk_override;
   if (chunk == 0) {
-    // about 32 groups (1024 tokens) per split, smaller when the (sequence,
-    // head) count alone cannot fill a few waves of the GPU
-    chunk = 32;
-    const long long pairs = static_cast<long long>(geo.S) * geo.H;
-    while (chunk > 8 && pairs * ((ng_max + chunk - 1) / chunk) < 4LL * 152 * 4) chunk /= 2;
+    // about six items per warp of a full GB300 (152 SMs x 16 warps) so the
+    // dynamic schedule balances, at least 8 groups per item, and at most
+    // ~512 items per (sequence, KV head) so the final merge stays short
+    const long long total = static_cast<long long>(geo.S) * geo.H * ng_max;
+    long long c = (total + 6LL * 152 * 16 - 1) / (6LL * 152 * 16);
+    c = max(c, (ng_max + 510) / 511);
+    c = min(max(c, 8LL), 1024LL);
+    chunk = static_cast<int>((c + 3) / 4 * 4);
   }
   p.chunk = chunk;
-  p.nsp = (ng_max + chunk - 1) / chunk + 1;
+  p.tail_passes = (geo.R - 1 + geo.ns + 31) / 32;
+  p.nsp = static_cast<int>((ng_max + chunk - 1) / chunk) + p.tail_passes;
+  p.items = static_cast<long long>(geo.S) * geo.H * p.nsp;
   p.n_base = geo.pre_rope ? (max(max_len - geo.ns, 1) + kG - 1) / kG : 0;
   const size_t rows = static_cast<size_t>(geo.S) * Hq * p.nsp;
   p.off_ml = align256(rows * kD * sizeof(float));
   p.off_cnt = p.off_ml + align256(rows * sizeof(float2));
-  p.off_base = p.off_cnt + align256(static_cast<size_t>(geo.S) * geo.H * sizeof(int));
+  p.cnt_bytes = (static_cast<size_t>(geo.S) * geo.H + 1) * sizeof(int);
+  p.off_base = p.off_cnt + align256(p.cnt_bytes);
   p.off_off = p.off_base + align256(static_cast<size_t>(p.n_base) * 64 * sizeof(float2));
   p.bytes = p.off_off + (geo.pre_rope ? align256(kG * 64 * sizeof(float2)) : 0);
   return p;
@@ -841,12 +942,15 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.part_o = reinterpret_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
   a.counters = reinterpret_cast<int *>(ws + p.off_cnt);
+  a.work = a.counters + static_cast<size_t>(geo.S) * geo.H;
+  a.items = static_cast<int>(p.items);
   a.nsp = p.nsp;
+  a.tail_passes = p.tail_passes;
   a.chunk = p.chunk;
   a.max_len = max_len;
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_base);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(geo.S) * geo.H * sizeof(int), stream);
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, p.cnt_bytes, stream);
   if (e != cudaSuccess) return e;
   if (geo.pre_rope) {
     const int n = (p.n_base + kG) * 64;
@@ -857,8 +961,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const int gq = Hq / geo.H;
-  dim3 grid(p.nsp, geo.H, geo.S);
-  e = geo.bits == 2 ? launch_split_b<2>(a, gq, grid, stream) : launch_split_b<4>(a, gq, grid, stream);
+  e = geo.bits == 2 ? launch_b<2>(a, gq, stream) : launch_b<4>(a, gq, stream);
   ++*launches;
   return e;
 }

@@ -62,6 +62,13 @@ __host__ __device__ inline Split split_len(int L, int ns, int R) {
   return sp;
 }
 
+// atomicAdd with acquire-release semantics at GPU scope; returns the old value.
+__device__ inline int atom_add_acq_rel(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ inline void set_status(int *status, int bit) {
   if (status) atomicOr(status, bit);
 }
@@ -101,16 +108,42 @@ __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the warp for up to `ns`
+// nanoseconds while the phase is incomplete (no spinning in the meantime).
+__device__ inline bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar`, giving up after about two seconds of SM
 // clock; returns false (and the caller records KVQ_STATUS_TIMEOUT) on timeout.
 __device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_hint(bar, parity, 100000u)) {
     if (clock64() - start > 4000000000LL) return false;
   }
   return true;
 }
+
+// 2^x on the special-function unit (approximate, flushes subnormal results
+// to zero; softmax weights that small do not matter).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Orders this thread's earlier generic-proxy accesses of shared memory
+// before its later async-proxy (bulk copy) accesses.
+__device__ inline void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // One-dimensional bulk copy global -> shared, completing on `bar`.
 __device__ inline void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
@@ -149,8 +182,9 @@ __device__ inline uint32_t hi_or_lo(float x0, float x1, bool want_lo) {
 // (partial outputs, partial (max, sum), per-(sequence, KV head) split
 // counters, RoPE tables), each 256-byte aligned.
 struct DecodePlan {
-  int chunk, nsp, n_base;
-  size_t off_ml, off_cnt, off_base, off_off, bytes;
+  int chunk, nsp, tail_passes, n_base;
+  long long items;
+  size_t off_ml, off_cnt, cnt_bytes, off_base, off_off, bytes;
 };
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
