@@ -50,15 +50,18 @@ def quantize_asymmetric(x, axis: int, bits: int):
     """Asymmetric b-bit quantization of fp16 `x`, one (scale, min) per slice
     taken along `axis`.
 
-    min/max are exact in fp32 (the inputs are fp16).  scale is
+    min/max are exact in fp32 (the inputs are fp16; a zero extreme is stored
+    as +0).  scale is
     fl32((max - min) / (2^b - 1)); code = clamp(rne(fl32(fl32(x - min) /
     scale)), 0, 2^b - 1), and a slice with max == min has scale 0 and all
     codes 0.  Returns (codes uint8 shaped like x, scale fp32, min fp32), the
     last two with `axis` removed.
     """
     x32 = np.asarray(x, dtype=np.float16).astype(np.float32)
-    mn = x32.min(axis=axis, keepdims=True)
-    mx = x32.max(axis=axis, keepdims=True)
+    # + 0 turns a -0 extreme into +0, so the stored min never depends on
+    # which of two equal zeros a reduction happened to return
+    mn = x32.min(axis=axis, keepdims=True) + np.float32(0)
+    mx = x32.max(axis=axis, keepdims=True) + np.float32(0)
     levels = np.float32(2 ** bits - 1)
     scale = (mx - mn) / levels                      # fp32 / fp32: one IEEE division
     assert scale.dtype == np.float32

@@ -409,3 +409,14 @@ def test_pre_rope_attention_equals_rotated_dense():
     np.testing.assert_allclose(got.astype(np.float64), want, rtol=2 ** -10, atol=2 ** -24)
     # and rotation changes the answer (it is not silently skipped)
     assert np.abs(c.attention(q, pre_rope=False)[0, 0].astype(np.float64) - want).max() > 1e-3
+
+
+def test_zero_extremes_are_stored_as_positive_zero():
+    """A slice whose min (or max) is a zero stores +0 whichever zero it saw."""
+    x = np.zeros((32, 128), np.float16)
+    x[:16, :] = np.float16(-0.0)
+    x[5, 7] = 1.0
+    c, s, m = oracle.quantize_key_group(x, 2)
+    assert not np.signbit(m).any() and not np.signbit(s).any()
+    c, s, m = oracle.quantize_value_tokens(-x, 2)
+    assert not np.signbit(m[16:]).any()
