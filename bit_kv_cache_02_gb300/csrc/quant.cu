@@ -9,18 +9,47 @@
 
 namespace kvq {
 
-// Code of one element: clamp(rne((x - mn) / scale), 0, 2^b - 1), each step an
-// IEEE fp32 operation; scale == 0 gives 0.
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, float mn, float scale) {
-  if (scale == 0.f) return 0u;
-  float y = __fdiv_rn(__fsub_rn(x, mn), scale);
-  float c = rintf(y);  // round half to even
-  c = fminf(fmaxf(c, 0.f), float((1 << BITS) - 1));
-  return static_cast<uint32_t>(c);
+constexpr int kQuantThreads = 256;
+constexpr float kMagic = 12582912.f;  // 1.5 * 2^23: x + kMagic rounds x to an integer (half to even)
+
+// Per-slice (one key channel of a group, or one value token) constants of
+// the code computation.  The code is rne(fl(fl(x - min) / scale)) clamped
+// to [0, 2^b - 1], scale == 0 giving 0.  It is first evaluated from
+// y' = fma(x, rcp, c) with rcp = fl(1/scale) and c = fl(-min * rcp), which
+// differs from both the exact quotient (x - min) / scale and the IEEE
+// result fl(fl(x - min) / scale) by less than half of `tol`
+// ((2^b) * 2^-23 + |c| * 2^-24 each, from the three roundings); when y'
+// lies farther than `tol` from every rounding boundary k + 1/2, all three
+// round to the same integer.  Otherwise the IEEE subtract and divide decide.
+struct SliceQ {
+  float rcp, c, tol, mn;
+};
+
+__device__ __forceinline__ SliceQ make_slice(float mn, float scale, float levels) {
+  SliceQ q;
+  q.mn = mn;
+  q.rcp = scale > 0.f ? __frcp_rn(scale) : 0.f;
+  q.c = __fmul_rn(-mn, q.rcp);
+  q.tol = (levels + 1.f) * 4.76837158203125e-07f + fabsf(q.c) * 2.384185791015625e-07f;  // 2^-21, 2^-22
+  return q;
 }
 
-constexpr int kQuantThreads = 256;
+// Fast code of x; `near` is set when y' is within tol of a rounding boundary.
+__device__ __forceinline__ uint32_t fast_code(float x, const SliceQ &q, bool &near) {
+  const float y = fmaf(x, q.rcp, q.c);
+  const float t = y + kMagic;
+  near = fabsf(fabsf(y - (t - kMagic)) - 0.5f) <= q.tol;
+  return __float_as_uint(t) - __float_as_uint(kMagic);
+}
+
+// The code by the IEEE subtract and divide (rarely needed, kept out of line).
+template <int BITS>
+__device__ __noinline__ uint32_t exact_code(float x, float mn, float scale) {
+  const float r = rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+  return static_cast<uint32_t>(fminf(fmaxf(r, 0.f), float((1 << BITS) - 1)));
+}
+
+constexpr int kVStride = kG + 2;  // padded row (in halves) of the transposed value tile
 
 // One CTA quantizes one 32-token group of one (sequence, KV head).
 // grid = (group slot, KV head, sequence).  Tokens of the group come from the
@@ -40,106 +69,147 @@ __global__ void __launch_bounds__(kQuantThreads) quant_flush_kernel(Geo geo, con
   if (gslot >= (Lq1 - Lq0) / kG) return;
   const int i0 = Lq0 + gslot * kG;  // first stream index of this group
 
-  __shared__ __align__(16) __half sk[kG][kD];
-  __shared__ __align__(16) __half sv[kG][kD];
-  __shared__ float k_sc[kD], k_mn[kD], v_sc[kG], v_mn[kG];
-
-  const size_t sh = static_cast<size_t>(s) * geo.H + h;
-  for (int idx = threadIdx.x; idx < kG * kD / 8; idx += kQuantThreads) {
-    const int t = idx / (kD / 8), c8 = idx % (kD / 8);
-    const int i = i0 + t;
-    const __half *pk, *pv;
-    if (i < n0) {
-      const size_t off = (sh * geo.R + (i - Lq0)) * kD;
-      pk = geo.k_res + off;
-      pv = geo.v_res + off;
-    } else {
-      const int j = i + geo.ns - L0;
-      const size_t off = (sh * max_new + j) * kD;
-      pk = k_new + off;
-      pv = v_new + off;
-    }
-    *reinterpret_cast<uint4 *>(&sk[t][c8 * 8]) = *reinterpret_cast<const uint4 *>(pk + c8 * 8);
-    *reinterpret_cast<uint4 *>(&sv[t][c8 * 8]) = *reinterpret_cast<const uint4 *>(pv + c8 * 8);
-  }
-  __syncthreads();
+  __shared__ __align__(16) __half sk[kG][kD];         // keys, token rows
+  __shared__ __align__(16) __half svT[kD][kVStride];  // values, channel rows
+  __shared__ __align__(16) SliceQ kq[kD];
+  __shared__ __align__(16) SliceQ vq[kG];
+  __shared__ float k_sc[kD], v_sc[kG];
 
   const float levels = float((1 << BITS) - 1);
+  const size_t sh = static_cast<size_t>(s) * geo.H + h;
   uint8_t *blk = geo.blocks + (sh * geo.max_groups + i0 / kG) * static_cast<size_t>(block_bytes(BITS));
-  if (threadIdx.x < kD) {  // keys: one channel per thread, min/max over the 32 tokens
-    const int d = threadIdx.x;
-    float mn = __half2float(sk[0][d]), mx = mn;
-#pragma unroll 8
-    for (int t = 1; t < kG; ++t) {
-      const float x = __half2float(sk[t][d]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+  {
+    // thread (p, c8): tokens 2p and 2p+1, channels 8 c8 .. 8 c8 + 7
+    const int p = threadIdx.x >> 4, c8 = threadIdx.x & 15;
+    uint4 kr[2], vr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = i0 + 2 * p + r;
+      const __half *pk, *pv;
+      if (i < n0) {
+        const size_t off = (sh * geo.R + (i - Lq0)) * kD;
+        pk = geo.k_res + off;
+        pv = geo.v_res + off;
+      } else {
+        const size_t off = (sh * max_new + (i + geo.ns - L0)) * kD;
+        pk = k_new + off;
+        pv = v_new + off;
+      }
+      kr[r] = *reinterpret_cast<const uint4 *>(pk + c8 * 8);
+      vr[r] = *reinterpret_cast<const uint4 *>(pv + c8 * 8);
     }
-    const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
-    k_sc[d] = sc;
-    k_mn[d] = mn;
-    reinterpret_cast<float *>(blk + off_ks(BITS))[d] = sc;
-    reinterpret_cast<float *>(blk + off_km(BITS))[d] = mn;
-  } else {  // values: warp w' takes tokens 8w'..8w'+7, min/max over 128 channels
-    const int w = (threadIdx.x - kD) >> 5, lane = threadIdx.x & 31;
-    for (int tt = 0; tt < kG / 4; ++tt) {
-      const int t = w * (kG / 4) + tt;
-      float mn = __half2float(sv[t][lane * 4]), mx = mn;
+    *reinterpret_cast<uint4 *>(&sk[2 * p][c8 * 8]) = kr[0];
+    *reinterpret_cast<uint4 *>(&sk[2 * p + 1][c8 * 8]) = kr[1];
+    const __half *va = reinterpret_cast<const __half *>(&vr[0]);
+    const __half *vb = reinterpret_cast<const __half *>(&vr[1]);
+    __half2 mn2 = __halves2half2(va[0], vb[0]), mx2 = mn2;
 #pragma unroll
-      for (int c = 1; c < 4; ++c) {
-        const float x = __half2float(sv[t][lane * 4 + c]);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
+    for (int c = 0; c < 8; ++c) {
+      const __half2 pair = __halves2half2(va[c], vb[c]);  // (token 2p, token 2p+1) of channel 8 c8 + c
+      *reinterpret_cast<__half2 *>(&svT[c8 * 8 + c][2 * p]) = pair;
+      mn2 = __hmin2(mn2, pair);
+      mx2 = __hmax2(mx2, pair);
+    }
+    // per-token min/max over the 16 lanes holding the token's 128 channels
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      if (lane == 0) {
-        const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
-        v_sc[t] = sc;
-        v_mn[t] = mn;
-        reinterpret_cast<float *>(blk + off_vs(BITS))[t] = sc;
-        reinterpret_cast<float *>(blk + off_vm(BITS))[t] = mn;
-      }
+    for (int o = 1; o < 16; o <<= 1) {
+      const uint32_t a = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mn2), o);
+      const uint32_t b = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mx2), o);
+      mn2 = __hmin2(mn2, *reinterpret_cast<const __half2 *>(&a));
+      mx2 = __hmax2(mx2, *reinterpret_cast<const __half2 *>(&b));
+    }
+    if (c8 < 2) {  // lane 0 of the pair finishes token 2p, lane 1 token 2p+1
+      const float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
+      // + 0 stores a zero extreme as +0 whichever zero the reduction kept
+      const float mn = __fadd_rn(c8 == 0 ? mnf.x : mnf.y, 0.f), mx = __fadd_rn(c8 == 0 ? mxf.x : mxf.y, 0.f);
+      const int t = 2 * p + c8;
+      const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
+      vq[t] = make_slice(mn, sc, levels);
+      v_sc[t] = sc;
+      reinterpret_cast<float *>(blk + off_vs(BITS))[t] = sc;
+      reinterpret_cast<float *>(blk + off_vm(BITS))[t] = mn;
     }
   }
   __syncthreads();
+  if (threadIdx.x < kD / 2) {  // keys: channels 2d, 2d+1, min/max over the 32 tokens (exact in fp16)
+    const int d = 2 * threadIdx.x;
+    __half2 mn2 = *reinterpret_cast<const __half2 *>(&sk[0][d]), mx2 = mn2;
+#pragma unroll 8
+    for (int t = 1; t < kG; ++t) {
+      const __half2 x = *reinterpret_cast<const __half2 *>(&sk[t][d]);
+      mn2 = __hmin2(mn2, x);
+      mx2 = __hmax2(mx2, x);
+    }
+    float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
+    mnf.x = __fadd_rn(mnf.x, 0.f);
+    mnf.y = __fadd_rn(mnf.y, 0.f);
+    mxf.x = __fadd_rn(mxf.x, 0.f);
+    mxf.y = __fadd_rn(mxf.y, 0.f);
+    const float sc0 = __fdiv_rn(__fsub_rn(mxf.x, mnf.x), levels);
+    const float sc1 = __fdiv_rn(__fsub_rn(mxf.y, mnf.y), levels);
+    kq[d] = make_slice(mnf.x, sc0, levels);
+    kq[d + 1] = make_slice(mnf.y, sc1, levels);
+    k_sc[d] = sc0;
+    k_sc[d + 1] = sc1;
+    reinterpret_cast<float2 *>(blk + off_ks(BITS))[threadIdx.x] = make_float2(sc0, sc1);
+    reinterpret_cast<float2 *>(blk + off_km(BITS))[threadIdx.x] = make_float2(mnf.x, mnf.y);
+  }
+  __syncthreads();
 
-  // Pack: word index t of a tile lives at byte 4t; t = (w/4)*128 + lane*4 + w%4.
-  constexpr int NU = 8 / BITS;           // fields per byte
+  // Pack: each thread builds whole 32-bit words.  Word index t' of a tile is
+  // stored at byte 4t' (coalesced), i.e. word w = 4(t'/128) + t'%4 of lane
+  // (t'/4)%32; its fields are (e, j, u) at bit 16e + 8j + b*u holding
+  // element (row, col) = (16 mt + 8 (tau%2) + g, 16 kt + 8 j + 2 q + e).
+  // Both tiles read their element pairs (e = 0, 1) as one half2: keys from
+  // token rows, values from the transposed channel rows.
+  constexpr int NU = 8 / BITS;                // fields per byte
   constexpr int WPL = kG * kD * BITS / 1024;  // words per lane
   for (int widx = threadIdx.x; widx < 2 * 32 * WPL; widx += kQuantThreads) {
-    const int tile = widx / (32 * WPL);  // 0: keys, 1: values
-    const int t = widx % (32 * WPL);
+    const bool keys = widx < 32 * WPL;
+    const int t = keys ? widx : widx - 32 * WPL;
     const int w = (t >> 7) * 4 + (t & 3);
     const int lane = (t >> 2) & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int KT = tile == 0 ? kD / 16 : kG / 16;
+    const int pk = w / (4 / NU);
+    const int kt = keys ? pk : (pk & 1);
+    const int mt0 = keys ? 0 : 2 * (pk >> 1);
+    const SliceQ *sq = keys ? kq : vq;
+    const float *ssc = keys ? k_sc : v_sc;
+    SliceQ sl[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) sl[j][e] = sq[16 * kt + 8 * j + 2 * q + e];
     uint32_t word = 0;
+    bool near = false;
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
       const int tau = (w % (4 / NU)) * NU + u;
-      const int pk = w / (4 / NU);
-      const int P = pk / KT, kt = pk % KT;
-      const int row = 16 * (2 * P + (tau >> 1)) + 8 * (tau & 1) + g;
+      const int row = 16 * (mt0 + (tau >> 1)) + 8 * (tau & 1) + g;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = 16 * kt + 8 * j + 2 * q + e;
-          uint32_t c;
-          if (tile == 0) {  // row = token, col = channel
-            c = quant_code<BITS>(__half2float(sk[row][col]), k_mn[col], k_sc[col]);
-          } else {  // row = channel, col = token
-            c = quant_code<BITS>(__half2float(sv[col][row]), v_mn[col], v_sc[col]);
-          }
-          word |= c << (16 * e + 8 * j + BITS * u);
-        }
+        const int col = 16 * kt + 8 * j + 2 * q;
+        const float2 x = __half22float2(keys ? *reinterpret_cast<const __half2 *>(&sk[row][col])
+                                             : *reinterpret_cast<const __half2 *>(&svT[row][col]));
+        bool n0f, n1f;
+        word |= fast_code(x.x, sl[j][0], n0f) << (8 * j + BITS * u);
+        word |= fast_code(x.y, sl[j][1], n1f) << (16 + 8 * j + BITS * u);
+        near |= n0f | n1f;
       }
     }
-    reinterpret_cast<uint32_t *>(blk + (tile == 0 ? off_kc(BITS) : off_vc(BITS)))[t] = word;
+    if (__any_sync(0xffffffffu, near) && near) {
+      // some field's fast code could differ from the IEEE one: redo the word
+      word = 0;
+      for (int f = 0; f < 4 * NU; ++f) {
+        const int u = f >> 2, j = (f >> 1) & 1, e = f & 1;
+        const int tau = (w % (4 / NU)) * NU + u;
+        const int row = 16 * (mt0 + (tau >> 1)) + 8 * (tau & 1) + g;
+        const int col = 16 * kt + 8 * j + 2 * q + e;
+        const float x = __half2float(keys ? sk[row][col] : svT[row][col]);
+        word |= exact_code<BITS>(x, sl[j][e].mn, ssc[col]) << (16 * e + 8 * j + BITS * u);
+      }
+    }
+    reinterpret_cast<uint32_t *>(blk + (keys ? off_kc(BITS) : off_vc(BITS)))[t] = word;
   }
 }
 

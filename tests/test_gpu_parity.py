@@ -257,3 +257,21 @@ def test_split_sizes_agree(kvq, chunk):
         _attn_close(_attend(kvq, cache, q, 1500), want)
     finally:
         kvq.set_decode_chunk(0)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_ties_and_near_ties_bit_exact(kvq, bits):
+    """Inputs on a half-step grid put many quotients exactly on rounding
+    boundaries (and fp16 neighbours just beside them); codes must match the
+    oracle's round-half-even of the IEEE quotient bit for bit."""
+    S, H, T = 2, 3, 256
+    rng = np.random.default_rng(40 + bits)
+    top = 2 ** bits - 1
+    k = (rng.integers(0, 2 * top + 1, (S, H, T, 128)) / 2.0).astype(np.float16)
+    v = (rng.integers(0, 2 * top + 1, (S, H, T, 128)) / 2.0).astype(np.float16)
+    # shift some slices by one fp16 ulp so quotients land just beside k + 1/2
+    k[:, :, ::3, ::5] = np.nextafter(k[:, :, ::3, ::5], np.float16(100))
+    v[:, 1] = (v[:, 1].astype(np.float32) * 0.3 - 7).astype(np.float16)
+    cache, orc = _build(kvq, S, H, 300, bits)
+    _append(kvq, cache, orc, k, v, [256, 256])
+    _compare_state(cache, orc)
