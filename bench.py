@@ -60,7 +60,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
-    p.add_argument("--chunk", type=int, default=0, help="groups per decode work item (0: library's choice)")
+    p.add_argument("--warps", type=int, default=0, help="warps a decode launch cuts its work into (0: library's choice)")
     return p.parse_args()
 
 
@@ -283,8 +283,8 @@ def run_ours(args, w, layers, rank, world, local):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    if args.chunk:
-        kvq.set_decode_chunk(args.chunk)
+    if args.warps:
+        kvq.set_decode_warps(args.warps)
     K, W = args.steps, args.warmup
     pool = max(1, min(4, K))
     pre = prefill_lengths(w, K, max(W, 1) + pool)

@@ -142,7 +142,6 @@ int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) softmax_scale = 1.f / sqrtf(static_cast<float>(kvq::kD));
   const kvq::Geo geo = make_geo(cache);
   const kvq::DecodePlan plan = kvq::plan_decode(geo, num_q_heads, max_len);
-  if (plan.items > 2147483647LL) return KVQ_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.bytes) return KVQ_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KVQ_ERR_ALIGNMENT;
   uint64_t n = 0;
@@ -177,6 +176,6 @@ const char *kvq_strerror(int err) {
 
 uint64_t kvq_launch_count(void) { return g_launches.load(); }
 
-int kvq_set_decode_chunk(int32_t groups) { return kvq::set_decode_chunk(groups) ? KVQ_ERR_INVALID_ARG : KVQ_OK; }
+int kvq_set_decode_warps(int32_t warps) { return kvq::set_decode_warps(warps) ? KVQ_ERR_INVALID_ARG : KVQ_OK; }
 
 }  // extern "C"

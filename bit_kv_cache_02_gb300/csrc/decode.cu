@@ -6,17 +6,20 @@
 // dequantization); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV
 // Cache", second and third paragraphs (what the groups and the window hold).
 //
-// The kernel is persistent and every warp is its own streaming engine: a
-// warp takes work items (a run of `chunk` packed groups of one (sequence, KV
-// head), or that pair's fp16 sink + window tokens) from a global counter,
-// keeps a small ring of group blocks in flight with one-dimensional bulk
-// copies completing on per-slot mbarriers, and already fetches the next
-// item's first groups while it finishes the current one.  Each item leaves a
-// partial (max, sum, unnormalized output) per query head; the warp that
-// finishes the last item of a (sequence, KV head) merges them with a
-// log-sum-exp and writes the fp16 output.  No CTA-wide synchronization
-// happens after start-up.
-//
+// The work of every (sequence, KV head) pair -- 32-token passes over its
+// fp16 sink + window tokens, then its packed groups -- is laid out as one
+// line of units, and each warp of a single wave of persistent CTAs takes an
+// equal, contiguous range of that line (stream-K): ranges cross pair
+// boundaries, so the split of each pair's token axis follows from the load
+// balance rather than from a fixed chunk size.  A warp streams its groups
+// through a small ring of shared-memory slots filled by one-dimensional bulk
+// copies completing on per-slot mbarriers, fetching across pair boundaries
+// so the next pair's first groups are in flight while the current one ends.
+// It leaves a partial (max, sum, unnormalized output) per query head for
+// each pair it touches; the warp that completes a pair's partial count
+// merges them with a log-sum-exp and writes the fp16 output.  No CTA-wide
+// synchronization happens after start-up.
+
 // Scores over a group use mma.sync m16n8k16 with the 32 tokens as M, the
 // channels as K and the query as N: the A operand comes straight from the
 // packed words (an AND mask leaves each code as an fp16 subnormal
@@ -40,20 +43,22 @@ constexpr int kWarps = 4;              // independent warps per CTA
 constexpr int kRopeOffStride = 65;     // padded row of the in-group rotation table
 constexpr unsigned kFull = 0xffffffffu;
 
+struct PlanHeader;
+
 struct DecodeArgs {
   Geo geo;
   int Hq;
   const __half *q;          // [S][Hq][D]
   __half *out;              // [S][Hq][D]
   float zscale;             // softmax scale * log2(e)
-  float *part_o;            // [S][Hq][nsp][D]
-  float2 *part_ml;          // [S][Hq][nsp] (max, sum) in log2 units
-  int *counters;            // [S][Hkv] items finished, zeroed before the launch
-  int *work;                // next work item, zeroed before the launch
-  int items;                // S * Hkv * nsp
-  int nsp;                  // items per (sequence, KV head): window passes + chunks
-  int tail_passes;          // window/sink items per (sequence, KV head), 32 tokens each
-  int chunk;                // groups per item
+  float *part_o;            // [slots][GQ][D] unnormalized partial outputs
+  float2 *part_ml;          // [slots][GQ] (max, sum) in log2 units
+  int *counters;            // [S][Hkv] partials finished, zeroed by the plan kernel
+  long long *base;          // [S + 1] first work unit of each sequence (plan kernel)
+  PlanHeader *plan;         // total work units (plan kernel)
+  int nw;                   // warps sharing the work
+  size_t pass_slot0;        // first partial slot of the window passes
+  int tail_passes;          // window/sink passes per (sequence, KV head) at most, 32 tokens each
   int max_len;              // host bound on seq_len the plan was sized for
   const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
   const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
@@ -280,52 +285,103 @@ __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, int kt, i
   return reinterpret_cast<const uint32_t *>(kc)[((w >> 2) * 32 + lane) * 4 + (w & 3)];
 }
 
-// Per-warp decode work item of one (sequence, KV head).  Its items are
-// numbered split = 0 .. nsp-1: the first `tail_passes` cover the fp16 sink +
-// window tokens 32 at a time (scheduled first: they are the slowest per
-// byte), the rest are runs of `chunk` packed groups.  kind: 1 = groups
-// [g0, g0+ng); 2 = window/sink tokens [32*split, 32*split + 32); 3 = zero the
-// output rows (empty sequence, or length out of range); 0 = nothing to do;
-// -1 = past the end.  nparts = partial results the (sequence, KV head)
-// produces in total.
-struct Item {
-  int s, h, split, kind, g0, ng, tparts, nparts;
-  Split spl;
+// ------------------------------------------------------------ work schedule
+//
+// The decode work of a (sequence, KV head) pair is a run of units: first
+// kPassUnits units per 32-token pass over its fp16 sink + window tokens, then
+// one unit per packed group.  Pairs are laid out sequence-major; the plan
+// kernel writes base[s] (first unit of sequence s) and the total W.  Warp gw
+// of NW takes units [gw W / NW, (gw + 1) W / NW): equal work, contiguous
+// across pair boundaries.  A warp leaves one partial result per pair it
+// touches (slot gw + pair) plus one per window pass it runs; the warp that
+// completes a pair's count merges them.
+constexpr int kPassUnits = 4;
+
+struct PlanHeader {
+  long long total;  // W
 };
 
-__device__ __forceinline__ Item item_of(const DecodeArgs &a, int it) {
-  Item x;
-  x.kind = -1;
-  x.s = x.h = x.split = x.g0 = x.ng = x.tparts = x.nparts = 0;
-  x.spl.nsink = x.spl.Lq = x.spl.r = 0;
-  if (it >= a.items) return x;
-  const int per_s = a.geo.H * a.nsp;
-  x.s = it / per_s;
-  const int rem = it - x.s * per_s;
-  x.h = rem / a.nsp;
-  x.split = rem - x.h * a.nsp;
-  const int L = a.geo.seq_len[x.s];
-  x.kind = 0;
-  if (L <= 0 || L > a.geo.capacity || L > a.max_len) {
-    if (x.split == 0) x.kind = 3;
-    return x;
+// Units of sequence s per KV head (0 when there is nothing to attend).
+__device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Split &spl, int &tp, int &ng) {
+  const int L = a.geo.seq_len[s];
+  tp = ng = 0;
+  spl.nsink = spl.Lq = spl.r = 0;
+  if (L <= 0 || L > a.geo.capacity || L > a.max_len) return 0;
+  spl = split_len(L, a.geo.ns, a.geo.R);
+  ng = spl.Lq / kG;
+  tp = (spl.nsink + spl.r + 31) / 32;
+  return kPassUnits * tp + ng;
+}
+
+// Per-sequence unit prefix (exclusive) times Hkv, the total, the merge
+// counters zeroed, and zero output rows for sequences with nothing to attend.
+// One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
+  __shared__ long long warp_sum[32];
+  const int S = a.geo.S, H = a.geo.H;
+  const int per = (S + blockDim.x - 1) / blockDim.x;
+  const int s0 = threadIdx.x * per, s1 = min(S, s0 + per);
+  long long mine = 0;
+  for (int s = s0; s < s1; ++s) {
+    Split spl;
+    int tp, ng;
+    mine += seq_units(a, s, spl, tp, ng);
   }
-  x.spl = split_len(L, a.geo.ns, a.geo.R);
-  const int ng_all = x.spl.Lq / kG;
-  const int nchunks = (ng_all + a.chunk - 1) / a.chunk;
-  x.tparts = (x.spl.nsink + x.spl.r + 31) / 32;
-  x.nparts = x.tparts + nchunks;
-  if (x.split < a.tail_passes) {
-    if (x.split < x.tparts) x.kind = 2;
-  } else {
-    const int c = x.split - a.tail_passes;
-    if (c < nchunks) {
-      x.kind = 1;
-      x.g0 = c * a.chunk;
-      x.ng = min(a.chunk, ng_all - x.g0);
+  // exclusive block scan of `mine`
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(kFull, ws, o);
+      if (lane >= o) ws += v;
     }
+    warp_sum[lane] = ws;  // inclusive over warps
   }
-  return x;
+  __syncthreads();
+  long long run = incl - mine + (warp > 0 ? warp_sum[warp - 1] : 0);
+  for (int s = s0; s < s1; ++s) {
+    a.base[s] = run * H;
+    Split spl;
+    int tp, ng;
+    run += seq_units(a, s, spl, tp, ng);
+  }
+  if (threadIdx.x == blockDim.x - 1) {
+    a.base[S] = run * H;
+    a.plan->total = run * H;
+  }
+  for (int i = threadIdx.x; i < S * H; i += blockDim.x) a.counters[i] = 0;
+  // sequences with nothing to attend (empty, or longer than the cache or the
+  // planned bound) get zero output rows, one warp per sequence
+  for (int s = warp; s < S; s += blockDim.x >> 5) {
+    const int L = a.geo.seq_len[s];
+    if (L > 0 && L <= a.geo.capacity && L <= a.max_len) continue;
+    if (lane == 0 && L > a.max_len) set_status(a.geo.status, KVQ_STATUS_MAX_LEN);
+    uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(s) * a.Hq * kD);
+    for (int i = lane; i < a.Hq * kD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The warp whose unit range holds unit x.
+__device__ __forceinline__ int owner_warp(long long x, long long W, int NW) {
+  return static_cast<int>(((x + 1) * NW - 1) / W);
+}
+
+// Warps with a non-empty unit range that intersect [P0, P1).
+__device__ __forceinline__ int touching_warps(long long P0, long long P1, long long W, int NW) {
+  const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
+  if (W >= NW) return w1 - w0 + 1;
+  int n = 0;
+  for (int w = w0; w <= w1; ++w) n += (w * W / NW) < ((w + 1) * W / NW);
+  return n;
 }
 
 // Scores of one packed group for this lane: z[tau] = log2-domain logit of
@@ -375,8 +431,15 @@ __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_
   }
 }
 
+// Resident CTAs per SM the register budget is cut for (tensor-core path,
+// query groups of one or two heads).
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 4
+#endif
+
 template <int BITS, int GQ, bool ROPE>
-__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DECODE_MIN_BLOCKS))
+    decode_kernel(DecodeArgs a) {
   using WS = WarpSmem<BITS>;
   constexpr int NS = WS::NS, BB = WS::BB;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -398,82 +461,228 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
   }
   __syncthreads();  // the only CTA-wide barrier: from here each warp runs alone
 
+  const long long W = a.plan->total;
+  const int NW = a.nw, gw = blockIdx.x * kWarps + warp;
+  if (gw >= NW) return;
+  const long long ua = gw * W / NW, ub = (gw + 1) * W / NW;
+  if (ua >= ub) return;
   const bool head_valid = q < GQ;
-    uint32_t fseq = 0, cseq = 0;                     // ring groups issued / consumed
-  bool ok = true;
+  const int H = geo.H;
 
-#ifndef KVQ_DECODE_STATIC
-#define KVQ_DECODE_STATIC 0
-#endif
-  int k_static = 0;
-  auto grab = [&]() {
-    int it = 0;
-    if (KVQ_DECODE_STATIC) {
-      it = (blockIdx.x * kWarps + warp) + (k_static++) * static_cast<int>(gridDim.x * kWarps);
-    } else if (lane == 0) {
-      it = atomicAdd(a.work, 1);
+  // the sequence holding unit ua: the last s with base[s] <= ua, by a
+  // 32-way search (base[0] = 0 <= ua keeps the answer in [lo, lo + n))
+  int s_first;
+  {
+    int lo = 0, n = geo.S;
+    while (n > 32) {
+      const int step = (n + 31) / 32;
+      const int idx = lo + lane * step;
+      const unsigned m = __ballot_sync(kFull, idx < lo + n && a.base[idx] <= ua);
+      const int nlo = lo + (31 - __clz(m)) * step;
+      n = min(step, lo + n - nlo);
+      lo = nlo;
     }
-    return it;
-  };
-  Item cur = item_of(a, __shfl_sync(kFull, grab(), 0)), nxt;
-  int cur_fetched = 0, nxt_fetched = 0;
-  bool have_nxt = false;
-  int nid = 0;
+    const unsigned m = __ballot_sync(kFull, lane < n && a.base[lo + lane] <= ua);
+    s_first = lo + 31 - __clz(m);
+  }
 
-  // issue the next group of `it` into the next ring slot (lane 0 issues)
-  auto issue = [&](const Item &it, int gidx) {
-    if (lane == 0) {
-      const uint32_t slot = fseq % NS;
-      const uint8_t *src =
-          geo.blocks + ((static_cast<size_t>(it.s) * geo.H + it.h) * geo.max_groups + it.g0 + gidx) * BB;
-      fence_proxy_async();  // generic reads of the slot before the async write
-      mbar_arrive_expect_tx(&full[slot], BB);
-      bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
-    }
-    ++fseq;
+  // ---- fetch cursor: walks the packed groups of [ua, ub) in consumer order
+  uint32_t fseq = 0, cseq = 0;  // ring groups issued / consumed
+  int fs = s_first, fh = 0, fg = 0, fg_end = 0;
+  bool fdone = false;
+  auto fetch_pair = [&](int s, int h) {  // set the group range of pair (s, h)
+    Split spl;
+    int tp, ng;
+    const int u = seq_units(a, s, spl, tp, ng);
+    const long long P0 = a.base[s] + static_cast<long long>(h) * u;
+    const long long gb = P0 + kPassUnits * tp;
+    fg = static_cast<int>(min(max(ua - gb, 0LL), static_cast<long long>(ng)));
+    fg_end = static_cast<int>(min(max(ub - gb, 0LL), static_cast<long long>(ng)));
+    return P0 < ub;
   };
-  auto top_up = [&]() {
-    while (fseq - cseq < static_cast<uint32_t>(NS)) {
-      if (cur.kind == 1 && cur_fetched < cur.ng) {
-        issue(cur, cur_fetched++);
-      } else if (have_nxt && nxt.kind == 1 && nxt_fetched < nxt.ng) {
-        issue(nxt, nxt_fetched++);
-      } else {
+  auto fetch_next_pair = [&]() {
+    while (!fdone) {
+      if (++fh == H) {
+        fh = 0;
+        if (++fs >= geo.S) {
+          fdone = true;
+          break;
+        }
+      }
+      if (!fetch_pair(fs, fh)) {
+        fdone = true;
         break;
       }
+      if (fg < fg_end) break;
+    }
+  };
+  {
+    Split spl;
+    int tp, ng;
+    const int u = seq_units(a, fs, spl, tp, ng);
+    fh = static_cast<int>((ua - a.base[fs]) / max(u, 1));
+    if (!fetch_pair(fs, fh)) fdone = true;
+    if (!fdone && fg >= fg_end) fetch_next_pair();
+  }
+  auto top_up = [&]() {
+    while (!fdone && fseq - cseq < static_cast<uint32_t>(NS)) {
+      if (lane == 0) {
+        const uint32_t slot = fseq % NS;
+        const uint8_t *src =
+            geo.blocks + ((static_cast<size_t>(fs) * H + fh) * geo.max_groups + fg) * BB;
+        fence_proxy_async();  // generic reads of the slot before the async write
+        mbar_arrive_expect_tx(&full[slot], BB);
+        bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
+      }
+      ++fseq;
+      if (++fg >= fg_end) fetch_next_pair();
     }
   };
   top_up();
-  // the next item is claimed at the start of the current one and resolved
-  // (its lengths read, its first groups fetched) once the first groups of
-  // the current item are under way, so the claim's latency stays hidden
-  auto resolve = [&]() {
-    if (!have_nxt) {
-      nxt = item_of(a, __shfl_sync(kFull, nid, 0));
-      nxt_fetched = 0;
-      have_nxt = true;
-      top_up();
-    }
-  };
 
-  while (cur.kind != -1) {
-    nid = grab();
-    if (cur.kind != 1 || ROPE) resolve();
-    const size_t orow0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ) * kD;
-    const size_t prow0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ) * a.nsp + cur.split;
-    if (cur.kind == 3) {
-      for (int i = lane; i < GQ * kD; i += 32) a.out[orow0 + i] = __float2half_rn(0.f);
-      if (lane == 0 && cur.h == 0 && geo.seq_len[cur.s] > a.max_len) set_status(geo.status, KVQ_STATUS_MAX_LEN);
-    } else if (cur.kind == 1 || cur.kind == 2) {
-      __syncwarp();  // the previous item's reads of q_s are done
-      for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
-      __syncwarp();
-      if (cur.kind == 1) {
-        // ---------------------------------------------------- quantized groups
-        float o[8][4];
+  // ---- consumer: pairs in order
+  bool ok = true;
+  int s = s_first;
+  Split spl;
+  int tp, ng;
+  int u = seq_units(a, s, spl, tp, ng);
+  int h = static_cast<int>((ua - a.base[s]) / max(u, 1));
+  while (ok) {
+    if (u == 0) {  // sequence with nothing to attend: skip it
+      if (++s >= geo.S) break;
+      h = 0;
+      u = seq_units(a, s, spl, tp, ng);
+      continue;
+    }
+    const long long P0 = a.base[s] + static_cast<long long>(h) * u, P1 = P0 + u;
+    if (P0 >= ub) break;
+    const long long lo = max(ua, P0), hi = min(ub, P1);
+    const int pair = s * H + h;
+    const size_t orow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * kD;
+    __syncwarp();  // the previous pair's reads of q_s are done
+    for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
+    __syncwarp();
+    int npart = 0;
+
+    // ------------------ window / sink passes whose first unit is ours
+    for (int k = 0; k < tp; ++k) {
+      const long long x = P0 + static_cast<long long>(kPassUnits) * k;
+      if (x < lo || x >= hi) continue;
+      const int T = spl.nsink + spl.r;
+      const int t0 = 32 * k;
+      const int nt = min(32, T - t0);
+      const size_t sh = static_cast<size_t>(pair);
+      const int i = t0 + lane;
+      const bool valid = lane < nt;
+      float dot[GQ];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_run = -INFINITY, l_run = 0.f, mu_run = 0.f;
+      for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
+      if (valid) {
+        int pos;
+        const __half *kp;
+        if (i < spl.nsink) {
+          pos = i;
+          kp = geo.k_sink + (sh * geo.ns + i) * kD;
+        } else {
+          const int slot = i - spl.nsink;
+          pos = spl.nsink + spl.Lq + slot;
+          kp = geo.k_res + (sh * geo.R + slot) * kD;
+        }
+        const int sidx = pos - geo.ns;  // stream index (negative for the sink)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 ra[4], rb[4];  // channels 32*half + 8c.. and 64 + 32*half + 8c..
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            ra[c] = *reinterpret_cast<const uint4 *>(kp + 32 * half + 8 * c);
+            rb[c] = *reinterpret_cast<const uint4 *>(kp + 64 + 32 * half + 8 * c);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const __half *ha = reinterpret_cast<const __half *>(&ra[c]);
+            const __half *hb = reinterpret_cast<const __half *>(&rb[c]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int ch = 32 * half + 8 * c + e;
+              float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
+              if (ROPE && sidx >= 0) {
+                const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
+                const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
+                const float cs = bs.x * of.x - bs.y * of.y;
+                const float sn = bs.y * of.x + bs.x * of.y;
+                const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
+                k1 = r1;
+                k2 = r2;
+              }
+#pragma unroll
+              for (int hh = 0; hh < GQ; ++hh)
+                dot[hh] = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, dot[hh]));
+            }
+          }
+        }
+      }
+      float p[GQ], mh[GQ], lh[GQ], acc[GQ][4];
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        const float zz = valid ? dot[hh] * a.zscale : -INFINITY;
+        float mx = zz;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        p[hh] = valid ? fast_exp2(zz - mx) : 0.f;
+        float sum = p[hh];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+        mh[hh] = mx;
+        lh[hh] = sum;
+        acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+      }
+      // values: lane holds channels 4*lane .. 4*lane+3; eight rows in flight
+      for (int tb = 0; tb < nt; tb += 8) {
+        uint2 raw[8];
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const int it = t0 + tb + uu;
+          raw[uu] = make_uint2(0u, 0u);
+          if (tb + uu < nt) {
+            const __half *vp = it < spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
+                                              : geo.v_res + (sh * geo.R + (it - spl.nsink)) * kD;
+            raw[uu] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < 8; ++uu) {
+          const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].x));
+          const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].y));
+#pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) {
+            const float pt = __shfl_sync(kFull, p[hh], (tb + uu) & 31);
+            acc[hh][0] = fmaf(pt, v01.x, acc[hh][0]);
+            acc[hh][1] = fmaf(pt, v01.y, acc[hh][1]);
+            acc[hh][2] = fmaf(pt, v23.x, acc[hh][2]);
+            acc[hh][3] = fmaf(pt, v23.y, acc[hh][3]);
+          }
+        }
+      }
+      const size_t slot = a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k;
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        float *po = a.part_o + (slot * GQ + hh) * kD;
+        *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        if (lane == 0) a.part_ml[slot * GQ + hh] = make_float2(mh[hh], lh[hh]);
+      }
+      ++npart;
+    }
+
+    // ------------------------------------------- packed groups of our range
+    {
+      const long long gb = P0 + static_cast<long long>(kPassUnits) * tp;
+      const int g_lo = static_cast<int>(min(max(lo - gb, 0LL), static_cast<long long>(ng)));
+      const int g_hi = static_cast<int>(min(max(hi - gb, 0LL), static_cast<long long>(ng)));
+      float o[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float m_run = -INFINITY, l_run = 0.f, mu_run = 0.f;
+      if (g_lo < g_hi) {
         if (!ROPE) {
           QkOperand<GQ> qo;
           qo.init(q_s, lane, a.zscale);
@@ -482,8 +691,8 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
           for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
           // two groups (64 tokens) per iteration: independent score mmas, one
           // softmax update, two value mmas
-          for (int gi = 0; gi < cur.ng; gi += 2) {
-            const bool two = gi + 1 < cur.ng;
+          for (int gi = g_lo; gi < g_hi; gi += 2) {
+            const bool two = gi + 1 < g_hi;
             const uint32_t sa = cseq % NS, sb = (cseq + 1) % NS;
             if (!mbar_wait_bounded(&full[sa], (cseq / NS) & 1) ||
                 (two && !mbar_wait_bounded(&full[sb], ((cseq + 1) / NS) & 1))) {
@@ -533,7 +742,6 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
               rescale_o(o, __shfl_sync(kFull, alpha, (2 * q) & 31), __shfl_sync(kFull, alpha, (2 * q + 1) & 31));
             group_values<BITS>(ba, psa, lane, o);
             if (two) group_values<BITS>(bb, psb, lane, o);
-            resolve();
             __syncwarp();
             cseq += two ? 2 : 1;
             top_up();
@@ -543,7 +751,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
           float m_all[GQ];
 #pragma unroll
           for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
-          for (int gi = 0; gi < cur.ng; ++gi) {
+          for (int gi = g_lo; gi < g_hi; ++gi) {
             const uint32_t slot = cseq % NS;
             if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1)) {
               ok = false;
@@ -555,9 +763,9 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
             const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
             const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
             const uint8_t *kc = blk + off_kc(BITS);
-            const float2 *base = a.rope_base + static_cast<size_t>(cur.g0 + gi) * 64;
+            const float2 *base = a.rope_base + static_cast<size_t>(gi) * 64;
             const int t = lane;
-            const int u = (t >> 3) % (8 / BITS);
+            const int uu = (t >> 3) % (8 / BITS);
             float dot[GQ];
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
@@ -572,7 +780,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
 #pragma unroll
                   for (int e = 0; e < 2; ++e) {
                     const int ch = 16 * kt + 8 * j + 2 * qq + e;
-                    const int sh = 16 * e + 8 * j + BITS * u;
+                    const int sh = 16 * e + 8 * j + BITS * uu;
                     const float ca = static_cast<float>((wa >> sh) & ((1u << BITS) - 1u));
                     const float cb = static_cast<float>((wb >> sh) & ((1u << BITS) - 1u));
                     const float k1 = fmaf(ca, ks[ch], km[ch]);
@@ -640,182 +848,85 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : 4)) dec
                 bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
               }
             pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
-            resolve();
             __syncwarp();
             ++cseq;
             top_up();
           }
         }
-        if (!ok) break;
-        // this item's partial state per query head
+      }
+      if (!ok) break;
+      // this warp's partial of the pair's packed groups (empty if it had none)
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          l_run += __shfl_xor_sync(kFull, l_run, off);
-          mu_run += __shfl_xor_sync(kFull, mu_run, off);
-        }
-        {
-          const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
+      for (int off = 4; off < 32; off <<= 1) {
+        l_run += __shfl_xor_sync(kFull, l_run, off);
+        mu_run += __shfl_xor_sync(kFull, mu_run, off);
+      }
+      const size_t slot = static_cast<size_t>(gw) + pair;
+      const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if (2 * q + c < GQ) {
-              float *po = a.part_o + (prow0 + static_cast<size_t>(2 * q + c) * a.nsp) * kD;
+      for (int c = 0; c < 2; ++c) {
+        if (2 * q + c < GQ) {
+          float *po = a.part_o + (slot * GQ + 2 * q + c) * kD;
 #pragma unroll
-              for (int mt = 0; mt < 8; ++mt)
+          for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr)
-                  po[16 * mt + 8 * rr + g] = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
-            }
-          }
-          if (head_valid && g == 0) a.part_ml[prow0 + static_cast<size_t>(q) * a.nsp] = make_float2(m_run, l_run);
-        }
-      } else {
-        // ------------------ 32 sink / window tokens, CUDA cores, one per lane
-        const int T = cur.spl.nsink + cur.spl.r;
-        const int t0 = 32 * cur.split;
-        const int nt = min(32, T - t0);
-        const size_t sh = static_cast<size_t>(cur.s) * geo.H + cur.h;
-        const int i = t0 + lane;
-        const bool valid = lane < nt;
-        float dot[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
-        if (valid) {
-          int pos;
-          const __half *kp;
-          if (i < cur.spl.nsink) {
-            pos = i;
-            kp = geo.k_sink + (sh * geo.ns + i) * kD;
-          } else {
-            const int slot = i - cur.spl.nsink;
-            pos = cur.spl.nsink + cur.spl.Lq + slot;
-            kp = geo.k_res + (sh * geo.R + slot) * kD;
-          }
-          const int sidx = pos - geo.ns;  // stream index (negative for the sink)
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint4 ra[4], rb[4];  // channels 32*half + 8c.. and 64 + 32*half + 8c..
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              ra[c] = *reinterpret_cast<const uint4 *>(kp + 32 * half + 8 * c);
-              rb[c] = *reinterpret_cast<const uint4 *>(kp + 64 + 32 * half + 8 * c);
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const __half *ha = reinterpret_cast<const __half *>(&ra[c]);
-              const __half *hb = reinterpret_cast<const __half *>(&rb[c]);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int ch = 32 * half + 8 * c + e;
-                float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
-                if (ROPE && sidx >= 0) {
-                  const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
-                  const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
-                  const float cs = bs.x * of.x - bs.y * of.y;
-                  const float sn = bs.y * of.x + bs.x * of.y;
-                  const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
-                  k1 = r1;
-                  k2 = r2;
-                }
-#pragma unroll
-                for (int hh = 0; hh < GQ; ++hh)
-                  dot[hh] = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, dot[hh]));
-              }
-            }
-          }
-        }
-        float p[GQ], mh[GQ], lh[GQ], acc[GQ][4];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float zz = valid ? dot[hh] * a.zscale : -INFINITY;
-          float mx = zz;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-          p[hh] = valid ? fast_exp2(zz - mx) : 0.f;
-          float sum = p[hh];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-          mh[hh] = mx;
-          lh[hh] = sum;
-          acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
-        }
-        // values: lane holds channels 4*lane .. 4*lane+3; eight rows in flight
-        for (int tb = 0; tb < nt; tb += 8) {
-          uint2 raw[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int it = t0 + tb + u;
-            raw[u] = make_uint2(0u, 0u);
-            if (tb + u < nt) {
-              const __half *vp = it < cur.spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
-                                                    : geo.v_res + (sh * geo.R + (it - cur.spl.nsink)) * kD;
-              raw[u] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u].x));
-            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[u].y));
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-              const float pt = __shfl_sync(kFull, p[hh], (tb + u) & 31);
-              acc[hh][0] = fmaf(pt, v01.x, acc[hh][0]);
-              acc[hh][1] = fmaf(pt, v01.y, acc[hh][1]);
-              acc[hh][2] = fmaf(pt, v23.x, acc[hh][2]);
-              acc[hh][3] = fmaf(pt, v23.y, acc[hh][3]);
-            }
-          }
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          float *po = a.part_o + (prow0 + static_cast<size_t>(hh) * a.nsp) * kD;
-          *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-          if (lane == 0) a.part_ml[prow0 + static_cast<size_t>(hh) * a.nsp] = make_float2(mh[hh], lh[hh]);
+            for (int rr = 0; rr < 2; ++rr)
+              po[16 * mt + 8 * rr + g] = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
         }
       }
-      // the last item of this (sequence, KV head) to finish merges them all;
-      // lane 0's acq_rel add publishes the warp's partial (ordered before it
-      // by the warp barrier) and observes every earlier item's
-      __syncwarp();
-      int last = 0;
-      if (lane == 0)
-        last = atom_add_acq_rel(&a.counters[static_cast<size_t>(cur.s) * geo.H + cur.h], 1) == cur.nparts - 1;
-      if (__shfl_sync(kFull, last, 0)) {
-        __threadfence();
-        for (int hh = 0; hh < GQ; ++hh) {
-          const size_t r0 = (static_cast<size_t>(cur.s) * a.Hq + static_cast<size_t>(cur.h) * GQ + hh) * a.nsp;
-          // partial i lives at split i (window passes) or tail_passes + i - tparts (chunks)
-          auto split_of = [&](int i) { return i < cur.tparts ? i : a.tail_passes + i - cur.tparts; };
-          float M = -INFINITY;
-          for (int i = lane; i < cur.nparts; i += 32) M = fmaxf(M, __ldcg(&a.part_ml[r0 + split_of(i)]).x);
+      if (head_valid && g == 0) a.part_ml[slot * GQ + q] = make_float2(m_run, l_run);
+      ++npart;
+    }
+
+    // ---- the warp completing the pair's count merges its partials; lane
+    // 0's acq_rel add publishes this warp's partials (ordered before it by
+    // the warp barrier) and observes every other warp's
+    __syncwarp();
+    const int expect = tp + touching_warps(P0, P1, W, NW);
+    int last = 0;
+    if (lane == 0) last = atom_add_acq_rel(&a.counters[pair], npart) + npart == expect;
+    if (__shfl_sync(kFull, last, 0)) {
+      __threadfence();
+      const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
+      for (int hh = 0; hh < GQ; ++hh) {
+        float M = -INFINITY;
+        for (int k = lane; k < tp; k += 32)
+          M = fmaxf(M, __ldcg(&a.part_ml[(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k) * GQ + hh]).x);
+        for (int w = w0 + lane; w <= w1; w += 32)
+          if (w * W / NW < (w + 1) * W / NW)
+            M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(w) + pair) * GQ + hh]).x);
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-          float Ls = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (M != -INFINITY) {
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto add = [&](size_t sl) {
+          const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
+          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
+          const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+          Ls = fmaf(ml.y, wgt, Ls);
+          acc.x = fmaf(ov.x, wgt, acc.x);
+          acc.y = fmaf(ov.y, wgt, acc.y);
+          acc.z = fmaf(ov.z, wgt, acc.z);
+          acc.w = fmaf(ov.w, wgt, acc.w);
+        };
+        if (M != -INFINITY) {
+          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k);
 #pragma unroll 4
-            for (int i = 0; i < cur.nparts; ++i) {
-              const size_t r = r0 + split_of(i);
-              const float2 ml = __ldcg(&a.part_ml[r]);
-              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + r * kD) + lane);
-              const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-              Ls = fmaf(ml.y, wgt, Ls);
-              acc.x = fmaf(ov.x, wgt, acc.x);
-              acc.y = fmaf(ov.y, wgt, acc.y);
-              acc.z = fmaf(ov.z, wgt, acc.z);
-              acc.w = fmaf(ov.w, wgt, acc.w);
-            }
-          }
-          const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
-          __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
-          op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-          op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+          for (int w = w0; w <= w1; ++w)
+            if (w * W / NW < (w + 1) * W / NW) add(static_cast<size_t>(w) + pair);
         }
+        const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
+        __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
+        op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
       }
     }
-    resolve();
-    cur = nxt;
-    cur_fetched = nxt_fetched;
-    have_nxt = false;
+    if (P1 >= ub) break;
+    if (++h == H) {
+      h = 0;
+      if (++s >= geo.S) break;
+      u = seq_units(a, s, spl, tp, ng);
+    }
   }
   if (!ok) {
     set_status(geo.status, KVQ_STATUS_TIMEOUT);
@@ -844,18 +955,21 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 
 // ---------------------------------------------------------------- host side
 
+// Resident CTAs per SM of one instantiation on the current device, and the
+// device's SM count (cached per device ordinal).
 template <int BITS, int GQ, bool ROPE>
-static cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
+static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
   using WS = WarpSmem<BITS>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
   auto kern = decode_kernel<BITS, GQ, ROPE>;
-  // per instantiation and device ordinal: attributes set, resident CTAs per SM
   static int resident[64] = {};
   static int sms[64] = {};
+  bytes_out = bytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int per_sm = dev < 64 ? resident[dev] : 0, n_sm = dev < 64 ? sms[dev] : 0;
+  per_sm = dev < 64 ? resident[dev] : 0;
+  n_sm = dev < 64 ? sms[dev] : 0;
   if (per_sm == 0) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -869,9 +983,30 @@ static cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
       sms[dev] = n_sm;
     }
   }
-  const long long want = (static_cast<long long>(a.items) + kWarps - 1) / kWarps;
-  const int grid = static_cast<int>(min(want, static_cast<long long>(n_sm) * per_sm));
-  kern<<<grid, kWarps * 32, bytes, stream>>>(a);
+  return cudaSuccess;
+}
+
+static int g_warps_override = 0;
+
+int set_decode_warps(int warps) {
+  if (warps < 0 || warps > kMaxDecodeWarps) return -1;
+  g_warps_override = warps;
+  return 0;
+}
+
+// Warps one launch spreads the work over: every resident warp of the device
+// (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
+template <int BITS, int GQ, bool ROPE>
+static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
+  int per_sm = 0, n_sm = 0, bytes = 0;
+  cudaError_t e = kernel_slots<BITS, GQ, ROPE>(per_sm, n_sm, bytes);
+  if (e != cudaSuccess) return e;
+  int nw = g_warps_override ? g_warps_override : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
+  nw = max(nw, 1);
+  a.nw = nw;
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  decode_kernel<BITS, GQ, ROPE><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -891,41 +1026,23 @@ static cudaError_t launch_b(const DecodeArgs &a, int gq, cudaStream_t stream) {
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-static int g_chunk_override = 0;
-
-int set_decode_chunk(int groups) {
-  if (groups != 0 && (groups < 4 || groups > 1024 || groups % 4 != 0)) return -1;
-  g_chunk_override = groups;
-  return 0;
-}
-
 DecodePlan plan_decode(const Geo &geo, int Hq, int max_len) {
   DecodePlan p;
-  const Split sp = split_len(max_len, geo.ns, geo.R);
-  const long long ng_max = sp.Lq / kG;
-  int chunk = g_chunk_override;
-  if (chunk == 0) {
-    // about six items per warp of a full GB300 (152 SMs x 16 warps) so the
-    // dynamic schedule balances, at least 8 groups per item, and at most
-    // ~512 items per (sequence, KV head) so the final merge stays short
-    const long long total = static_cast<long long>(geo.S) * geo.H * ng_max;
-    long long c = (total + 6LL * 152 * 16 - 1) / (6LL * 152 * 16);
-    c = max(c, (ng_max + 510) / 511);
-    c = min(max(c, 8LL), 1024LL);
-    chunk = static_cast<int>((c + 3) / 4 * 4);
-  }
-  p.chunk = chunk;
+  const int gq = Hq / geo.H;
+  const size_t pairs = static_cast<size_t>(geo.S) * geo.H;
   p.tail_passes = (geo.R - 1 + geo.ns + 31) / 32;
-  p.nsp = static_cast<int>((ng_max + chunk - 1) / chunk) + p.tail_passes;
-  p.items = static_cast<long long>(geo.S) * geo.H * p.nsp;
   p.n_base = geo.pre_rope ? (max(max_len - geo.ns, 1) + kG - 1) / kG : 0;
-  const size_t rows = static_cast<size_t>(geo.S) * Hq * p.nsp;
-  p.off_ml = align256(rows * kD * sizeof(float));
-  p.off_cnt = p.off_ml + align256(rows * sizeof(float2));
-  p.cnt_bytes = (static_cast<size_t>(geo.S) * geo.H + 1) * sizeof(int);
-  p.off_base = p.off_cnt + align256(p.cnt_bytes);
-  p.off_off = p.off_base + align256(static_cast<size_t>(p.n_base) * 64 * sizeof(float2));
-  p.bytes = p.off_off + (geo.pre_rope ? align256(kG * 64 * sizeof(float2)) : 0);
+  // group partial slots gw + pair (gw < kMaxDecodeWarps), then the window
+  // pass slots pair * tail_passes + k
+  p.pass_slot0 = kMaxDecodeWarps + pairs;
+  const size_t slots = p.pass_slot0 + pairs * p.tail_passes;
+  p.off_ml = align256(slots * gq * kD * sizeof(float));
+  p.off_cnt = p.off_ml + align256(slots * gq * sizeof(float2));
+  p.off_base = p.off_cnt + align256(pairs * sizeof(int));
+  p.off_hdr = p.off_base + align256((static_cast<size_t>(geo.S) + 1) * sizeof(long long));
+  p.off_rope = p.off_hdr + 256;
+  p.off_off = p.off_rope + align256(static_cast<size_t>(p.n_base) * 64 * sizeof(float2));
+  p.bytes = geo.pre_rope ? p.off_off + align256(kG * 64 * sizeof(float2)) : p.off_rope;
   return p;
 }
 
@@ -942,19 +1059,18 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.part_o = reinterpret_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
   a.counters = reinterpret_cast<int *>(ws + p.off_cnt);
-  a.work = a.counters + static_cast<size_t>(geo.S) * geo.H;
-  a.items = static_cast<int>(p.items);
-  a.nsp = p.nsp;
+  a.base = reinterpret_cast<long long *>(ws + p.off_base);
+  a.plan = reinterpret_cast<PlanHeader *>(ws + p.off_hdr);
+  a.nw = 0;
+  a.pass_slot0 = p.pass_slot0;
   a.tail_passes = p.tail_passes;
-  a.chunk = p.chunk;
   a.max_len = max_len;
-  a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_base);
+  a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, p.cnt_bytes, stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   if (geo.pre_rope) {
     const int n = (p.n_base + kG) * 64;
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(reinterpret_cast<float2 *>(ws + p.off_base), p.n_base,
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(reinterpret_cast<float2 *>(ws + p.off_rope), p.n_base,
                                                            reinterpret_cast<float2 *>(ws + p.off_off), geo.ns,
                                                            geo.theta);
     ++*launches;
@@ -962,7 +1078,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   }
   const int gq = Hq / geo.H;
   e = geo.bits == 2 ? launch_b<2>(a, gq, stream) : launch_b<4>(a, gq, stream);
-  ++*launches;
+  *launches += 2;
   return e;
 }
 

@@ -177,14 +177,18 @@ __device__ inline uint32_t hi_or_lo(float x0, float x1, bool want_lo) {
 
 // ------------------------------------------------------- host-side launchers
 
-// Workspace plan of one decode call: groups per split, splits per (sequence,
-// query head), RoPE base rows, and the byte offsets of the workspace regions
-// (partial outputs, partial (max, sum), per-(sequence, KV head) split
-// counters, RoPE tables), each 256-byte aligned.
+// Warps one decode launch spreads its work over, at most (sizes the
+// workspace's partial-result slots).
+constexpr int kMaxDecodeWarps = 2560;
+
+// Workspace plan of one decode call: window passes per (sequence, KV head)
+// at most, RoPE base rows, and the byte offsets of the workspace regions
+// (partial outputs, partial (max, sum), merge counters, per-sequence work
+// prefix, plan header, RoPE tables), each 256-byte aligned.
 struct DecodePlan {
-  int chunk, nsp, tail_passes, n_base;
-  long long items;
-  size_t off_ml, off_cnt, cnt_bytes, off_base, off_off, bytes;
+  int tail_passes, n_base;
+  size_t pass_slot0;
+  size_t off_ml, off_cnt, off_base, off_hdr, off_rope, off_off, bytes;
 };
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
@@ -194,6 +198,6 @@ DecodePlan plan_decode(const Geo &geo, int Hq, int max_len);
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
                           void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
                           uint64_t *launches);
-int set_decode_chunk(int groups);
+int set_decode_warps(int warps);
 
 }  // namespace kvq

@@ -27,7 +27,7 @@ BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN = range(6)
 EXPORTED = (
     "kvq_block_bytes", "kvq_max_groups", "kvq_buffer_bytes", "kv_quant_append",
     "kv_decode_workspace_bytes", "kv_decode_attn", "kv_dequant", "kvq_strerror",
-    "kvq_launch_count", "kvq_set_decode_chunk", "kv_decode_attn_noalloc",
+    "kvq_launch_count", "kvq_set_decode_warps", "kv_decode_attn_noalloc",
 )
 
 
@@ -60,7 +60,7 @@ def _load():
         "kv_dequant": (ctypes.c_int, [P, c_void_p, c_void_p, c_void_p]),
         "kvq_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvq_launch_count": (c_uint64, []),
-        "kvq_set_decode_chunk": (ctypes.c_int, [c_int32]),
+        "kvq_set_decode_warps": (ctypes.c_int, [c_int32]),
         "kv_decode_attn_noalloc": (ctypes.c_int, [P, c_int32, c_void_p, c_float, c_void_p, c_int32, c_void_p]),
     }
     for name, (res, args) in sig.items():
@@ -190,5 +190,6 @@ def launch_count() -> int:
     return lib.kvq_launch_count()
 
 
-def set_decode_chunk(groups: int):
-    _check(lib.kvq_set_decode_chunk(groups), "kvq_set_decode_chunk")
+def set_decode_warps(warps: int):
+    """Warps a decode launch cuts its work into (0: every resident warp)."""
+    _check(lib.kvq_set_decode_warps(warps), "kvq_set_decode_warps")

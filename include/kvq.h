@@ -178,17 +178,20 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  *   workspace, workspace_bytes  device scratch of at least
  *           kv_decode_workspace_bytes(cache, num_q_heads, max_len) bytes,
  *           256-byte aligned; no contents need to be preserved between calls
- *           (the call zeroes its split counters itself).
- *   max_len host bound on every seq_len (sizes the split-K grid); a
+ *           (the call zeroes its merge counters itself).
+ *   max_len host bound on every seq_len (sizes the RoPE table); a
  *           sequence longer than max_len gets a zero output row and sets
  *           KVQ_STATUS_MAX_LEN.
  *
  * Keys are k_hat = code * scale + min (pre-RoPE keys then rotated by
- * rotate-half RoPE at their absolute position); values likewise.  The kernel
- * dequantizes in registers, forms scores, runs an online softmax per split of
- * the token axis, and the last split to finish merges them (log-sum-exp).
- * Enqueues a memset of the split counters and one kernel (plus a RoPE table
- * kernel when pre_rope).
+ * rotate-half RoPE at their absolute position); values likewise.  The work
+ * of all (sequence, KV head) pairs -- 32-token passes over the fp16 sink and
+ * window, then packed groups -- is cut into equal contiguous ranges, one per
+ * warp; the kernel dequantizes in registers, forms scores, runs an online
+ * softmax over each range, and the last range of a pair to finish merges its
+ * partials (log-sum-exp).  Enqueues a plan kernel (work prefix over the
+ * sequences, counters zeroed, rows of empty sequences zeroed) and the decode
+ * kernel, plus a RoPE table kernel when pre_rope.
  */
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    const uint16_t *q, float softmax_scale, uint16_t *out,
@@ -244,11 +247,12 @@ const char *kvq_strerror(int err);
  * launch accounting in benchmarks). */
 uint64_t kvq_launch_count(void);
 
-/* Groups per decode split (a multiple of 4, 4..1024); 0 restores the
- * built-in choice.  Affects kv_decode_workspace_bytes and kv_decode_attn
- * calls made afterwards in this process.  Returns KVQ_OK or
+/* Warps a decode launch cuts its work into (1..2560); 0 restores the
+ * built-in choice (every resident warp of the device, at most 2560).
+ * Affects kv_decode_attn calls made afterwards in this process; the
+ * workspace size does not depend on it.  Returns KVQ_OK or
  * KVQ_ERR_INVALID_ARG. */
-int kvq_set_decode_chunk(int32_t groups);
+int kvq_set_decode_warps(int32_t warps);
 
 #ifdef __cplusplus
 }

@@ -107,5 +107,6 @@ def test_null_and_misaligned_buffers_rejected_before_launch(kvq):
     assert kvq.lib.kv_decode_attn(p, 24, q, 0.0, q, ws, need, 1000, None) == -2
     assert kvq.lib.kv_decode_attn(p, 6, None, 0.0, q, ws, need, 1000, None) == -1
     assert kvq.lib.kv_dequant(p, None, q, None) == -1
-    assert kvq.lib.kvq_set_decode_chunk(6) == -1 and kvq.lib.kvq_set_decode_chunk(0) == 0
+    assert kvq.lib.kvq_set_decode_warps(-1) == -1 and kvq.lib.kvq_set_decode_warps(2561) == -1
+    assert kvq.lib.kvq_set_decode_warps(7) == 0 and kvq.lib.kvq_set_decode_warps(0) == 0
     assert kvq.lib.kvq_strerror(-4) == b"workspace missing or too small"

@@ -243,9 +243,11 @@ def test_workspace_too_small_raises(kvq):
     assert e.value.code == -4
 
 
-@pytest.mark.parametrize("chunk", [4, 8, 64])
-def test_split_sizes_agree(kvq, chunk):
-    """The answer does not depend on how the token axis is split."""
+@pytest.mark.parametrize("warps", [1, 3, 7, 50, 333, 2560])
+def test_split_sizes_agree(kvq, warps):
+    """The answer does not depend on how the work is cut into warp ranges:
+    one warp for everything, ranges that end inside window passes and
+    groups, and more warps than units (empty ranges)."""
     S, H, T = 2, 2, 1500
     k, v = _rand_kv(S, H, T, seed=12)
     cache, orc = _build(kvq, S, H, 1600, 2, ns=1)
@@ -253,10 +255,10 @@ def test_split_sizes_agree(kvq, chunk):
     q = _rand_q(S, 4 * H, seed=4)
     want = orc.attention(q)
     try:
-        kvq.set_decode_chunk(chunk)
+        kvq.set_decode_warps(warps)
         _attn_close(_attend(kvq, cache, q, 1500), want)
     finally:
-        kvq.set_decode_chunk(0)
+        kvq.set_decode_warps(0)
 
 
 @pytest.mark.parametrize("bits", [2, 4])
