@@ -300,7 +300,7 @@ def run_ours(args, w, layers, rank, world, local):
     # The decode grid is sized for the cache capacity, so one captured graph
     # serves every step (the kernel reads the actual lengths on the device).
     max_len = capacity
-    ws = torch.empty(kvq.kv_decode_workspace_bytes(caches[0], Hq, max_len), dtype=torch.uint8, device=device)
+    ws = kvq.alloc_workspace(caches[0], Hq, max_len)  # zero-filled; every layer's call leaves it so
 
     def step_calls(p, append=True):
         for l in range(layers):

@@ -128,8 +128,9 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads, i
   return static_cast<int64_t>(kvq::plan_decode(make_geo(cache), num_q_heads, max_len).bytes);
 }
 
-int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
-                   uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
+static int decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                       uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream,
+                       bool zero_counters) {
   int e = check_buffers(cache);
   if (e) return e;
   if (!q || !out || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
@@ -146,10 +147,16 @@ int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *
   if (!aligned(workspace, 256)) return KVQ_ERR_ALIGNMENT;
   uint64_t n = 0;
   cudaError_t ce = kvq::launch_decode(geo, num_q_heads, reinterpret_cast<const __half *>(q), softmax_scale,
-                                      reinterpret_cast<__half *>(out), workspace, plan, max_len,
+                                      reinterpret_cast<__half *>(out), workspace, plan, max_len, zero_counters,
                                       static_cast<cudaStream_t>(stream), &n);
   return from_cuda(ce, n);
 }
+
+int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                   uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
+  return decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream, false);
+}
+
 
 int kv_dequant(const kvq_cache *cache, float *k_out, float *v_out, void *stream) {
   int e = check_buffers(cache);
@@ -179,3 +186,12 @@ uint64_t kvq_launch_count(void) { return g_launches.load(); }
 int kvq_set_decode_warps(int32_t warps) { return kvq::set_decode_warps(warps) ? KVQ_ERR_INVALID_ARG : KVQ_OK; }
 
 }  // extern "C"
+
+namespace kvq {
+
+int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                         uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
+  return ::decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream, true);
+}
+
+}  // namespace kvq

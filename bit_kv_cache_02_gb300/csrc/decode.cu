@@ -53,8 +53,9 @@ struct DecodeArgs {
   float zscale;             // softmax scale * log2(e)
   float *part_o;            // [slots][GQ][D] unnormalized partial outputs
   float2 *part_ml;          // [slots][GQ] (max, sum) in log2 units
-  int *counters;            // [S][Hkv] partials finished, zeroed by the plan kernel
-  long long *base;          // [S + 1] first work unit of each sequence (plan kernel)
+  int *counters;            // [S][Hkv] partials finished: zero on entry, left zero on exit
+  long long *base;          // [S + 1] first work unit of each sequence (plan kernel), or
+                            // null when the decode kernel plans by itself
   PlanHeader *plan;         // total work units (plan kernel)
   int nw;                   // warps sharing the work
   size_t pass_slot0;        // first partial slot of the window passes
@@ -65,22 +66,23 @@ struct DecodeArgs {
 };
 
 // Shared memory of one warp: a ring of NS group blocks, one mbarrier per
-// slot, and the query of the current item (fp32, up to 4 heads).
+// slot, and the query of the current pair (fp32, GQ heads), whose space the
+// score operand staging reuses once the query sits in registers.
 // Ring slots (group blocks in flight) per warp.
 #ifndef KVQ_DECODE_RING_2BIT
-#define KVQ_DECODE_RING_2BIT 3
+#define KVQ_DECODE_RING_2BIT 4
 #endif
 #ifndef KVQ_DECODE_RING_4BIT
 #define KVQ_DECODE_RING_4BIT 2
 #endif
 
-template <int BITS>
+template <int BITS, int GQ>
 struct WarpSmem {
   static constexpr int BB = block_bytes(BITS);
   static constexpr int NS = BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT;
   static constexpr int BAR_OFF = NS * BB;
   static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
-  static constexpr int BYTES = (Q_OFF + 4 * kD * 4 + 127) / 128 * 128;
+  static constexpr int BYTES = (Q_OFF + GQ * kD * 4 + 127) / 128 * 128;
   static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
 };
 
@@ -105,94 +107,108 @@ __device__ __forceinline__ uint32_t split_part(float x0, float x1, float lo_sel)
   return h2_as_u32(__floats2half2_rn(fmaf(-lo_sel, f.x, x0), fmaf(-lo_sel, f.y, x1)));
 }
 
-// Query side of the score mma.  build() returns, per group, bq[kt][j] = the
-// B-fragment register of this lane (column g: query head g/2, high part for
-// even g, low part for odd g; channels 16kt + 8j + 2q + {0,1}) and beta =
-// sum_d q_d min_d of head q, both for the normalized query q / 2^e.
+// Query side of the score mma.  Per group, lane L forms q_d * scale_d for
+// the four channels 16 kt + 8 j + 2 c + {0, 1} (kt = L % 8, c = L / 8,
+// j = 0, 1) of every query head, splits each product into an fp16 high part
+// and the fp16 rounding remainder, and stages both in shared memory in the
+// order of the B fragments: row (2 head + part) * 4 + c holds, for k-tiles
+// 0..7 and j = 0, 1, the channel pair (kt, j, c), 64 bytes per row with the
+// 16-byte chunks XOR-swizzled by (row / 2) % 4 so that neither the 8-byte
+// stores nor the 16-byte fragment loads meet a bank conflict.  Lane (g, q)
+// then loads B column g (query head g / 2, high part for even g, low part for
+// odd g; columns of heads that do not exist repeat the last head) with four
+// 16-byte loads.  beta = sum_d q_d min_d of head q is reduced across the warp.
+// Both use the normalized query q / 2^e (e per head, from frexp of its
+// largest |q_d|), so the products stay inside the fp16 range; qscale undoes
+// it together with the softmax scale.
 template <int GQ>
 struct QkOperand {
-  // GQ <= 2: the 64 channel pairs x heads x {high, low} are spread over all
-  // 32 lanes (lane = pair % PL + PL * part + 2 PL * head) and gathered with
-  // one shuffle per fragment register.  GQ == 4: each lane computes exactly
-  // the 16 pairs its own fragment holds.
-  static constexpr bool kGather = GQ <= 2;
-  static constexpr int PL = kGather ? 16 / GQ : 4;
-  static constexpr int NR = kGather ? 4 * GQ : 16;
-  float qv[2 * NR];
-  float lo_sel;
-  int pbase;
-  int head_lane;
-  float qscale;
+  float qv[GQ][4];  // channels c0, c0 + 1, c0 + 8, c0 + 9 of each head
+  float qscale;     // zscale * 2^e of head (lane & 3)
 
-  __device__ __forceinline__ int channel(int r) const {
-    return kGather ? 2 * (pbase + PL * r) : 16 * (r >> 1) + 8 * (r & 1) + 2 * pbase;
-  }
+  static __device__ __forceinline__ int chan0(int lane) { return 16 * (lane & 7) + 2 * (lane >> 3); }
+  static __device__ __forceinline__ int swz(int row, int chunk) { return row * 16 + 4 * (chunk ^ ((row >> 1) & 3)); }
 
   __device__ __forceinline__ void init(const float *q_s, int lane, float zscale) {
-    const int g = lane >> 2, q = lane & 3;
-    int hd;
-    if (kGather) {
-      pbase = lane % PL;
-      lo_sel = static_cast<float>((lane / PL) & 1);
-      hd = min(lane / (2 * PL), GQ - 1);
-    } else {
-      pbase = q;
-      lo_sel = static_cast<float>(g & 1);
-      hd = min(g >> 1, GQ - 1);
+    const int c0 = chan0(lane);
+    int ex_mine = 0;
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+      const float2 a = *reinterpret_cast<const float2 *>(q_s + h * kD + c0);
+      const float2 b = *reinterpret_cast<const float2 *>(q_s + h * kD + c0 + 8);
+      qv[h][0] = a.x;
+      qv[h][1] = a.y;
+      qv[h][2] = b.x;
+      qv[h][3] = b.y;
+      float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+      int ex;
+      frexpf(amax, &ex);  // |q / 2^ex| < 1
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[h][i] = ldexpf(qv[h][i], -ex);
+      if (h == min(lane & 3, GQ - 1)) ex_mine = ex;
     }
-    float amax = 0.f;
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      const int ch = channel(r);
-      qv[2 * r] = q_s[hd * kD + ch];
-      qv[2 * r + 1] = q_s[hd * kD + ch + 1];
-      amax = fmaxf(amax, fmaxf(fabsf(qv[2 * r]), fabsf(qv[2 * r + 1])));
-    }
-#pragma unroll
-    for (int off = 1; off < (kGather ? PL : 4); off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-    int ex;
-    frexpf(amax, &ex);  // |q / 2^ex| < 1 keeps q * scale inside the fp16 range
-#pragma unroll
-    for (int i = 0; i < 2 * NR; ++i) qv[i] = ldexpf(qv[i], -ex);
-    head_lane = kGather ? min(2 * PL * q, 31) : 8 * q;
-    qscale = ldexpf(zscale, __shfl_sync(kFull, ex, head_lane));
+    qscale = ldexpf(zscale, ex_mine);
   }
 
-  __device__ __forceinline__ void build(const float *ks, const float *km, int lane, uint32_t (&bq)[8][2],
-                                        float &beta) const {
-    const int g = lane >> 2, q = lane & 3;
-    uint32_t v[NR];
-    float bp = 0.f;
+  // stage: GQ * 512 bytes of this warp's shared memory, 16-byte aligned.
+  __device__ __forceinline__ void build(const float *ks, const float *km, uint32_t *stage, int lane,
+                                        uint32_t (&bq)[8][2], float &beta) const {
+    const int c0 = chan0(lane), kt = lane & 7, c = lane >> 3;
+    const float2 s0 = *reinterpret_cast<const float2 *>(ks + c0);
+    const float2 s1 = *reinterpret_cast<const float2 *>(ks + c0 + 8);
+    const float2 m0 = *reinterpret_cast<const float2 *>(km + c0);
+    const float2 m1 = *reinterpret_cast<const float2 *>(km + c0 + 8);
+    float bp[GQ];
+    __syncwarp();  // earlier reads of the stage (or of the query it aliases) are done
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      const int ch = channel(r);
-      const float2 sc = *reinterpret_cast<const float2 *>(ks + ch);
-      const float2 mn = *reinterpret_cast<const float2 *>(km + ch);
-      v[r] = split_part(qv[2 * r] * sc.x, qv[2 * r + 1] * sc.y, lo_sel);
-      bp = fmaf(qv[2 * r], mn.x, fmaf(qv[2 * r + 1], mn.y, bp));
+    for (int h = 0; h < GQ; ++h) {
+      const float x0 = qv[h][0] * s0.x, x1 = qv[h][1] * s0.y, x2 = qv[h][2] * s1.x, x3 = qv[h][3] * s1.y;
+      const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+      const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y), l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
+      const int rh = (2 * h) * 4 + c, rl = (2 * h + 1) * 4 + c;
+      *reinterpret_cast<uint2 *>(stage + swz(rh, kt >> 1) + 2 * (kt & 1)) = make_uint2(h2_as_u32(h01), h2_as_u32(h23));
+      *reinterpret_cast<uint2 *>(stage + swz(rl, kt >> 1) + 2 * (kt & 1)) = make_uint2(h2_as_u32(l01), h2_as_u32(l23));
+      bp[h] = fmaf(qv[h][0], m0.x, fmaf(qv[h][1], m0.y, fmaf(qv[h][2], m1.x, qv[h][3] * m1.y)));
     }
-    if (kGather) {
-      bp = lo_sel != 0.f ? 0.f : bp;  // each pair counted once, by its high-part lane
+    __syncwarp();
+    {
+      const int g = lane >> 2, q = lane & 3;
+      const int row = (2 * min(g >> 1, GQ - 1) + (g & 1)) * 4 + q;
 #pragma unroll
-      for (int off = 1; off < PL; off <<= 1) bp += __shfl_xor_sync(kFull, bp, off);
-      const int src_hi = PL * (g & 1) + 2 * PL * (g >> 1);
-#pragma unroll
-      for (int kt = 0; kt < 8; ++kt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int P = 8 * kt + 4 * j + q;
-          bq[kt][j] = __shfl_sync(kFull, v[(8 * kt) / PL], (P % PL + src_hi) & 31);
-        }
-    } else {
-#pragma unroll
-      for (int kt = 0; kt < 8; ++kt) {
-        bq[kt][0] = v[2 * kt];
-        bq[kt][1] = v[2 * kt + 1];
+      for (int i = 0; i < 4; ++i) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + swz(row, i));
+        bq[2 * i][0] = w.x;
+        bq[2 * i][1] = w.y;
+        bq[2 * i + 1][0] = w.z;
+        bq[2 * i + 1][1] = w.w;
       }
-      bp += __shfl_xor_sync(kFull, bp, 1);
-      bp += __shfl_xor_sync(kFull, bp, 2);
     }
-    beta = __shfl_sync(kFull, bp, head_lane) * qscale;
+    // beta of every head summed over the warp: halving exchanges leave one
+    // head's total per lane group, then lane (g, q) fetches head q's
+    if (GQ == 1) {
+      float v = bp[0];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = v * qscale;
+    } else if (GQ == 2) {
+      const bool up = lane & 16;
+      float v = (up ? bp[1] : bp[0]) + __shfl_xor_sync(kFull, up ? bp[0] : bp[1], 16);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = __shfl_sync(kFull, v, 16 * min(lane & 3, 1)) * qscale;  // lanes 0..15: head 0, 16..31: head 1
+    } else {
+      const bool b4 = lane & 16, b3 = lane & 8;
+      const float t0 = __shfl_xor_sync(kFull, b4 ? bp[0] : bp[2 % GQ], 16);
+      const float t1 = __shfl_xor_sync(kFull, b4 ? bp[1] : bp[3 % GQ], 16);
+      const float k0 = (b4 ? bp[2 % GQ] : bp[0]) + t0, k1 = (b4 ? bp[3 % GQ] : bp[1]) + t1;
+      float v = (b3 ? k1 : k0) + __shfl_xor_sync(kFull, b3 ? k0 : k1, 8);
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = __shfl_sync(kFull, v, 8 * (lane & 3)) * qscale;  // lane 8h holds head h = 2 b4 + b3
+    }
   }
 };
 
@@ -289,13 +305,16 @@ __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, int kt, i
 //
 // The decode work of a (sequence, KV head) pair is a run of units: first
 // kPassUnits units per 32-token pass over its fp16 sink + window tokens, then
-// one unit per packed group.  Pairs are laid out sequence-major; the plan
-// kernel writes base[s] (first unit of sequence s) and the total W.  Warp gw
-// of NW takes units [gw W / NW, (gw + 1) W / NW): equal work, contiguous
+// one unit per packed group.  Pairs are laid out sequence-major: sequence s
+// starts at unit base[s] = Hkv * (units per head of the sequences before
+// it), the line holds W units in all.  Each warp derives base[] and W from
+// seq_len itself (warp scans), or, for large batches, reads them from a plan
+// kernel.  Warp gw of NW takes units [gw W / NW, (gw + 1) W / NW): equal work, contiguous
 // across pair boundaries.  A warp leaves one partial result per pair it
 // touches (slot gw + pair) plus one per window pass it runs; the warp that
 // completes a pair's count merges them.
 constexpr int kPassUnits = 4;
+constexpr int kInlinePlanSeqs = 256;  // larger batches use the plan kernel
 
 struct PlanHeader {
   long long total;  // W
@@ -313,9 +332,9 @@ __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Split &spl,
   return kPassUnits * tp + ng;
 }
 
-// Per-sequence unit prefix (exclusive) times Hkv, the total, the merge
-// counters zeroed, and zero output rows for sequences with nothing to attend.
-// One CTA of 1024 threads.
+// Per-sequence unit prefix (exclusive) times Hkv, the total, and zero output
+// rows for sequences with nothing to attend, for batches too large to plan
+// inside the decode kernel.  One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
   __shared__ long long warp_sum[32];
   const int S = a.geo.S, H = a.geo.H;
@@ -358,7 +377,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
     a.base[S] = run * H;
     a.plan->total = run * H;
   }
-  for (int i = threadIdx.x; i < S * H; i += blockDim.x) a.counters[i] = 0;
   // sequences with nothing to attend (empty, or longer than the cache or the
   // planned bound) get zero output rows, one warp per sequence
   for (int s = warp; s < S; s += blockDim.x >> 5) {
@@ -388,11 +406,11 @@ __device__ __forceinline__ int touching_warps(long long P0, long long P1, long l
 // token 8*tau + g for query head q.
 template <int BITS, int GQ>
 __device__ __forceinline__ void group_scores(const uint8_t *blk, const QkOperand<GQ> &qo, const float (&kfac)[4],
-                                             int lane, float (&z)[4]) {
+                                             uint32_t *stage, int lane, float (&z)[4]) {
   uint32_t bq[8][2];
   float beta;
   qo.build(reinterpret_cast<const float *>(blk + off_ks(BITS)), reinterpret_cast<const float *>(blk + off_km(BITS)),
-           lane, bq, beta);
+           stage, lane, bq, beta);
   float acc[2][4];
   qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
 #pragma unroll
@@ -436,11 +454,14 @@ __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_
 #ifndef KVQ_DECODE_MIN_BLOCKS
 #define KVQ_DECODE_MIN_BLOCKS 4
 #endif
+#ifndef KVQ_DECODE_MIN_BLOCKS_GQ4
+#define KVQ_DECODE_MIN_BLOCKS_GQ4 3
+#endif
 
 template <int BITS, int GQ, bool ROPE>
-__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DECODE_MIN_BLOCKS))
+__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
     decode_kernel(DecodeArgs a) {
-  using WS = WarpSmem<BITS>;
+  using WS = WarpSmem<BITS, GQ>;
   constexpr int NS = WS::NS, BB = WS::BB;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -448,6 +469,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
   uint8_t *ring = smem + warp * WS::BYTES;
   uint64_t *full = reinterpret_cast<uint64_t *>(ring + WS::BAR_OFF);
   float *q_s = reinterpret_cast<float *>(ring + WS::Q_OFF);              // [GQ][D]
+  uint32_t *stage = reinterpret_cast<uint32_t *>(q_s);                   // score operand staging
   float2 *roff_s = reinterpret_cast<float2 *>(smem + kWarps * WS::BYTES);  // [32][65]
   const Geo &geo = a.geo;
 
@@ -461,19 +483,65 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
   }
   __syncthreads();  // the only CTA-wide barrier: from here each warp runs alone
 
-  const long long W = a.plan->total;
   const int NW = a.nw, gw = blockIdx.x * kWarps + warp;
   if (gw >= NW) return;
-  const long long ua = gw * W / NW, ub = (gw + 1) * W / NW;
-  if (ua >= ub) return;
   const bool head_valid = q < GQ;
-  const int H = geo.H;
+  const int H = geo.H, S = geo.S;
 
-  // the sequence holding unit ua: the last s with base[s] <= ua, by a
-  // 32-way search (base[0] = 0 <= ua keeps the answer in [lo, lo + n))
-  int s_first;
-  {
-    int lo = 0, n = geo.S;
+  // ---- the work line: total units W, and the sequence s_first holding this
+  // warp's first unit with its first unit sbase.  Small batches plan here,
+  // every warp on its own (one coalesced read of seq_len per 32 sequences);
+  // large ones read the plan kernel's prefix.
+  long long W, ua, ub, sbase = 0;
+  int s_first = 0;
+  if (a.base == nullptr) {
+    for (int s2 = gw; s2 < S; s2 += NW) {  // rows of sequences with nothing to attend
+      const int L = geo.seq_len[s2];
+      if (L > 0 && L <= geo.capacity && L <= a.max_len) continue;
+      if (lane == 0 && L > a.max_len) set_status(geo.status, KVQ_STATUS_MAX_LEN);
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(s2) * a.Hq * kD);
+      for (int i = lane; i < a.Hq * kD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    long long tot = 0;
+    for (int s2 = lane; s2 < S; s2 += 32) {
+      Split spl;
+      int tp, ng;
+      tot += seq_units(a, s2, spl, tp, ng);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFull, tot, off);
+    W = tot * H;
+    ua = gw * W / NW;
+    ub = (gw + 1) * W / NW;
+    if (ua >= ub) return;
+    long long run = 0;  // units of the sequences before chunk c, per KV head
+    for (int c = 0; c < S; c += 32) {
+      Split spl;
+      int tp, ng;
+      const long long v = c + lane < S ? seq_units(a, c + lane, spl, tp, ng) : 0;
+      long long incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long t = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += t;
+      }
+      const unsigned m = __ballot_sync(kFull, c + lane < S && (run + incl) * H > ua);
+      if (m) {
+        const int idx = __ffs(m) - 1;
+        s_first = c + idx;
+        sbase = (run + __shfl_sync(kFull, incl - v, idx)) * H;
+        break;
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+  } else {
+    W = a.plan->total;
+    ua = gw * W / NW;
+    ub = (gw + 1) * W / NW;
+    if (ua >= ub) return;
+    // the last s with base[s] <= ua, by a 32-way search (base[0] = 0 <= ua
+    // keeps the answer in [lo, lo + n))
+    int lo = 0, n = S;
     while (n > 32) {
       const int step = (n + 31) / 32;
       const int idx = lo + lane * step;
@@ -484,17 +552,26 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
     }
     const unsigned m = __ballot_sync(kFull, lane < n && a.base[lo + lane] <= ua);
     s_first = lo + 31 - __clz(m);
+    sbase = a.base[s_first];
   }
 
   // ---- fetch cursor: walks the packed groups of [ua, ub) in consumer order
+  // (fbase: first unit of sequence fs; its unit counts are re-derived from
+  // seq_len at each pair change rather than held in registers)
   uint32_t fseq = 0, cseq = 0;  // ring groups issued / consumed
-  int fs = s_first, fh = 0, fg = 0, fg_end = 0;
+  int fs = s_first, fh, fg = 0, fg_end = 0;
+  long long fbase = sbase;
   bool fdone = false;
-  auto fetch_pair = [&](int s, int h) {  // set the group range of pair (s, h)
+  {
     Split spl;
     int tp, ng;
-    const int u = seq_units(a, s, spl, tp, ng);
-    const long long P0 = a.base[s] + static_cast<long long>(h) * u;
+    fh = static_cast<int>((ua - fbase) / max(seq_units(a, fs, spl, tp, ng), 1));
+  }
+  auto fetch_pair = [&]() {  // the group range of pair (fs, fh); false past ub
+    Split spl;
+    int tp, ng;
+    const int u = seq_units(a, fs, spl, tp, ng);
+    const long long P0 = fbase + static_cast<long long>(fh) * u;
     const long long gb = P0 + kPassUnits * tp;
     fg = static_cast<int>(min(max(ua - gb, 0LL), static_cast<long long>(ng)));
     fg_end = static_cast<int>(min(max(ub - gb, 0LL), static_cast<long long>(ng)));
@@ -503,27 +580,24 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
   auto fetch_next_pair = [&]() {
     while (!fdone) {
       if (++fh == H) {
+        Split spl;
+        int tp, ng;
+        fbase += static_cast<long long>(H) * seq_units(a, fs, spl, tp, ng);
         fh = 0;
-        if (++fs >= geo.S) {
+        if (++fs >= S) {
           fdone = true;
           break;
         }
       }
-      if (!fetch_pair(fs, fh)) {
+      if (!fetch_pair()) {
         fdone = true;
         break;
       }
       if (fg < fg_end) break;
     }
   };
-  {
-    Split spl;
-    int tp, ng;
-    const int u = seq_units(a, fs, spl, tp, ng);
-    fh = static_cast<int>((ua - a.base[fs]) / max(u, 1));
-    if (!fetch_pair(fs, fh)) fdone = true;
-    if (!fdone && fg >= fg_end) fetch_next_pair();
-  }
+  if (!fetch_pair()) fdone = true;
+  if (!fdone && fg >= fg_end) fetch_next_pair();
   auto top_up = [&]() {
     while (!fdone && fseq - cseq < static_cast<uint32_t>(NS)) {
       if (lane == 0) {
@@ -540,21 +614,22 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
   };
   top_up();
 
-  // ---- consumer: pairs in order
+  // ---- consumer: pairs in order (cbase: first unit of sequence s)
   bool ok = true;
   int s = s_first;
+  long long cbase = sbase;
   Split spl;
   int tp, ng;
   int u = seq_units(a, s, spl, tp, ng);
-  int h = static_cast<int>((ua - a.base[s]) / max(u, 1));
+  int h = static_cast<int>((ua - cbase) / max(u, 1));
   while (ok) {
     if (u == 0) {  // sequence with nothing to attend: skip it
-      if (++s >= geo.S) break;
+      if (++s >= S) break;
       h = 0;
       u = seq_units(a, s, spl, tp, ng);
       continue;
     }
-    const long long P0 = a.base[s] + static_cast<long long>(h) * u, P1 = P0 + u;
+    const long long P0 = cbase + static_cast<long long>(h) * u, P1 = P0 + u;
     if (P0 >= ub) break;
     const long long lo = max(ua, P0), hi = min(ub, P1);
     const int pair = s * H + h;
@@ -701,9 +776,9 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
             }
             const uint8_t *ba = ring + sa * BB, *bb = ring + sb * BB;
             float za[4], zb[4];
-            group_scores<BITS, GQ>(ba, qo, kfac, lane, za);
+            group_scores<BITS, GQ>(ba, qo, kfac, stage, lane, za);
             if (two) {
-              group_scores<BITS, GQ>(bb, qo, kfac, lane, zb);
+              group_scores<BITS, GQ>(bb, qo, kfac, stage, lane, zb);
             } else {
               zb[0] = zb[1] = zb[2] = zb[3] = -INFINITY;
             }
@@ -887,6 +962,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
     if (lane == 0) last = atom_add_acq_rel(&a.counters[pair], npart) + npart == expect;
     if (__shfl_sync(kFull, last, 0)) {
       __threadfence();
+      if (lane == 0) a.counters[pair] = 0;  // ready for the next call
       const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
       for (int hh = 0; hh < GQ; ++hh) {
         float M = -INFINITY;
@@ -924,7 +1000,8 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? 3 : KVQ_DEC
     if (P1 >= ub) break;
     if (++h == H) {
       h = 0;
-      if (++s >= geo.S) break;
+      cbase += static_cast<long long>(H) * u;
+      if (++s >= S) break;
       u = seq_units(a, s, spl, tp, ng);
     }
   }
@@ -959,7 +1036,7 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 // device's SM count (cached per device ordinal).
 template <int BITS, int GQ, bool ROPE>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
-  using WS = WarpSmem<BITS>;
+  using WS = WarpSmem<BITS, GQ>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
   auto kern = decode_kernel<BITS, GQ, ROPE>;
   static int resident[64] = {};
@@ -1004,8 +1081,10 @@ static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   int nw = g_warps_override ? g_warps_override : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
   nw = max(nw, 1);
   a.nw = nw;
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.base != nullptr) {
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   decode_kernel<BITS, GQ, ROPE><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
@@ -1047,8 +1126,8 @@ DecodePlan plan_decode(const Geo &geo, int Hq, int max_len) {
 }
 
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
-                          void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
-                          uint64_t *launches) {
+                          void *workspace, const DecodePlan &p, int max_len, bool zero_counters,
+                          cudaStream_t stream, uint64_t *launches) {
   DecodeArgs a;
   a.geo = geo;
   a.Hq = Hq;
@@ -1059,7 +1138,10 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.part_o = reinterpret_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
   a.counters = reinterpret_cast<int *>(ws + p.off_cnt);
-  a.base = reinterpret_cast<long long *>(ws + p.off_base);
+  // batches of up to kInlinePlanSeqs sequences are planned inside the decode
+  // kernel; larger ones by a one-CTA plan kernel
+  const bool inline_plan = geo.S <= kInlinePlanSeqs;
+  a.base = inline_plan ? nullptr : reinterpret_cast<long long *>(ws + p.off_base);
   a.plan = reinterpret_cast<PlanHeader *>(ws + p.off_hdr);
   a.nw = 0;
   a.pass_slot0 = p.pass_slot0;
@@ -1067,7 +1149,10 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.max_len = max_len;
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
+  if (zero_counters &&
+      (e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(geo.S) * geo.H * sizeof(int), stream)) != cudaSuccess)
+    return e;
   if (geo.pre_rope) {
     const int n = (p.n_base + kG) * 64;
     rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(reinterpret_cast<float2 *>(ws + p.off_rope), p.n_base,
@@ -1078,7 +1163,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   }
   const int gq = Hq / geo.H;
   e = geo.bits == 2 ? launch_b<2>(a, gq, stream) : launch_b<4>(a, gq, stream);
-  *launches += 2;
+  *launches += inline_plan ? 1 : 2;
   return e;
 }
 

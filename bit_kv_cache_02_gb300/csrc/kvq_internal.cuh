@@ -196,8 +196,12 @@ cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __hal
 cudaError_t launch_dequant(const Geo &geo, float *k_out, float *v_out, cudaStream_t stream, uint64_t *launches);
 DecodePlan plan_decode(const Geo &geo, int Hq, int max_len);
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
-                          void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
-                          uint64_t *launches);
+                          void *workspace, const DecodePlan &p, int max_len, bool zero_counters,
+                          cudaStream_t stream, uint64_t *launches);
+// kv_decode_attn that first clears the workspace's merge counters (for
+// scratch shared by calls of different geometries).
+int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                         uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream);
 int set_decode_warps(int warps);
 
 }  // namespace kvq

@@ -50,5 +50,8 @@ extern "C" int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_head
   void *scratch = nullptr;
   const int e = scratch_for_current_device(&scratch);
   if (e != KVQ_OK) return e;
-  return kv_decode_attn(cache, num_q_heads, q, softmax_scale, out, scratch, kScratchBytes, max_len, stream);
+  // the array is shared by calls of every geometry, so each call clears its
+  // own merge counters instead of relying on the previous call to leave them zero
+  return kvq::decode_attn_clearing(cache, num_q_heads, q, softmax_scale, out, scratch, kScratchBytes, max_len,
+                                   stream);
 }

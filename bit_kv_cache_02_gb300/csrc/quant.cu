@@ -51,24 +51,14 @@ __device__ __noinline__ uint32_t exact_code(float x, float mn, float scale) {
 
 constexpr int kVStride = kG + 2;  // padded row (in halves) of the transposed value tile
 
-// One CTA quantizes one 32-token group of one (sequence, KV head).
-// grid = (group slot, KV head, sequence).  Tokens of the group come from the
-// old window (stream index < n0) or from the new input.
+// The CTA (kQuantThreads threads) quantizes the 32-token group of (sequence
+// s, KV head h) starting at stream index i0.  Its tokens come from the old
+// window (stream index < n0, window slot i - Lq0) or from the new input
+// (new token i + num_sink - L0).
 template <int BITS>
-__global__ void __launch_bounds__(kQuantThreads) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
-                                                                    const __half *__restrict__ v_new,
-                                                                    const int *__restrict__ new_len, int max_new) {
-  const int s = blockIdx.z, h = blockIdx.y, gslot = blockIdx.x;
-  const int L0 = geo.seq_len[s];
-  const int nn = new_len[s];
-  if (nn < 0 || nn > max_new || L0 + nn > geo.capacity || L0 < 0) return;  // reported by the tail kernel
-  const int n0 = max(L0 - geo.ns, 0);
-  const int Lq0 = n0 - n0 % geo.R;
-  const int n1 = max(L0 + nn - geo.ns, 0);
-  const int Lq1 = n1 - n1 % geo.R;
-  if (gslot >= (Lq1 - Lq0) / kG) return;
-  const int i0 = Lq0 + gslot * kG;  // first stream index of this group
-
+__device__ __forceinline__ void flush_group(const Geo &geo, int s, int h, int i0, int n0, int Lq0, int L0,
+                                            const __half *__restrict__ k_new, const __half *__restrict__ v_new,
+                                            int max_new) {
   __shared__ __align__(16) __half sk[kG][kD];         // keys, token rows
   __shared__ __align__(16) __half svT[kD][kVStride];  // values, channel rows
   __shared__ __align__(16) SliceQ kq[kD];
@@ -213,6 +203,149 @@ __global__ void __launch_bounds__(kQuantThreads) quant_flush_kernel(Geo geo, con
   }
 }
 
+// Length bits of seq_len; while the fused step append runs, the bits above
+// count the CTAs of a sequence that have finished with it.
+constexpr int kLenBits = 22;
+constexpr int kLenMask = (1 << kLenBits) - 1;
+
+// One CTA quantizes one 32-token group of one (sequence, KV head).
+// grid = (group slot, KV head, sequence).
+template <int BITS>
+__global__ void __launch_bounds__(kQuantThreads) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
+                                                                    const __half *__restrict__ v_new,
+                                                                    const int *__restrict__ new_len, int max_new) {
+  const int s = blockIdx.z, h = blockIdx.y, gslot = blockIdx.x;
+  const int L0 = geo.seq_len[s];
+  const int nn = new_len[s];
+  if (nn < 0 || nn > max_new || L0 + nn > geo.capacity || L0 < 0) return;  // reported by the tail kernel
+  const int n0 = max(L0 - geo.ns, 0);
+  const int Lq0 = n0 - n0 % geo.R;
+  const int n1 = max(L0 + nn - geo.ns, 0);
+  const int Lq1 = n1 - n1 % geo.R;
+  if (gslot >= (Lq1 - Lq0) / kG) return;
+  flush_group<BITS>(geo, s, h, Lq0 + gslot * kG, n0, Lq0, L0, k_new, v_new, max_new);
+}
+
+// Copy the new tokens of (sequence s, KV heads [h0, h1)) that land in the
+// sink or in the window; threads tid = 0 .. nthr-1 of the CTA share the work.
+__device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1, int L0, int nn,
+                                          const __half *__restrict__ k_new, const __half *__restrict__ v_new,
+                                          int max_new, int tid, int nthr) {
+  const int n1 = max(L0 + nn - geo.ns, 0);
+  const int Lq1 = n1 - n1 % geo.R;
+  const int j_sink_end = min(max(geo.ns - L0, 0), nn);      // new tokens [0, j_sink_end) -> sink
+  const int j_win = max(Lq1 + geo.ns - L0, j_sink_end);      // new tokens [j_win, nn) -> window
+  const int n_copy = j_sink_end + max(nn - j_win, 0);
+  constexpr int C16 = kD / 8;  // 16-byte chunks per token row
+  for (int idx = tid; idx < (h1 - h0) * n_copy * C16; idx += nthr) {
+    const int c8 = idx % C16;
+    const int k = (idx / C16) % n_copy;
+    const int h = h0 + idx / (C16 * n_copy);
+    const int j = k < j_sink_end ? k : j_win + (k - j_sink_end);
+    const int pos = L0 + j;
+    const size_t sh = static_cast<size_t>(s) * geo.H + h;
+    __half *dk, *dv;
+    if (pos < geo.ns) {
+      dk = geo.k_sink + (sh * geo.ns + pos) * kD;
+      dv = geo.v_sink + (sh * geo.ns + pos) * kD;
+    } else {
+      const int slot = pos - geo.ns - Lq1;
+      dk = geo.k_res + (sh * geo.R + slot) * kD;
+      dv = geo.v_res + (sh * geo.R + slot) * kD;
+    }
+    const size_t src = (sh * max_new + j) * kD + c8 * 8;
+    reinterpret_cast<uint4 *>(dk)[c8] = *reinterpret_cast<const uint4 *>(k_new + src);
+    reinterpret_cast<uint4 *>(dv)[c8] = *reinterpret_cast<const uint4 *>(v_new + src);
+  }
+}
+
+// Append of at most R new tokens per sequence in one kernel, one CTA per
+// (KV head, sequence): at most one window fills, and the CTA then quantizes
+// its R / 32 groups one after another.  Each CTA adds 1 << kLenBits to
+// seq_len[s] once it needs seq_len no more; the CTA that completes the count
+// (Hkv arrivals) stores the final length (clearing the count) and reports
+// bad lengths, and no CTA reads seq_len[s] after that store.  When no window
+// fills, a CTA arrives right after reading the length and copies its head's
+// new tokens into the window (or sink), prefetched at launch.  When one
+// fills, the copy would overwrite window slots the sequence's other CTAs may
+// still be quantizing, so the CTAs arrive after quantizing and the last one
+// copies the new tokens of every head.
+template <int BITS>
+__global__ void __launch_bounds__(kQuantThreads) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
+                                                                    const __half *__restrict__ v_new,
+                                                                    const int *__restrict__ new_len, int max_new) {
+  const int s = blockIdx.y, h = blockIdx.x;
+  __shared__ int s_last, s_old;
+  constexpr int C16 = kD / 8;  // 16-byte chunks per token row
+  // thread (pj, pc) prefetches chunk pc of new token pj of this head
+  const int pj = threadIdx.x / C16, pc = threadIdx.x % C16;
+  const bool pre = pj < min(max_new, kQuantThreads / C16);
+  uint4 pk = make_uint4(0u, 0u, 0u, 0u), pv = pk;
+  const size_t sh = static_cast<size_t>(s) * geo.H + h;
+  if (pre) {
+    const size_t src = (sh * max_new + pj) * kD + pc * 8;
+    pk = *reinterpret_cast<const uint4 *>(k_new + src);
+    pv = *reinterpret_cast<const uint4 *>(v_new + src);
+  }
+  const int raw = geo.seq_len[s];  // the length, plus arrivals of other CTAs in the high bits
+  const int nn = new_len[s];
+  if (raw < 0) {  // a negative length: no CTA of the sequence arrives, so it stays as it is
+    if (threadIdx.x == 0) set_status(geo.status, KVQ_STATUS_BAD_LEN);
+    return;
+  }
+  const int L0 = raw & kLenMask;
+  const bool bad_len = nn < 0 || nn > max_new;
+  const bool over = !bad_len && L0 + nn > geo.capacity;
+  const int n0 = max(L0 - geo.ns, 0);
+  const int Lq0 = n0 - n0 % geo.R;
+  const int n1 = max(L0 + nn - geo.ns, 0);
+  const int Lq1 = n1 - n1 % geo.R;
+  const bool flush = !bad_len && !over && Lq1 != Lq0;
+
+  auto arrive = [&]() {  // thread 0; s_last / s_old valid after the next barrier
+    const int old = atomicAdd(&geo.seq_len[s], 1 << kLenBits);
+    s_old = old - (geo.H - 1) * (1 << kLenBits);  // seq_len[s] before this kernel
+    s_last = (old >> kLenBits) == geo.H - 1;
+  };
+  if (!flush) {
+    if (threadIdx.x == 0) arrive();
+    if (!bad_len && !over) {
+      if (nn <= kQuantThreads / C16) {
+        if (pj < nn) {  // no window fills: every new token goes to the sink or the window
+          const int pos = L0 + pj;
+          __half *dk, *dv;
+          if (pos < geo.ns) {
+            dk = geo.k_sink + (sh * geo.ns + pos) * kD;
+            dv = geo.v_sink + (sh * geo.ns + pos) * kD;
+          } else {
+            const int slot = pos - geo.ns - Lq1;
+            dk = geo.k_res + (sh * geo.R + slot) * kD;
+            dv = geo.v_res + (sh * geo.R + slot) * kD;
+          }
+          reinterpret_cast<uint4 *>(dk)[pc] = pk;
+          reinterpret_cast<uint4 *>(dv)[pc] = pv;
+        }
+      } else {
+        copy_tail(geo, s, h, h + 1, L0, nn, k_new, v_new, max_new, threadIdx.x, blockDim.x);
+      }
+    }
+    __syncthreads();
+  } else {
+    for (int i0 = Lq0; i0 < Lq1; i0 += kG) {
+      flush_group<BITS>(geo, s, h, i0, n0, Lq0, L0, k_new, v_new, max_new);
+      __syncthreads();  // the group's reads are done and its shared tiles free again
+    }
+    if (threadIdx.x == 0) arrive();
+    __syncthreads();
+    if (s_last) copy_tail(geo, s, 0, geo.H, L0, nn, k_new, v_new, max_new, threadIdx.x, blockDim.x);
+  }
+  if (s_last && threadIdx.x == 0) {
+    if (bad_len) set_status(geo.status, KVQ_STATUS_BAD_LEN);
+    if (over) set_status(geo.status, KVQ_STATUS_CAPACITY);
+    geo.seq_len[s] = bad_len || over ? s_old : L0 + nn;
+  }
+}
+
 // One CTA per sequence: copy the new tokens that land in the sink or in the
 // window, then advance seq_len (one CTA owns a sequence, so no other CTA
 // reads seq_len[s] after it is written).
@@ -230,32 +363,7 @@ __global__ void __launch_bounds__(256) append_tail_kernel(Geo geo, const __half 
     if (threadIdx.x == 0) set_status(geo.status, KVQ_STATUS_CAPACITY);
     return;
   }
-  const int n1 = max(L0 + nn - geo.ns, 0);
-  const int Lq1 = n1 - n1 % geo.R;
-  const int j_sink_end = min(max(geo.ns - L0, 0), nn);      // new tokens [0, j_sink_end) -> sink
-  const int j_win = max(Lq1 + geo.ns - L0, j_sink_end);      // new tokens [j_win, nn) -> window
-  const int n_copy = j_sink_end + (nn - j_win);
-  constexpr int C16 = kD / 8;  // 16-byte chunks per token row
-  for (int idx = threadIdx.x; idx < geo.H * n_copy * C16; idx += blockDim.x) {
-    const int c8 = idx % C16;
-    const int k = (idx / C16) % n_copy;
-    const int h = idx / (C16 * n_copy);
-    const int j = k < j_sink_end ? k : j_win + (k - j_sink_end);
-    const int pos = L0 + j;
-    const size_t sh = static_cast<size_t>(s) * geo.H + h;
-    __half *dk, *dv;
-    if (pos < geo.ns) {
-      dk = geo.k_sink + (sh * geo.ns + pos) * kD;
-      dv = geo.v_sink + (sh * geo.ns + pos) * kD;
-    } else {
-      const int slot = pos - geo.ns - Lq1;
-      dk = geo.k_res + (sh * geo.R + slot) * kD;
-      dv = geo.v_res + (sh * geo.R + slot) * kD;
-    }
-    const size_t src = (sh * max_new + j) * kD + c8 * 8;
-    reinterpret_cast<uint4 *>(dk)[c8] = *reinterpret_cast<const uint4 *>(k_new + src);
-    reinterpret_cast<uint4 *>(dv)[c8] = *reinterpret_cast<const uint4 *>(v_new + src);
-  }
+  copy_tail(geo, s, 0, geo.H, L0, nn, k_new, v_new, max_new, threadIdx.x, blockDim.x);
   __syncthreads();
   if (threadIdx.x == 0) geo.seq_len[s] = L0 + nn;
 }
@@ -266,6 +374,16 @@ int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R /
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                 int max_new, cudaStream_t stream, uint64_t *launches) {
+  // a decode-sized append (at most one window fills): one kernel
+  if (max_new <= geo.R && geo.capacity <= kLenMask && geo.H < (1 << (31 - kLenBits))) {
+    dim3 grid(geo.H, geo.S);
+    if (geo.bits == 2)
+      step_append_kernel<2><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+    else
+      step_append_kernel<4><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+    ++*launches;
+    return cudaGetLastError();
+  }
   const int gmax = max_flush_groups(geo.R, max_new);
   if (gmax > 0) {
     dim3 grid(gmax, geo.H, geo.S);

@@ -145,7 +145,11 @@ int64_t kvq_buffer_bytes(const kvq_cache *cache, int32_t which);
  * clamped; scale 0 gives code 0) and the window empties.  The result is the
  * same for any split of a token stream into appends.  A sequence whose
  * new_len is out of range or would exceed capacity is left unchanged and the
- * matching KVQ_STATUS_* bit is set.  Enqueues two kernels.
+ * matching KVQ_STATUS_* bit is set.  When max_new <= residual (at most one
+ * window fills), capacity < 2^22 and num_kv_heads < 512, enqueues one
+ * kernel, which counts its finished blocks in the high bits of
+ * seq_len while it runs (seq_len is exact again when the kernel ends);
+ * otherwise two kernels (quantize, then copy and advance seq_len).
  */
 int kv_quant_append(const kvq_cache *cache, const uint16_t *k_new,
                     const uint16_t *v_new, const int32_t *new_len,
@@ -177,8 +181,12 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  *   out     [S][Hq][D] fp16, written for every row (zeros when seq_len is 0).
  *   workspace, workspace_bytes  device scratch of at least
  *           kv_decode_workspace_bytes(cache, num_q_heads, max_len) bytes,
- *           256-byte aligned; no contents need to be preserved between calls
- *           (the call zeroes its merge counters itself).
+ *           256-byte aligned, owned by the library between calls.  It must
+ *           be zero-filled before its first use with a given cache geometry
+ *           and num_q_heads: the call's merge counters live in it, and every
+ *           call that ends without KVQ_STATUS_TIMEOUT leaves them zero again
+ *           (so no clearing step runs per call).  After a timeout, or before
+ *           reusing it for another geometry, zero it again.
  *   max_len host bound on every seq_len (sizes the RoPE table); a
  *           sequence longer than max_len gets a zero output row and sets
  *           KVQ_STATUS_MAX_LEN.
@@ -189,9 +197,9 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  * window, then packed groups -- is cut into equal contiguous ranges, one per
  * warp; the kernel dequantizes in registers, forms scores, runs an online
  * softmax over each range, and the last range of a pair to finish merges its
- * partials (log-sum-exp).  Enqueues a plan kernel (work prefix over the
- * sequences, counters zeroed, rows of empty sequences zeroed) and the decode
- * kernel, plus a RoPE table kernel when pre_rope.
+ * partials (log-sum-exp).  Enqueues the decode kernel, plus a plan kernel
+ * (work prefix over the sequences) when S > 256 and a RoPE table kernel when
+ * pre_rope.
  */
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    const uint16_t *q, float softmax_scale, uint16_t *out,

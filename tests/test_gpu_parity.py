@@ -261,6 +261,58 @@ def test_split_sizes_agree(kvq, warps):
         kvq.set_decode_warps(0)
 
 
+@pytest.mark.parametrize("S", [200, 300])
+def test_many_sequences_with_empty_and_overlong(kvq, S):
+    """Batches planned inside the decode kernel (S <= 256) and by the plan
+    kernel (S > 256): ragged lengths with empty sequences and sequences
+    longer than max_len, whose rows come back zero with
+    KVQ_STATUS_MAX_LEN set."""
+    H, T, max_len = 1, 200, 150
+    rng = np.random.default_rng(S)
+    lens = rng.integers(0, T + 1, S).astype(np.int32)
+    lens[::17] = 0
+    k, v = _rand_kv(S, H, T, seed=S + 1)
+    cache, orc = _build(kvq, S, H, T + 8, 2, ns=1)
+    _append(kvq, cache, orc, k, v, lens)
+    q = _rand_q(S, 2 * H, seed=5)
+    dq = torch.from_numpy(q).cuda()
+    out = torch.full_like(dq, float("nan"))
+    ws = kvq.alloc_workspace(cache, 2 * H, max_len)
+    kvq.kv_decode_attn(cache, dq, out, ws, max_len)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    over = lens > max_len
+    assert over.any() and (lens == 0).any()
+    assert bool(int(cache.status.item()) & kvq.KVQ_STATUS_MAX_LEN) == bool(over.any())
+    assert (got[over | (lens == 0)] == 0).all()
+    want = orc.attention(q)
+    keep = ~over
+    _attn_close(got[keep], want[keep])
+
+
+def test_workspace_reused_across_calls(kvq):
+    """The merge counters a call leaves behind are the zeros the next call
+    starts from: several calls on one workspace, with the work cut into
+    different numbers of warp ranges, all match the oracle."""
+    S, H, T = 3, 2, 700
+    k, v = _rand_kv(S, H, T, seed=21)
+    cache, orc = _build(kvq, S, H, 720, 2)
+    _append(kvq, cache, orc, k, v, [700, 333, 64])
+    ws = kvq.alloc_workspace(cache, 2 * H, 720)
+    try:
+        for i, warps in enumerate([0, 5, 0, 77, 1, 0]):
+            kvq.set_decode_warps(warps)
+            q = _rand_q(S, 2 * H, seed=30 + i)
+            dq = torch.from_numpy(q).cuda()
+            out = torch.empty_like(dq)
+            kvq.kv_decode_attn(cache, dq, out, ws, 720)
+            torch.cuda.synchronize()
+            _attn_close(out.cpu().numpy(), orc.attention(q))
+    finally:
+        kvq.set_decode_warps(0)
+    assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_ties_and_near_ties_bit_exact(kvq, bits):
     """Inputs on a half-step grid put many quotients exactly on rounding
