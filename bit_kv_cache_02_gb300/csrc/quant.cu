@@ -5,22 +5,31 @@
 // and third paragraph (newest tokens kept in full precision, quantized in
 // blocks when the window fills); "KV cache quantization", "What they report"
 // (first token kept in fp16).
+//
+// A CTA of 256 threads quantizes one group at a time: its 32 key and value
+// rows are loaded into registers (the next group's while the current one is
+// processed), stored to shared tiles laid out so that every later access is
+// free of bank conflicts, reduced to per-channel key and per-token value
+// min/max, and packed into the block format, which is staged in shared
+// memory and written with one bulk copy.
 #include "kvq_internal.cuh"
 
 namespace kvq {
 
 constexpr int kQuantThreads = 256;
-constexpr float kMagic = 12582912.f;  // 1.5 * 2^23: x + kMagic rounds x to an integer (half to even)
+constexpr float kMagic = 12582912.f;    // 1.5 * 2^23: x + kMagic rounds x to an integer (half to even)
+constexpr float kPackBase = 8388608.f;  // 2^23: the low bits of 2^23 + n hold the integer n < 2^23
 
 // Per-slice (one key channel of a group, or one value token) constants of
 // the code computation.  The code is rne(fl(fl(x - min) / scale)) clamped
 // to [0, 2^b - 1], scale == 0 giving 0.  It is first evaluated from
-// y' = fma(x, rcp, c) with rcp = fl(1/scale) and c = fl(-min * rcp), which
-// differs from both the exact quotient (x - min) / scale and the IEEE
-// result fl(fl(x - min) / scale) by less than half of `tol`
-// ((2^b) * 2^-23 + |c| * 2^-24 each, from the three roundings); when y'
-// lies farther than `tol` from every rounding boundary k + 1/2, all three
-// round to the same integer.  Otherwise the IEEE subtract and divide decide.
+// y' = fma(x, rcp, c) with rcp = 1/scale to 2^-22 relative (the hardware
+// approximate reciprocal) and c = fl(-min * rcp).  With Q = (x - min) /
+// scale <= 2^b - 1 (to 2^-24), y' - Q stays below (2^b - 1) (2^-22 + 2^-24)
+// + |c| 2^-24 and the IEEE result fl(fl(x - min) / scale) - Q below (2^b -
+// 1) 2^-23, both under tol / 2 = 2^b 2^-21 + |c| 2^-23; when y' lies
+// farther than tol from every rounding boundary k + 1/2, all three round to
+// the same integer.  Otherwise the IEEE subtract and divide decide.
 struct SliceQ {
   float rcp, c, tol, mn;
 };
@@ -28,18 +37,12 @@ struct SliceQ {
 __device__ __forceinline__ SliceQ make_slice(float mn, float scale, float levels) {
   SliceQ q;
   q.mn = mn;
-  q.rcp = scale > 0.f ? __frcp_rn(scale) : 0.f;
+  float rcp;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rcp) : "f"(scale));
+  q.rcp = scale > 0.f ? rcp : 0.f;
   q.c = __fmul_rn(-mn, q.rcp);
-  q.tol = (levels + 1.f) * 4.76837158203125e-07f + fabsf(q.c) * 2.384185791015625e-07f;  // 2^-21, 2^-22
+  q.tol = (levels + 1.f) * 9.5367431640625e-07f + fabsf(q.c) * 2.384185791015625e-07f;  // 2^-20, 2^-22
   return q;
-}
-
-// Fast code of x; `near` is set when y' is within tol of a rounding boundary.
-__device__ __forceinline__ uint32_t fast_code(float x, const SliceQ &q, bool &near) {
-  const float y = fmaf(x, q.rcp, q.c);
-  const float t = y + kMagic;
-  near = fabsf(fabsf(y - (t - kMagic)) - 0.5f) <= q.tol;
-  return __float_as_uint(t) - __float_as_uint(kMagic);
 }
 
 // The code by the IEEE subtract and divide (rarely needed, kept out of line).
@@ -49,157 +52,355 @@ __device__ __noinline__ uint32_t exact_code(float x, float mn, float scale) {
   return static_cast<uint32_t>(fminf(fmaxf(r, 0.f), float((1 << BITS) - 1)));
 }
 
-constexpr int kVStride = kG + 2;  // padded row (in halves) of the transposed value tile
+// ------------------------------------------------- paired fp32 arithmetic
 
-// The CTA (kQuantThreads threads) quantizes the 32-token group of (sequence
-// s, KV head h) starting at stream index i0.  Its tokens come from the old
-// window (stream index < n0, window slot i - Lq0) or from the new input
-// (new token i + num_sink - L0).
-template <int BITS>
-__device__ __forceinline__ void flush_group(const Geo &geo, int s, int h, int i0, int n0, int Lq0, int L0,
-                                            const __half *__restrict__ k_new, const __half *__restrict__ v_new,
-                                            int max_new) {
-  __shared__ __align__(16) __half sk[kG][kD];         // keys, token rows
-  __shared__ __align__(16) __half svT[kD][kVStride];  // values, channel rows
-  __shared__ __align__(16) SliceQ kq[kD];
-  __shared__ __align__(16) SliceQ vq[kG];
-  __shared__ float k_sc[kD], v_sc[kG];
+typedef unsigned long long f2x;  // two fp32 lanes in one 64-bit register
 
-  const float levels = float((1 << BITS) - 1);
-  const size_t sh = static_cast<size_t>(s) * geo.H + h;
-  uint8_t *blk = geo.blocks + (sh * geo.max_groups + i0 / kG) * static_cast<size_t>(block_bytes(BITS));
-  {
-    // thread (p, c8): tokens 2p and 2p+1, channels 8 c8 .. 8 c8 + 7
-    const int p = threadIdx.x >> 4, c8 = threadIdx.x & 15;
-    uint4 kr[2], vr[2];
+__device__ __forceinline__ f2x f2_pack(float a, float b) {
+  f2x u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(a), "f"(b));
+  return u;
+}
+__device__ __forceinline__ float2 f2_unpack(f2x u) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(u));
+  return f;
+}
+__device__ __forceinline__ f2x f2_fma(f2x a, f2x b, f2x c) {
+  f2x d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2x f2_add(f2x a, f2x b) {
+  f2x d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_sub(f2x a, f2x b) {
+  f2x d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ------------------------------------------------------- shared tiles
+
+// Value tile: the token-pair word (tokens 2 tw, 2 tw + 1) of channel ch.
+// Two channels (ch, ch ^ 1) share a 32-word row, XOR-swizzled so that both
+// the transposing stores (fixed channel offset, 16 channel blocks x 2 token
+// pairs per warp) and the packing loads (fixed field, 8 channels x 4 token
+// pairs per warp) touch 32 distinct banks.
+__device__ __forceinline__ int vword(int ch, int tw) {
+  const int rp = ch >> 1;
+  const int swz = (4 * (rp & 3)) ^ (2 * ((rp >> 2) & 15));
+  return rp * 32 + ((((ch & 1) << 4) + tw) ^ swz);
+}
+
+struct __align__(128) QuantSmem {
+  uint32_t k[kG * 64];       // key tile: word (token, channel pair) at token * 64 + pair
+  uint32_t v[kD * 16];       // value tile: vword()
+  uint32_t kstat[8][64][2];  // per-warp key (min, max) half2 of each channel pair
+  SliceQ kq[kD];             // key channel constants
+  SliceQ vq[kG];             // value token constants
+  uint32_t vstat[kG / 2][2]; // value (min, max) half2 of each token pair
+  __align__(128) uint8_t blk[block_bytes(4)];  // the packed block being built
+};
+
+// One group's rows in registers: thread (p, c8) holds the 16-byte chunk c8
+// (channels 8 c8 .. 8 c8 + 7) of tokens 2p and 2p + 1 of the keys and values.
+struct GroupRegs {
+  uint4 k[2], v[2];
+};
+
+// Where the 32 tokens of a group come from: stream index i < n0 sits in
+// window slot i - Lq0, later ones are new token i + num_sink - L0.
+struct GroupSrc {
+  int s, h, i0, n0, Lq0, L0;
+};
+
+__device__ __forceinline__ void load_group(GroupRegs &r, const Geo &geo, const GroupSrc &g,
+                                           const __half *__restrict__ k_new, const __half *__restrict__ v_new,
+                                           int max_new) {
+  const int p = threadIdx.x >> 4, c8 = threadIdx.x & 15;
+  const size_t sh = static_cast<size_t>(g.s) * geo.H + g.h;
+  if (g.i0 >= g.n0) {  // the whole group is new input (every prefill group)
+    const __half *pk = k_new + (sh * max_new + (g.i0 + 2 * p + geo.ns - g.L0)) * kD + c8 * 8;
+    const __half *pv = v_new + (sh * max_new + (g.i0 + 2 * p + geo.ns - g.L0)) * kD + c8 * 8;
+    r.k[0] = *reinterpret_cast<const uint4 *>(pk);
+    r.k[1] = *reinterpret_cast<const uint4 *>(pk + kD);
+    r.v[0] = *reinterpret_cast<const uint4 *>(pv);
+    r.v[1] = *reinterpret_cast<const uint4 *>(pv + kD);
+    return;
+  }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int i = i0 + 2 * p + r;
-      const __half *pk, *pv;
-      if (i < n0) {
-        const size_t off = (sh * geo.R + (i - Lq0)) * kD;
-        pk = geo.k_res + off;
-        pv = geo.v_res + off;
-      } else {
-        const size_t off = (sh * max_new + (i + geo.ns - L0)) * kD;
-        pk = k_new + off;
-        pv = v_new + off;
-      }
-      kr[r] = *reinterpret_cast<const uint4 *>(pk + c8 * 8);
-      vr[r] = *reinterpret_cast<const uint4 *>(pv + c8 * 8);
+  for (int t = 0; t < 2; ++t) {
+    const int i = g.i0 + 2 * p + t;
+    const __half *pk, *pv;
+    if (i < g.n0) {
+      const size_t off = (sh * geo.R + (i - g.Lq0)) * kD;
+      pk = geo.k_res + off;
+      pv = geo.v_res + off;
+    } else {
+      const size_t off = (sh * max_new + (i + geo.ns - g.L0)) * kD;
+      pk = k_new + off;
+      pv = v_new + off;
     }
-    *reinterpret_cast<uint4 *>(&sk[2 * p][c8 * 8]) = kr[0];
-    *reinterpret_cast<uint4 *>(&sk[2 * p + 1][c8 * 8]) = kr[1];
-    const __half *va = reinterpret_cast<const __half *>(&vr[0]);
-    const __half *vb = reinterpret_cast<const __half *>(&vr[1]);
+    r.k[t] = *reinterpret_cast<const uint4 *>(pk + c8 * 8);
+    r.v[t] = *reinterpret_cast<const uint4 *>(pv + c8 * 8);
+  }
+}
+
+__device__ __forceinline__ uint32_t h2min(uint32_t a, uint32_t b) {
+  const __half2 m = __hmin2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&m);
+}
+__device__ __forceinline__ uint32_t h2max(uint32_t a, uint32_t b) {
+  const __half2 m = __hmax2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&m);
+}
+// fp16 pair -> fp32, + 0 so that a zero extreme is stored as +0 whichever
+// zero the reduction kept
+__device__ __forceinline__ float2 h2_to_f2_pos0(uint32_t a) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&a));
+  return make_float2(__fadd_rn(f.x, 0.f), __fadd_rn(f.y, 0.f));
+}
+
+// One-dimensional bulk copy shared -> global as its own bulk group.
+__device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+               "r"(static_cast<uint32_t>(__cvta_generic_to_shared(src_smem))), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared source of every committed bulk copy has been read
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk copy has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Codes of one packed word from NF fp16 pairs: pair f holds the fields e = 0
+// and e = 1 of one (u, j), placed at bits pos[f] and 16 + pos[f].  The two
+// lanes of the paired arithmetic are the e = 0 and e = 1 halves of the word;
+// each accumulates its codes as 2^23 + sum code * 2^pos, exact in fp32, and
+// the low 16 bits of both are joined by one byte permute.  Sets `near` when
+// some y' lies farther than thr = 1/2 - tol from its rounded value, i.e.
+// within tol of a rounding boundary (the word is then redone exactly).
+template <int NF>
+__device__ __forceinline__ uint32_t pack_word(const uint32_t (&x)[NF], const f2x (&rcp)[NF], const f2x (&c)[NF],
+                                              const int (&pos)[NF], float thr, bool &near) {
+  const f2x magic = f2_pack(kMagic, kMagic);
+  f2x acc = f2_pack(kPackBase, kPackBase);
+  float emax = 0.f;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x[f]));
+    const f2x y = f2_fma(f2_pack(xf.x, xf.y), rcp[f], c[f]);
+    const f2x r = f2_sub(f2_add(y, magic), magic);  // rne(y'), exact
+    const float2 e = f2_unpack(f2_sub(y, r));
+    emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
+    const float sc = __int_as_float((127 + pos[f]) << 23);  // 2^pos
+    acc = f2_fma(r, f2_pack(sc, sc), acc);
+  }
+  near = emax > thr;
+  const float2 a = f2_unpack(acc);
+  return __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x5410);
+}
+
+// Quantize and pack the group held in `r` (tokens from stream index i0 of
+// (s, h)) and write its block with a bulk copy issued by thread 0.  Before
+// the call thread 0 must have waited (bulk_wait_read) for the previous
+// block's copy out of sm.blk.  Three CTA barriers inside, the last one after
+// every read of the tiles.
+template <int BITS>
+__device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r, const Geo &geo, int s, int h,
+                                               int i0) {
+  constexpr int NU = 8 / BITS;  // fields per byte
+  constexpr int WH = 4 / NU;    // words per (lane, k-tile)
+  const float levels = float((1 << BITS) - 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p = tid >> 4, c8 = tid & 15;
+  float *blkf = reinterpret_cast<float *>(sm.blk);
+  uint32_t *blkw = reinterpret_cast<uint32_t *>(sm.blk);
+
+  // ---- tiles, partial key statistics, value token statistics
+  {
+    *reinterpret_cast<uint4 *>(&sm.k[(2 * p) * 64 + 4 * c8]) = r.k[0];
+    *reinterpret_cast<uint4 *>(&sm.k[(2 * p + 1) * 64 + 4 * c8]) = r.k[1];
+    const uint32_t ka[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
+    const uint32_t kb[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
+    uint32_t kmn[4], kmx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kmn[i] = h2min(ka[i], kb[i]);
+      kmx[i] = h2max(ka[i], kb[i]);
+      kmn[i] = h2min(kmn[i], __shfl_xor_sync(0xffffffffu, kmn[i], 16));  // the warp's other token pair
+      kmx[i] = h2max(kmx[i], __shfl_xor_sync(0xffffffffu, kmx[i], 16));
+    }
+    if (lane < 16) {
+      uint4 *ks = reinterpret_cast<uint4 *>(&sm.kstat[warp][4 * c8][0]);
+      ks[0] = make_uint4(kmn[0], kmx[0], kmn[1], kmx[1]);
+      ks[1] = make_uint4(kmn[2], kmx[2], kmn[3], kmx[3]);
+    }
+    const __half *va = reinterpret_cast<const __half *>(&r.v[0]);
+    const __half *vb = reinterpret_cast<const __half *>(&r.v[1]);
     __half2 mn2 = __halves2half2(va[0], vb[0]), mx2 = mn2;
+    // vword(8 c8 + c, p) = 128 c8 + 32 (c / 2) + ((p ^ 2 c8) ^ 16 (c % 2) ^ 4 (c / 2))
+    uint32_t *vrow = sm.v + 128 * c8;
+    const int vx = p ^ (2 * c8);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const __half2 pair = __halves2half2(va[c], vb[c]);  // (token 2p, token 2p+1) of channel 8 c8 + c
-      *reinterpret_cast<__half2 *>(&svT[c8 * 8 + c][2 * p]) = pair;
-      mn2 = __hmin2(mn2, pair);
-      mx2 = __hmax2(mx2, pair);
+      const __half2 pr = __halves2half2(va[c], vb[c]);  // (token 2p, token 2p + 1) of channel 8 c8 + c
+      vrow[32 * (c >> 1) + (vx ^ ((16 * (c & 1)) ^ (4 * (c >> 1))))] = *reinterpret_cast<const uint32_t *>(&pr);
+      mn2 = __hmin2(mn2, pr);
+      mx2 = __hmax2(mx2, pr);
     }
-    // per-token min/max over the 16 lanes holding the token's 128 channels
 #pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
+    for (int o = 1; o < 16; o <<= 1) {  // over the 16 lanes holding the tokens' 128 channels
       const uint32_t a = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mn2), o);
       const uint32_t b = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mx2), o);
       mn2 = __hmin2(mn2, *reinterpret_cast<const __half2 *>(&a));
       mx2 = __hmax2(mx2, *reinterpret_cast<const __half2 *>(&b));
     }
-    if (c8 < 2) {  // lane 0 of the pair finishes token 2p, lane 1 token 2p+1
-      const float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
-      // + 0 stores a zero extreme as +0 whichever zero the reduction kept
-      const float mn = __fadd_rn(c8 == 0 ? mnf.x : mnf.y, 0.f), mx = __fadd_rn(c8 == 0 ? mxf.x : mxf.y, 0.f);
-      const int t = 2 * p + c8;
-      const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
-      vq[t] = make_slice(mn, sc, levels);
-      v_sc[t] = sc;
-      reinterpret_cast<float *>(blk + off_vs(BITS))[t] = sc;
-      reinterpret_cast<float *>(blk + off_vm(BITS))[t] = mn;
-    }
+    if (c8 == 0)
+      *reinterpret_cast<uint2 *>(sm.vstat[p]) =
+          make_uint2(*reinterpret_cast<uint32_t *>(&mn2), *reinterpret_cast<uint32_t *>(&mx2));
   }
   __syncthreads();
-  if (threadIdx.x < kD / 2) {  // keys: channels 2d, 2d+1, min/max over the 32 tokens (exact in fp16)
-    const int d = 2 * threadIdx.x;
-    __half2 mn2 = *reinterpret_cast<const __half2 *>(&sk[0][d]), mx2 = mn2;
-#pragma unroll 8
-    for (int t = 1; t < kG; ++t) {
-      const __half2 x = *reinterpret_cast<const __half2 *>(&sk[t][d]);
-      mn2 = __hmin2(mn2, x);
-      mx2 = __hmax2(mx2, x);
+  // ---- key channel statistics over the 8 warps' partials; block scales
+  if (tid < kD) {
+    const int cp = tid >> 1, e = tid & 1;
+    uint32_t mn = sm.kstat[0][cp][0], mx = sm.kstat[0][cp][1];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      mn = h2min(mn, sm.kstat[w][cp][0]);
+      mx = h2max(mx, sm.kstat[w][cp][1]);
     }
-    float2 mnf = __half22float2(mn2), mxf = __half22float2(mx2);
-    mnf.x = __fadd_rn(mnf.x, 0.f);
-    mnf.y = __fadd_rn(mnf.y, 0.f);
-    mxf.x = __fadd_rn(mxf.x, 0.f);
-    mxf.y = __fadd_rn(mxf.y, 0.f);
-    const float sc0 = __fdiv_rn(__fsub_rn(mxf.x, mnf.x), levels);
-    const float sc1 = __fdiv_rn(__fsub_rn(mxf.y, mnf.y), levels);
-    kq[d] = make_slice(mnf.x, sc0, levels);
-    kq[d + 1] = make_slice(mnf.y, sc1, levels);
-    k_sc[d] = sc0;
-    k_sc[d + 1] = sc1;
-    reinterpret_cast<float2 *>(blk + off_ks(BITS))[threadIdx.x] = make_float2(sc0, sc1);
-    reinterpret_cast<float2 *>(blk + off_km(BITS))[threadIdx.x] = make_float2(mnf.x, mnf.y);
+    const float2 mnf = h2_to_f2_pos0(mn), mxf = h2_to_f2_pos0(mx);
+    const float lo = e ? mnf.y : mnf.x, hi = e ? mxf.y : mxf.x;
+    const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
+    sm.kq[tid] = make_slice(lo, sc, levels);
+    blkf[off_ks(BITS) / 4 + tid] = sc;
+    blkf[off_km(BITS) / 4 + tid] = lo;
+  } else if (tid < kD + kG) {  // value tokens
+    const int t = tid - kD;
+    const float2 mnf = h2_to_f2_pos0(sm.vstat[t >> 1][0]), mxf = h2_to_f2_pos0(sm.vstat[t >> 1][1]);
+    const float lo = t & 1 ? mnf.y : mnf.x, hi = t & 1 ? mxf.y : mxf.x;
+    const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
+    sm.vq[t] = make_slice(lo, sc, levels);
+    blkf[off_vs(BITS) / 4 + t] = sc;
+    blkf[off_vm(BITS) / 4 + t] = lo;
   }
   __syncthreads();
 
-  // Pack: each thread builds whole 32-bit words.  Word index t' of a tile is
-  // stored at byte 4t' (coalesced), i.e. word w = 4(t'/128) + t'%4 of lane
-  // (t'/4)%32; its fields are (e, j, u) at bit 16e + 8j + b*u holding
-  // element (row, col) = (16 mt + 8 (tau%2) + g, 16 kt + 8 j + 2 q + e).
-  // Both tiles read their element pairs (e = 0, 1) as one half2: keys from
-  // token rows, values from the transposed channel rows.
-  constexpr int NU = 8 / BITS;                // fields per byte
-  constexpr int WPL = kG * kD * BITS / 1024;  // words per lane
-  for (int widx = threadIdx.x; widx < 2 * 32 * WPL; widx += kQuantThreads) {
-    const bool keys = widx < 32 * WPL;
-    const int t = keys ? widx : widx - 32 * WPL;
-    const int w = (t >> 7) * 4 + (t & 3);
-    const int lane = (t >> 2) & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int pk = w / (4 / NU);
-    const int kt = keys ? pk : (pk & 1);
-    const int mt0 = keys ? 0 : 2 * (pk >> 1);
-    const SliceQ *sq = keys ? kq : vq;
-    const float *ssc = keys ? k_sc : v_sc;
-    SliceQ sl[2][2];
+  // ---- pack.  Warps 0-3: key words, warps 4-7: value words.
+  if (warp < 4) {
+    // word (lane 4g + q, w = kt * WH + hw): tokens 8 tau + g for tau = hw NU
+    // + u, channels 16 kt + 8 j + 2 q + e.  Lanes of a warp share g and take
+    // the 32 (kt, q); half of them visit j in the other order so that each
+    // load instruction covers 32 distinct channel pairs mod 32 (banks).
+    const int kt = lane >> 2, q = lane & 3;
+    const int jx = kt >> 2;
+    f2x rcp[2], cc[2];
+    float tol = 0.f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < 2; ++j) {
+      const SliceQ a = sm.kq[16 * kt + 8 * j + 2 * q], b = sm.kq[16 * kt + 8 * j + 2 * q + 1];
+      rcp[j] = f2_pack(a.rcp, b.rcp);
+      cc[j] = f2_pack(a.c, b.c);
+      tol = fmaxf(tol, fmaxf(a.tol, b.tol));
+    }
+    const float thr = 0.5f - tol;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) sl[j][e] = sq[16 * kt + 8 * j + 2 * q + e];
-    uint32_t word = 0;
-    bool near = false;
+    for (int gi = 0; gi < 2; ++gi) {
+      const int g = 2 * warp + gi;
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      const int tau = (w % (4 / NU)) * NU + u;
-      const int row = 16 * (mt0 + (tau >> 1)) + 8 * (tau & 1) + g;
+      for (int hw = 0; hw < WH; ++hw) {
+        uint32_t x[2 * NU];
+        f2x fr[2 * NU], fc[2 * NU];
+        int pos[2 * NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = jj ^ jx, tau = hw * NU + u, f = 2 * u + jj;
+            x[f] = sm.k[(8 * tau + g) * 64 + 8 * kt + 4 * j + q];
+            fr[f] = jx ? rcp[jj ^ 1] : rcp[jj];
+            fc[f] = jx ? cc[jj ^ 1] : cc[jj];
+            pos[f] = 8 * j + BITS * u;
+          }
+        bool near;
+        uint32_t word = pack_word<2 * NU>(x, fr, fc, pos, thr, near);
+        if (__any_sync(0xffffffffu, near) && near) {
+          word = 0;
+          for (int f = 0; f < 4 * NU; ++f) {
+            const int u = f >> 2, j = (f >> 1) & 1, e = f & 1;
+            const int tau = hw * NU + u, ch = 16 * kt + 8 * j + 2 * q + e;
+            const uint32_t w2 = sm.k[(8 * tau + g) * 64 + (ch >> 1)];
+            const float xv = __half2float(reinterpret_cast<const __half *>(&w2)[e]);
+            word |= exact_code<BITS>(xv, sm.kq[ch].mn, blkf[off_ks(BITS) / 4 + ch]) << (16 * e + 8 * j + BITS * u);
+          }
+        }
+        const int w = kt * WH + hw, L = 4 * g + q;
+        blkw[off_kc(BITS) / 4 + ((w >> 2) * 32 + L) * 4 + (w & 3)] = word;
+      }
+    }
+  } else {
+    // word (lane 4g + q, w = (2P + kt) * WH + hw): channels 32 P + 8 tau + g
+    // for tau = hw NU + u, tokens 16 kt + 8 j + 2 q + e; warp 4 + P.
+    const int P = warp - 4, g = lane >> 2, q = lane & 3;
+    // vword(32 P + 8 tau + g, 8 kt + 4 j + q) = vbase + 128 tau
+    //   + ((16 (g % 2) + q) ^ 4 (g / 2) ^ 8 kt ^ 8 P ^ 4 j ^ 2 tau)
+    const uint32_t *vbase = sm.v + (16 * P + (g >> 1)) * 32;
+    const int vy = ((16 * (g & 1)) | q) ^ (4 * (g >> 1));
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      const int vyk = vy ^ (8 * kt) ^ (8 * P);
+      f2x rcp[2], cc[2];
+      float tol = 0.f;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int col = 16 * kt + 8 * j + 2 * q;
-        const float2 x = __half22float2(keys ? *reinterpret_cast<const __half2 *>(&sk[row][col])
-                                             : *reinterpret_cast<const __half2 *>(&svT[row][col]));
-        bool n0f, n1f;
-        word |= fast_code(x.x, sl[j][0], n0f) << (8 * j + BITS * u);
-        word |= fast_code(x.y, sl[j][1], n1f) << (16 + 8 * j + BITS * u);
-        near |= n0f | n1f;
+        const SliceQ a = sm.vq[16 * kt + 8 * j + 2 * q], b = sm.vq[16 * kt + 8 * j + 2 * q + 1];
+        rcp[j] = f2_pack(a.rcp, b.rcp);
+        cc[j] = f2_pack(a.c, b.c);
+        tol = fmaxf(tol, fmaxf(a.tol, b.tol));
+      }
+      const float thr = 0.5f - tol;
+#pragma unroll
+      for (int hw = 0; hw < WH; ++hw) {
+        uint32_t x[2 * NU];
+        f2x fr[2 * NU], fc[2 * NU];
+        int pos[2 * NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int tau = hw * NU + u, f = 2 * u + j;
+            x[f] = vbase[128 * tau + (vyk ^ (4 * j) ^ (2 * tau))];
+            fr[f] = rcp[j];
+            fc[f] = cc[j];
+            pos[f] = 8 * j + BITS * u;
+          }
+        bool near;
+        uint32_t word = pack_word<2 * NU>(x, fr, fc, pos, thr, near);
+        if (__any_sync(0xffffffffu, near) && near) {
+          word = 0;
+          for (int f = 0; f < 4 * NU; ++f) {
+            const int u = f >> 2, j = (f >> 1) & 1, e = f & 1;
+            const int tau = hw * NU + u, tok = 16 * kt + 8 * j + 2 * q + e;
+            const uint32_t w2 = sm.v[vword(32 * P + 8 * tau + g, tok >> 1)];
+            const float xv = __half2float(reinterpret_cast<const __half *>(&w2)[e]);
+            word |= exact_code<BITS>(xv, sm.vq[tok].mn, blkf[off_vs(BITS) / 4 + tok]) << (16 * e + 8 * j + BITS * u);
+          }
+        }
+        const int w = (2 * P + kt) * WH + hw, L = 4 * g + q;
+        blkw[off_vc(BITS) / 4 + ((w >> 2) * 32 + L) * 4 + (w & 3)] = word;
       }
     }
-    if (__any_sync(0xffffffffu, near) && near) {
-      // some field's fast code could differ from the IEEE one: redo the word
-      word = 0;
-      for (int f = 0; f < 4 * NU; ++f) {
-        const int u = f >> 2, j = (f >> 1) & 1, e = f & 1;
-        const int tau = (w % (4 / NU)) * NU + u;
-        const int row = 16 * (mt0 + (tau >> 1)) + 8 * (tau & 1) + g;
-        const int col = 16 * kt + 8 * j + 2 * q + e;
-        const float x = __half2float(keys ? sk[row][col] : svT[row][col]);
-        word |= exact_code<BITS>(x, sl[j][e].mn, ssc[col]) << (16 * e + 8 * j + BITS * u);
-      }
-    }
-    reinterpret_cast<uint32_t *>(blk + (keys ? off_kc(BITS) : off_vc(BITS)))[t] = word;
+  }
+  fence_proxy_async();  // this thread's block writes, before the bulk copy reads them
+  __syncthreads();
+  if (tid == 0) {
+    uint8_t *dst = geo.blocks + ((static_cast<size_t>(s) * geo.H + h) * geo.max_groups + i0 / kG) *
+                                    static_cast<size_t>(block_bytes(BITS));
+    bulk_s2g(dst, sm.blk, block_bytes(BITS));
   }
 }
 
@@ -208,22 +409,66 @@ __device__ __forceinline__ void flush_group(const Geo &geo, int s, int h, int i0
 constexpr int kLenBits = 22;
 constexpr int kLenMask = (1 << kLenBits) - 1;
 
-// One CTA quantizes one 32-token group of one (sequence, KV head).
-// grid = (group slot, KV head, sequence).
+// Flush groups of an append, by persistent CTAs.  Task t = group slot
+// t % gmax of (sequence, KV head) t / gmax (fewer than 2^31 tasks); CTA b
+// takes tasks b, b + grid, ... and loads the next task's rows while it
+// quantizes the current one.
 template <int BITS>
-__global__ void __launch_bounds__(kQuantThreads) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
-                                                                    const __half *__restrict__ v_new,
-                                                                    const int *__restrict__ new_len, int max_new) {
-  const int s = blockIdx.z, h = blockIdx.y, gslot = blockIdx.x;
-  const int L0 = geo.seq_len[s];
-  const int nn = new_len[s];
-  if (nn < 0 || nn > max_new || L0 + nn > geo.capacity || L0 < 0) return;  // reported by the tail kernel
-  const int n0 = max(L0 - geo.ns, 0);
-  const int Lq0 = n0 - n0 % geo.R;
-  const int n1 = max(L0 + nn - geo.ns, 0);
-  const int Lq1 = n1 - n1 % geo.R;
-  if (gslot >= (Lq1 - Lq0) / kG) return;
-  flush_group<BITS>(geo, s, h, Lq0 + gslot * kG, n0, Lq0, L0, k_new, v_new, max_new);
+__global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
+                                                                       const __half *__restrict__ v_new,
+                                                                       const int *__restrict__ new_len,
+                                                                       int max_new, int gmax) {
+  __shared__ QuantSmem sm;
+  // task = (sequence, KV head) sh, group slot gs; CTA b starts at task b and
+  // steps by the grid, i.e. by (dq, dr) in (sh, gs)
+  const int nsh = geo.S * geo.H;
+  const int dq = static_cast<int>(gridDim.x / static_cast<unsigned>(gmax));
+  const int dr = static_cast<int>(gridDim.x % static_cast<unsigned>(gmax));
+  int sh = static_cast<int>(blockIdx.x / static_cast<unsigned>(gmax));
+  int gs = static_cast<int>(blockIdx.x % static_cast<unsigned>(gmax));
+  // advance (sh, gs) to the first task at or after it with a group to flush;
+  // false past the last task
+  auto find = [&](GroupSrc &g) {
+    for (; sh < nsh; gs += dr, sh += dq + (gs >= gmax ? 1 : 0), gs -= gs >= gmax ? gmax : 0) {
+      const int s = static_cast<int>(static_cast<unsigned>(sh) / static_cast<unsigned>(geo.H));
+      const int L0 = geo.seq_len[s], nn = new_len[s];
+      if (nn < 0 || nn > max_new || L0 < 0 || L0 + nn > geo.capacity) continue;  // reported by the tail kernel
+      const int n0 = max(L0 - geo.ns, 0), n1 = max(L0 + nn - geo.ns, 0);
+      const int Lq0 = n0 - n0 % geo.R, Lq1 = n1 - n1 % geo.R;
+      if (gs >= (Lq1 - Lq0) / kG) continue;
+      g.s = s;
+      g.h = sh - s * geo.H;
+      g.i0 = Lq0 + gs * kG;
+      g.n0 = n0;
+      g.Lq0 = Lq0;
+      g.L0 = L0;
+      return true;
+    }
+    return false;
+  };
+  auto step = [&]() {
+    gs += dr;
+    sh += dq;
+    if (gs >= gmax) {
+      gs -= gmax;
+      ++sh;
+    }
+  };
+  GroupSrc cur, nxt;
+  if (!find(cur)) return;
+  GroupRegs rc, rn;
+  load_group(rc, geo, cur, k_new, v_new, max_new);
+  while (true) {
+    step();
+    const bool more = find(nxt);
+    if (more) load_group(rn, geo, nxt, k_new, v_new, max_new);
+    if (threadIdx.x == 0) bulk_wait_read();  // the previous block's copy has left sm.blk
+    quantize_group<BITS>(sm, rc, geo, cur.s, cur.h, cur.i0);
+    if (!more) break;
+    cur = nxt;
+    rc = rn;
+  }
+  if (threadIdx.x == 0) bulk_wait_all();
 }
 
 // Copy the new tokens of (sequence s, KV heads [h0, h1)) that land in the
@@ -261,19 +506,21 @@ __device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1,
 
 // Append of at most R new tokens per sequence in one kernel, one CTA per
 // (KV head, sequence): at most one window fills, and the CTA then quantizes
-// its R / 32 groups one after another.  Each CTA adds 1 << kLenBits to
-// seq_len[s] once it needs seq_len no more; the CTA that completes the count
-// (Hkv arrivals) stores the final length (clearing the count) and reports
-// bad lengths, and no CTA reads seq_len[s] after that store.  When no window
+// its R / 32 groups one after another (loading the next group's rows while
+// it quantizes the current one).  Each CTA adds 1 << kLenBits to seq_len[s]
+// once it needs seq_len no more; the CTA that completes the count (Hkv
+// arrivals) stores the final length (clearing the count) and reports bad
+// lengths, and no CTA reads seq_len[s] after that store.  When no window
 // fills, a CTA arrives right after reading the length and copies its head's
 // new tokens into the window (or sink), prefetched at launch.  When one
 // fills, the copy would overwrite window slots the sequence's other CTAs may
 // still be quantizing, so the CTAs arrive after quantizing and the last one
 // copies the new tokens of every head.
 template <int BITS>
-__global__ void __launch_bounds__(kQuantThreads) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
+__global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                     const __half *__restrict__ v_new,
                                                                     const int *__restrict__ new_len, int max_new) {
+  __shared__ QuantSmem sm;
   const int s = blockIdx.y, h = blockIdx.x;
   __shared__ int s_last, s_old;
   constexpr int C16 = kD / 8;  // 16-byte chunks per token row
@@ -331,13 +578,29 @@ __global__ void __launch_bounds__(kQuantThreads) step_append_kernel(Geo geo, con
     }
     __syncthreads();
   } else {
+    GroupSrc g;
+    g.s = s;
+    g.h = h;
+    g.i0 = Lq0;
+    g.n0 = n0;
+    g.Lq0 = Lq0;
+    g.L0 = L0;
+    GroupRegs rc, rn;
+    load_group(rc, geo, g, k_new, v_new, max_new);
     for (int i0 = Lq0; i0 < Lq1; i0 += kG) {
-      flush_group<BITS>(geo, s, h, i0, n0, Lq0, L0, k_new, v_new, max_new);
-      __syncthreads();  // the group's reads are done and its shared tiles free again
+      if (i0 + kG < Lq1) {
+        g.i0 = i0 + kG;
+        load_group(rn, geo, g, k_new, v_new, max_new);
+      }
+      if (threadIdx.x == 0) bulk_wait_read();
+      quantize_group<BITS>(sm, rc, geo, s, h, i0);
+      rc = rn;
     }
+    // quantize_group ends with a barrier: every read of the window is done
     if (threadIdx.x == 0) arrive();
     __syncthreads();
     if (s_last) copy_tail(geo, s, 0, geo.H, L0, nn, k_new, v_new, max_new, threadIdx.x, blockDim.x);
+    if (threadIdx.x == 0) bulk_wait_all();
   }
   if (s_last && threadIdx.x == 0) {
     if (bad_len) set_status(geo.status, KVQ_STATUS_BAD_LEN);
@@ -372,6 +635,28 @@ __global__ void __launch_bounds__(256) append_tail_kernel(Geo geo, const __half 
 // most max_new tokens: a window holding R-1 tokens plus max_new new ones.
 int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R / kG); }
 
+// Persistent CTAs of the flush kernel on the current device: every resident
+// slot (cached per device ordinal).
+template <int BITS>
+static cudaError_t flush_grid(int &ctas) {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && cache[dev]) {
+    ctas = cache[dev];
+    return cudaSuccess;
+  }
+  int per_sm = 0, n_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_flush_kernel<BITS>, kQuantThreads, 0)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  ctas = max(per_sm, 1) * n_sm;
+  if (dev < 64) cache[dev] = ctas;
+  return cudaSuccess;
+}
+
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                 int max_new, cudaStream_t stream, uint64_t *launches) {
   // a decode-sized append (at most one window fills): one kernel
@@ -386,14 +671,18 @@ cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __hal
   }
   const int gmax = max_flush_groups(geo.R, max_new);
   if (gmax > 0) {
-    dim3 grid(gmax, geo.H, geo.S);
-    if (geo.bits == 2)
-      quant_flush_kernel<2><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
-    else
-      quant_flush_kernel<4><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
-    ++*launches;
-    cudaError_t e = cudaGetLastError();
+    int ctas = 0;
+    cudaError_t e = geo.bits == 2 ? flush_grid<2>(ctas) : flush_grid<4>(ctas);
     if (e != cudaSuccess) return e;
+    const long long ntask = static_cast<long long>(gmax) * geo.H * geo.S;
+    if (ntask > 2147483647LL) return cudaErrorInvalidValue;
+    const int grid = static_cast<int>(min(static_cast<long long>(ctas), ntask));
+    if (geo.bits == 2)
+      quant_flush_kernel<2><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
+    else
+      quant_flush_kernel<4><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
+    ++*launches;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   append_tail_kernel<<<geo.S, 256, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
   ++*launches;
