@@ -66,8 +66,9 @@ struct DecodeArgs {
 };
 
 // Shared memory of one warp: a ring of NS group blocks, one mbarrier per
-// slot, and the query of the current pair (fp32, GQ heads), whose space the
-// score operand staging reuses once the query sits in registers.
+// slot, the query of the current pair (fp32, GQ heads), whose space the
+// score operand staging reuses once the query sits in registers, and (keys
+// stored pre-RoPE) the per-group channel-pair coefficients.
 // Ring slots (group blocks in flight) per warp.
 #ifndef KVQ_DECODE_RING_2BIT
 #define KVQ_DECODE_RING_2BIT 4
@@ -76,13 +77,14 @@ struct DecodeArgs {
 #define KVQ_DECODE_RING_4BIT 2
 #endif
 
-template <int BITS, int GQ>
+template <int BITS, int GQ, bool ROPE>
 struct WarpSmem {
   static constexpr int BB = block_bytes(BITS);
-  static constexpr int NS = BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT;
+  static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2) : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
   static constexpr int BAR_OFF = NS * BB;
   static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
-  static constexpr int BYTES = (Q_OFF + GQ * kD * 4 + 127) / 128 * 128;
+  static constexpr int COEF_OFF = Q_OFF + GQ * kD * 4;            // [GQ][64] float4, then [GQ][64] float2
+  static constexpr int BYTES = (COEF_OFF + (ROPE ? GQ * 64 * 24 : 0) + 127) / 128 * 128;
   static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
 };
 
@@ -459,9 +461,9 @@ __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_
 #endif
 
 template <int BITS, int GQ, bool ROPE>
-__global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
+__global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
     decode_kernel(DecodeArgs a) {
-  using WS = WarpSmem<BITS, GQ>;
+  using WS = WarpSmem<BITS, GQ, ROPE>;
   constexpr int NS = WS::NS, BB = WS::BB;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -822,7 +824,16 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? KVQ_DECODE_
             top_up();
           }
         } else {
-          // pre-RoPE keys: one lane per token, dequantize, rotate, dot
+          // pre-RoPE keys, one lane per token t.  With (C0, S0) the rotation of
+          // the group's first position p0 and (Ct, St) that of the offset t, the
+          // query rotated back to p0 (a = q'_i, b = q'_{i+64}) gives
+          //   q . R(p0 + t) k = sum_i Ct (a k_i + b k_{i+64}) + St (b k_i - a k_{i+64}),
+          // and with k = code * scale + min the per-pair coefficients of
+          //   X = c1 (a s_i) + c2 (b s_{i+64}) + (a m_i + b m_{i+64}),
+          //   Y = c1 (b s_i) - c2 (a s_{i+64}) + (b m_i - a m_{i+64})
+          // are formed once per group (two pairs per lane) for all 32 tokens.
+          float4 *coef = reinterpret_cast<float4 *>(ring + WS::COEF_OFF);            // [GQ][64]
+          float2 *coef0 = reinterpret_cast<float2 *>(ring + WS::COEF_OFF + GQ * 64 * 16);  // [GQ][64]
           float m_all[GQ];
 #pragma unroll
           for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
@@ -838,37 +849,62 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 2 : (GQ == 4 ? KVQ_DECODE_
             const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
             const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
             const uint8_t *kc = blk + off_kc(BITS);
-            const float2 *base = a.rope_base + static_cast<size_t>(gi) * 64;
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+              const int i = lane + 32 * r2;
+              const float2 b0 = a.rope_base[static_cast<size_t>(gi) * 64 + i];  // (cos, sin) of p0 theta_i
+              const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
+#pragma unroll
+              for (int hh = 0; hh < GQ; ++hh) {
+                const float qa = q_s[hh * kD + i], qb = q_s[hh * kD + i + 64];
+                const float av = fmaf(qa, b0.x, qb * b0.y), bv = fmaf(qb, b0.x, -qa * b0.y);
+                coef[hh * 64 + i] = make_float4(av * s1, bv * s2, bv * s1, -av * s2);
+                coef0[hh * 64 + i] = make_float2(fmaf(av, m1, bv * m2), fmaf(bv, m1, -av * m2));
+              }
+            }
+            __syncwarp();
             const int t = lane;
-            const int uu = (t >> 3) % (8 / BITS);
+            const int tau = t >> 3, uu = tau % (8 / BITS);
             float dot[GQ];
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
 #pragma unroll 1
-            for (int kt = 0; kt < 4; ++kt) {
+            for (int qq = 0; qq < 4; ++qq) {
+              // this token's words of lane 4 (t % 8) + qq: word kt (2-bit) or
+              // 2 kt + tau / 2 (4-bit) holds channels 16 kt + 8 j + 2 qq + e
+              constexpr int WPL = BITS * 4;  // words per lane
+              const uint4 *lw = reinterpret_cast<const uint4 *>(kc) + (4 * (t & 7) + qq);
+              uint32_t wv[WPL];
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                const uint32_t wa = key_word<BITS>(kc, t, kt, qq);
-                const uint32_t wb = key_word<BITS>(kc, t, kt + 4, qq);
+              for (int m = 0; m < WPL / 4; ++m) {
+                const uint4 c4 = lw[32 * m];
+                wv[4 * m] = c4.x;
+                wv[4 * m + 1] = c4.y;
+                wv[4 * m + 2] = c4.z;
+                wv[4 * m + 3] = c4.w;
+              }
+#pragma unroll
+              for (int kt = 0; kt < 4; ++kt) {
+                const uint32_t wa = BITS == 2 ? wv[kt] : ((tau >> 1) ? wv[2 * kt + 1] : wv[2 * kt]);
+                const uint32_t wb = BITS == 2 ? wv[kt + 4] : ((tau >> 1) ? wv[2 * (kt + 4) + 1] : wv[2 * (kt + 4)]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                   for (int e = 0; e < 2; ++e) {
-                    const int ch = 16 * kt + 8 * j + 2 * qq + e;
+                    const int i = 16 * kt + 8 * j + 2 * qq + e;
                     const int sh = 16 * e + 8 * j + BITS * uu;
-                    const float ca = static_cast<float>((wa >> sh) & ((1u << BITS) - 1u));
-                    const float cb = static_cast<float>((wb >> sh) & ((1u << BITS) - 1u));
-                    const float k1 = fmaf(ca, ks[ch], km[ch]);
-                    const float k2 = fmaf(cb, ks[ch + 64], km[ch + 64]);
-                    const float2 bs = base[ch];
-                    const float2 of = roff_s[t * kRopeOffStride + ch];
-                    const float cs = bs.x * of.x - bs.y * of.y;
-                    const float sn = bs.y * of.x + bs.x * of.y;
-                    const float r1 = k1 * cs - k2 * sn;
-                    const float r2 = k2 * cs + k1 * sn;
+                    // code -> fp32 on the FMA pipe: the field under 2^23
+                    const float c1 = __uint_as_float(((wa >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                    const float c2 = __uint_as_float(((wb >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                    const float2 cs = roff_s[t * kRopeOffStride + i];
 #pragma unroll
-                    for (int hh = 0; hh < GQ; ++hh)
-                      dot[hh] = fmaf(q_s[hh * kD + ch], r1, fmaf(q_s[hh * kD + ch + 64], r2, dot[hh]));
+                    for (int hh = 0; hh < GQ; ++hh) {
+                      const float4 cf = coef[hh * 64 + i];
+                      const float2 c0 = coef0[hh * 64 + i];
+                      const float X = fmaf(c1, cf.x, fmaf(c2, cf.y, c0.x));
+                      const float Y = fmaf(c1, cf.z, fmaf(c2, cf.w, c0.y));
+                      dot[hh] = fmaf(cs.x, X, fmaf(cs.y, Y, dot[hh]));
+                    }
                   }
               }
             }
@@ -1036,7 +1072,7 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 // device's SM count (cached per device ordinal).
 template <int BITS, int GQ, bool ROPE>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
-  using WS = WarpSmem<BITS, GQ>;
+  using WS = WarpSmem<BITS, GQ, ROPE>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
   auto kern = decode_kernel<BITS, GQ, ROPE>;
   static int resident[64] = {};
