@@ -124,26 +124,31 @@ def decode_bytes(lengths, w):
     return total
 
 
-def kernel_source_hash():
+def kernel_source_hash(names=("decode.cu", "kvq_internal.cuh")):
     h = hashlib.sha256()
-    for name in ("decode.cu", "kvq_internal.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "bit_kv_cache_02_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per decode-attention call from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_attn_{workload}.md")
+QUANT_SOURCES = ("quant.cu", "kvq_internal.cuh")
+
+
+def ncu_traffic(profile, algorithmic_bytes, sources=("decode.cu", "kvq_internal.cuh")):
+    """DRAM bytes per call: the committed ncu summary's ratio of captured DRAM
+    traffic to the captured launch's algorithmic bytes, scaled to this run's
+    algorithmic bytes per call; None unless the summary was taken on the
+    current kernel source."""
+    path = os.path.join(ROOT, "profiles", profile)
     try:
         text = open(path).read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_call:\s*([0-9]+)\s+source_hash:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != kernel_source_hash():
+    m = re.search(r"traffic_per_algorithmic_byte:\s*([0-9.]+)\s+source_hash:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash(sources):
         return None
-    return int(m.group(1))
+    return float(m.group(1)) * algorithmic_bytes
 
 
 class ClockSampler:
@@ -546,7 +551,8 @@ def main():
     peaks, which = measured_peaks()
     achieved = r["bytes_avg"] / r["attn_avg_s"] / 1e9
     peak = float(peaks["hbm_gbs"])
-    traffic = ncu_traffic(w.name)
+    traffic = ncu_traffic(f"decode_attn_{w.name}.md", r["bytes_avg"])
+    q_traffic = ncu_traffic(f"quant_prefill_{w.name}.md", r["prefill"]["bytes_per_layer"], QUANT_SOURCES)
     line = {
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["elapsed_ms"] / args.steps, "higher_is_better": True,
@@ -562,7 +568,7 @@ def main():
                      "achieved": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9,
                      "unit": "GB/s", "peak": peak,
                      "frac": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9 / peak,
-                     "algorithmic_bytes": r["prefill"]["bytes_per_layer"],
+                     "algorithmic_bytes": r["prefill"]["bytes_per_layer"], "traffic": q_traffic,
                      "us": r["prefill"]["seconds_per_layer"] * 1e6},
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
