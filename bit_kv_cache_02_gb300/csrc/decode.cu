@@ -666,37 +666,48 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
           kp = geo.k_res + (sh * geo.R + slot) * kD;
         }
         const int sidx = pos - geo.ns;  // stream index (negative for the sink)
+        // the key row in flight at once (in two halves for four query heads,
+        // whose register budget is tighter); two dot chains per head
+        constexpr int KH = GQ == 4 ? 2 : 1;  // load rounds
+        float dot2[GQ];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 ra[4], rb[4];  // channels 32*half + 8c.. and 64 + 32*half + 8c..
+        for (int hh = 0; hh < GQ; ++hh) dot2[hh] = 0.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            ra[c] = *reinterpret_cast<const uint4 *>(kp + 32 * half + 8 * c);
-            rb[c] = *reinterpret_cast<const uint4 *>(kp + 64 + 32 * half + 8 * c);
-          }
+        for (int kh = 0; kh < KH; ++kh) {
+        uint4 kr[16 / KH];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const __half *ha = reinterpret_cast<const __half *>(&ra[c]);
-            const __half *hb = reinterpret_cast<const __half *>(&rb[c]);
+        for (int c = 0; c < 8 / KH; ++c) {
+          kr[c] = *reinterpret_cast<const uint4 *>(kp + 8 * (c + kh * 8 / KH));
+          kr[c + 8 / KH] = *reinterpret_cast<const uint4 *>(kp + 64 + 8 * (c + kh * 8 / KH));
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int ch = 32 * half + 8 * c + e;
-              float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
-              if (ROPE && sidx >= 0) {
-                const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
-                const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
-                const float cs = bs.x * of.x - bs.y * of.y;
-                const float sn = bs.y * of.x + bs.x * of.y;
-                const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
-                k1 = r1;
-                k2 = r2;
-              }
+        for (int cc = 0; cc < 8 / KH; ++cc) {
+          const int c = cc + kh * 8 / KH;
+          const __half *ha = reinterpret_cast<const __half *>(&kr[cc]);           // channels 8c ..
+          const __half *hb = reinterpret_cast<const __half *>(&kr[cc + 8 / KH]);  // channels 64 + 8c ..
 #pragma unroll
-              for (int hh = 0; hh < GQ; ++hh)
-                dot[hh] = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, dot[hh]));
+          for (int e = 0; e < 8; ++e) {
+            const int ch = 8 * c + e;
+            float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
+            if (ROPE && sidx >= 0) {
+              const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
+              const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
+              const float cs = bs.x * of.x - bs.y * of.y;
+              const float sn = bs.y * of.x + bs.x * of.y;
+              const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
+              k1 = r1;
+              k2 = r2;
+            }
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              float &d = (e & 1) ? dot2[hh] : dot[hh];
+              d = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, d));
             }
           }
         }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) dot[hh] += dot2[hh];
       }
       float p[GQ], mh[GQ], lh[GQ], acc[GQ][4];
 #pragma unroll
@@ -713,11 +724,12 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
         lh[hh] = sum;
         acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
       }
-      // values: lane holds channels 4*lane .. 4*lane+3; eight rows in flight
-      for (int tb = 0; tb < nt; tb += 8) {
-        uint2 raw[8];
+      // values: lane holds channels 4*lane .. 4*lane+3; VB rows in flight at once
+      constexpr int VB = GQ == 4 ? 8 : 32;
+      for (int tb = 0; tb < nt; tb += VB) {
+        uint2 raw[VB];
 #pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
+        for (int uu = 0; uu < VB; ++uu) {
           const int it = t0 + tb + uu;
           raw[uu] = make_uint2(0u, 0u);
           if (tb + uu < nt) {
@@ -727,7 +739,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
           }
         }
 #pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
+        for (int uu = 0; uu < VB; ++uu) {
           const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].x));
           const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].y));
 #pragma unroll
