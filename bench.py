@@ -559,7 +559,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": f"u{w.bits}-codes/f32-accum",
         "data": "synthetic", "config": dict(config, mean_ctx_timed=r["mean_ctx"]),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "frac_of_nominal_8tbs": achieved / 8000.0, "traffic": traffic,
                      "kernel": "decode_kernel (one per kv_decode_attn call)", "peak_source": which,
                      "timing": "CUDA events around K replays of a graph of 32 kv_decode_attn calls",
                      "algorithmic_bytes_per_call": r["bytes_avg"], "call_us": r["attn_avg_s"] * 1e6},

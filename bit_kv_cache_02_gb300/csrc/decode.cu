@@ -315,7 +315,10 @@ __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, int kt, i
 // across pair boundaries.  A warp leaves one partial result per pair it
 // touches (slot gw + pair) plus one per window pass it runs; the warp that
 // completes a pair's count merges them.
-constexpr int kPassUnits = 4;
+#ifndef KVQ_PASS_UNITS
+#define KVQ_PASS_UNITS 4
+#endif
+constexpr int kPassUnits = KVQ_PASS_UNITS;
 constexpr int kInlinePlanSeqs = 256;  // larger batches use the plan kernel
 
 struct PlanHeader {

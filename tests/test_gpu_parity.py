@@ -186,6 +186,31 @@ def test_streaming_appends_match_prefill(kvq, ns):
         assert torch.equal(c.blocks.cpu(), b0)
 
 
+@pytest.mark.parametrize("R,bits,ns,pre_rope", [(32, 2, 1, False), (64, 4, 0, False), (96, 2, 1, True),
+                                                 (32, 4, 1, True)])
+def test_residual_window_sizes(kvq, R, bits, ns, pre_rope):
+    """Windows of R = 32, 64, 96 tokens: per-token appends (the one-kernel
+    step path), then appends of up to R tokens, then a prefill-sized append
+    (the two-kernel path) leave the oracle's bytes, and attention matches
+    after each phase."""
+    S, H, T = 2, 2, 4 * R + 40  # the last append (1.5 R + 32 tokens) exceeds R
+    k, v = _rand_kv(S, H, T, seed=R + bits)
+    cache, orc = _build(kvq, S, H, T + 8, bits, ns=ns, pre_rope=pre_rope, R=R)
+    lens = np.array([T, T - 17])
+    pos = 0
+    steps = [1] * (R + 3) + [R, R // 2 + 5]
+    steps.append(T - pos - sum(steps))
+    for i, step in enumerate(steps):
+        sl = np.clip(lens - pos, 0, step).astype(np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+        if i in (R + 2, len(steps) - 2, len(steps) - 1):
+            _compare_state(cache, orc)
+            q = _rand_q(S, 2 * H, seed=i)
+            _attn_close(_attend(kvq, cache, q, T), orc.attention(q, pre_rope=pre_rope))
+    assert pos == T
+
+
 def test_decode_step_flush_then_attend(kvq):
     """A window holding R-1 tokens plus one appended token flushes; attention
     then reads only quantized groups."""
