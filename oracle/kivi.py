@@ -202,33 +202,36 @@ def unpack_tile(buf, bits: int, rows: int, cols: int):
     return (vals & mask).astype(np.uint8).reshape(buf.shape[:-1] + (rows, cols))
 
 
-def block_bytes(bits: int, head_dim: int = HEAD_DIM) -> int:
+def block_bytes(bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False) -> int:
     """Bytes of one 32-token group block: K codes, V codes (32*D*b/8 each),
-    K scale and K min (fp32 per channel), V scale and V min (fp32 per token)."""
-    return 2 * (GROUP * head_dim * bits // 8) + 2 * 4 * head_dim + 2 * 4 * GROUP
+    K scale and K min (fp32 per channel; per token when keys are grouped per
+    token), V scale and V min (fp32 per token)."""
+    kmeta = GROUP if key_per_token else head_dim
+    return 2 * (GROUP * head_dim * bits // 8) + 2 * 4 * kmeta + 2 * 4 * GROUP
 
 
-def pack_block(kc, ks, km, vc, vs, vm, bits: int):
-    """One group block.  kc: [32 tok][D] key codes, ks/km: [D];
-    vc: [32 tok][D] value codes, vs/vm: [32]."""
+def pack_block(kc, ks, km, vc, vs, vm, bits: int, key_per_token: bool = False):
+    """One group block.  kc: [32 tok][D] key codes, ks/km: [D] ([32] when
+    keys are grouped per token); vc: [32 tok][D] value codes, vs/vm: [32]."""
     D = kc.shape[-1]
     kbytes = GROUP * D * bits // 8
+    km_n = GROUP if key_per_token else D
     parts = [
         pack_tile(kc, bits),                                   # rows = tokens
         pack_tile(np.swapaxes(vc, -1, -2), bits),              # rows = channels
-        np.asarray(ks, np.float32).view(np.uint8).reshape(ks.shape[:-1] + (4 * D,)),
-        np.asarray(km, np.float32).view(np.uint8).reshape(km.shape[:-1] + (4 * D,)),
+        np.asarray(ks, np.float32).view(np.uint8).reshape(ks.shape[:-1] + (4 * km_n,)),
+        np.asarray(km, np.float32).view(np.uint8).reshape(km.shape[:-1] + (4 * km_n,)),
         np.asarray(vs, np.float32).view(np.uint8).reshape(vs.shape[:-1] + (4 * GROUP,)),
         np.asarray(vm, np.float32).view(np.uint8).reshape(vm.shape[:-1] + (4 * GROUP,)),
     ]
     out = np.concatenate(parts, axis=-1)
-    assert out.shape[-1] == block_bytes(bits, D) and parts[0].shape[-1] == kbytes
+    assert out.shape[-1] == block_bytes(bits, D, key_per_token) and parts[0].shape[-1] == kbytes
     return out
 
 
-def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM):
-    """Inverse of `pack_block`: returns (kc [32][D], ks [D], km [D],
-    vc [32][D], vs [32], vm [32])."""
+def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False):
+    """Inverse of `pack_block`: returns (kc [32][D], ks [D], km [D] (both
+    [32] for per-token keys), vc [32][D], vs [32], vm [32])."""
     D = head_dim
     buf = np.ascontiguousarray(buf, np.uint8)
     cb = GROUP * D * bits // 8
@@ -241,8 +244,8 @@ def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM):
         a = np.ascontiguousarray(buf[..., o:o + 4 * n]).view(np.float32)
         o += 4 * n
         return a
-    ks = f32(D)
-    km = f32(D)
+    ks = f32(GROUP if key_per_token else D)
+    km = f32(GROUP if key_per_token else D)
     vs = f32(GROUP)
     vm = f32(GROUP)
     return kc, ks, km, np.swapaxes(vcT, -1, -2), vs, vm
@@ -282,17 +285,22 @@ class OracleCache:
     enters the full-precision window, and whenever the window holds R tokens
     those R tokens are quantized into R/32 group blocks and the window empties
     (KIVI page, third paragraph).  seq_len counts every stored token.
+
+    key_per_token switches keys to the per-token grouping the KIVI page's
+    first paragraph describes as the baseline (one scale and min per token
+    over its D channels, like values): the ablation of per-channel keys.
     """
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits, residual=128,
-                 num_sink=0, head_dim=HEAD_DIM):
+                 num_sink=0, head_dim=HEAD_DIM, key_per_token=False):
         assert bits in (2, 4) and residual % GROUP == 0 and residual > 0
         assert num_sink in (0, 1) and capacity >= 1
         self.S, self.H, self.D = num_seqs, num_kv_heads, head_dim
         self.bits, self.R, self.ns, self.capacity = bits, residual, num_sink, capacity
+        self.kpt = bool(key_per_token)
         stream_cap = max(capacity - num_sink, 0)
         self.max_groups = (stream_cap // residual) * residual // GROUP
-        self.bb = block_bytes(bits, head_dim)
+        self.bb = block_bytes(bits, head_dim, self.kpt)
         self.blocks = np.zeros((num_seqs, num_kv_heads, self.max_groups, self.bb), np.uint8)
         self.k_res = np.zeros((num_seqs, num_kv_heads, residual, head_dim), np.float16)
         self.v_res = np.zeros_like(self.k_res)
@@ -331,9 +339,12 @@ class OracleCache:
         H, D, R = self.H, self.D, self.R
         kg = self.k_res[s].reshape(H, R // GROUP, GROUP, D)
         vg = self.v_res[s].reshape(H, R // GROUP, GROUP, D)
-        kc, ks, km = quantize_key_group(kg, self.bits)      # per channel
-        vc, vs, vm = quantize_value_tokens(vg, self.bits)   # per token
-        blk = pack_block(kc, ks, km, vc, vs, vm, self.bits)
+        if self.kpt:
+            kc, ks, km = quantize_keys_per_token(kg, self.bits)  # per token
+        else:
+            kc, ks, km = quantize_key_group(kg, self.bits)       # per channel
+        vc, vs, vm = quantize_value_tokens(vg, self.bits)        # per token
+        blk = pack_block(kc, ks, km, vc, vs, vm, self.bits, self.kpt)
         self.blocks[s, :, first_group:first_group + R // GROUP] = blk
 
     # -- reading the state back -------------------------------------------
@@ -353,8 +364,11 @@ class OracleCache:
         vs = [self.v_sink[s, h, :ns].astype(np.float64)]
         ng = Lq // GROUP
         if ng:
-            kc, ksc, kmn, vc, vsc, vmn = unpack_block(self.blocks[s, h, :ng], self.bits, self.D)
-            ks.append(dequantize(kc, ksc[:, None, :], kmn[:, None, :]).reshape(-1, self.D))
+            kc, ksc, kmn, vc, vsc, vmn = unpack_block(self.blocks[s, h, :ng], self.bits, self.D, self.kpt)
+            if self.kpt:
+                ks.append(dequantize(kc, ksc[:, :, None], kmn[:, :, None]).reshape(-1, self.D))
+            else:
+                ks.append(dequantize(kc, ksc[:, None, :], kmn[:, None, :]).reshape(-1, self.D))
             vs.append(dequantize(vc, vsc[:, :, None], vmn[:, :, None]).reshape(-1, self.D))
         ks.append(self.k_res[s, h, :r].astype(np.float64))
         vs.append(self.v_res[s, h, :r].astype(np.float64))

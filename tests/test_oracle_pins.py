@@ -420,3 +420,71 @@ def test_zero_extremes_are_stored_as_positive_zero():
     assert not np.signbit(m).any() and not np.signbit(s).any()
     c, s, m = oracle.quantize_value_tokens(-x, 2)
     assert not np.signbit(m[16:]).any()
+
+
+# ------------------------------------------- per-token key ablation (f1)
+
+def test_per_token_key_block_layout_roundtrip():
+    """Per-token keys keep one fp32 (scale, min) per token: 2560 B (2-bit)
+    and 4608 B (4-bit) per block; packing round-trips."""
+    assert oracle.block_bytes(2, key_per_token=True) == 2 * 1024 + 4 * 4 * 32
+    assert oracle.block_bytes(4, key_per_token=True) == 2 * 2048 + 4 * 4 * 32
+    rng = np.random.default_rng(3)
+    for bits in (2, 4):
+        kc = rng.integers(0, 1 << bits, (3, 32, 128)).astype(np.uint8)
+        vc = rng.integers(0, 1 << bits, (3, 32, 128)).astype(np.uint8)
+        ks, km, vs, vm = (rng.standard_normal((3, 32)).astype(np.float32) for _ in range(4))
+        blk = oracle.kivi.pack_block(kc, ks, km, vc, vs, vm, bits, key_per_token=True)
+        assert blk.shape == (3, oracle.block_bytes(bits, key_per_token=True))
+        out = oracle.kivi.unpack_block(blk, bits, key_per_token=True)
+        for a, b in zip(out, (kc, ks, km, vc, vs, vm)):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_per_token_key_cache_dequant_and_streaming():
+    """A per-token-key cache dequantizes every quantized key as code * s_t +
+    m_t with (s_t, m_t) taken over that token's 128 channels, keeps the
+    window exact, and prefill equals token-by-token appends."""
+    rng = np.random.default_rng(4)
+    S, H, T = 2, 2, 200
+    k = rng.standard_normal((S, H, T, 128)).astype(np.float16)
+    v = rng.standard_normal((S, H, T, 128)).astype(np.float16)
+    a = oracle.OracleCache(S, H, 256, 2, residual=64, key_per_token=True)
+    a.append(k, v, [T, T - 9])
+    b = oracle.OracleCache(S, H, 256, 2, residual=64, key_per_token=True)
+    for t in range(T):
+        b.append(k[:, :, t:t + 1], v[:, :, t:t + 1], [1, int(t < T - 9)])
+    np.testing.assert_array_equal(a.blocks, b.blocks)
+    ns, Lq, r = a.split(0)
+    kh, _ = a.keys_values(0, 1)
+    x = k[0, 1, :Lq].astype(np.float32)
+    mn, mx = x.min(-1), x.max(-1)
+    sc = ((mx - mn) / np.float32(3)).astype(np.float32)
+    c = np.clip(np.rint((x - mn[:, None]) / sc[:, None]), 0, 3)
+    np.testing.assert_allclose(kh[:Lq], c * sc[:, None].astype(np.float64) + mn[:, None], rtol=0, atol=1e-6)
+    np.testing.assert_array_equal(kh[Lq:], k[0, 1, Lq:Lq + r].astype(np.float64))
+
+
+def test_ablation_ordering_on_outlier_keys():
+    """The pages' qualitative ordering on keys with fixed outlier channels
+    (KIVI page, paragraphs 1-3; "KV cache quantization", "Keys are harder
+    than values"): per-channel key groups with the 128-token window beat a
+    32-token window (the smallest the group storage allows, the reading of
+    'no residual'), and both beat per-token key groups, measured as mean
+    attention error against exact fp16 attention."""
+    rng = np.random.default_rng(11)
+    T, Hq = 250, 64
+    k = rng.standard_normal((1, 1, T, 128)).astype(np.float32)
+    k[..., [3, 17, 64, 101]] *= 20
+    k = k.astype(np.float16)
+    v = rng.standard_normal((1, 1, T, 128)).astype(np.float16)
+    q = rng.standard_normal((1, Hq, 128)).astype(np.float16)
+    scale = 1 / np.sqrt(128)
+    exact = np.stack([oracle.dense_attention(q[0, j].astype(np.float64), k[0, 0].astype(np.float64),
+                                             v[0, 0].astype(np.float64), scale) for j in range(Hq)])
+    errs = {}
+    for name, R, kpt in (("channel_R128", 128, False), ("channel_R32", 32, False), ("token_R128", 128, True)):
+        c = oracle.OracleCache(1, 1, 256, 2, residual=R, key_per_token=kpt)
+        c.append(k, v, [T])
+        errs[name] = float(np.abs(c.attention(q)[0].astype(np.float64) - exact).mean())
+    assert errs["channel_R128"] < errs["channel_R32"] < errs["token_R128"], errs
