@@ -23,6 +23,8 @@ int check_geometry(const kvq_cache *c) {
   if (c->num_sink != 0 && c->num_sink != 1) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && !(c->rope_theta > 1.f && isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
+  if (c->key_per_token != 0 && c->key_per_token != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->key_per_token && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
   if (c->num_seqs > 65535 || c->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
@@ -53,6 +55,7 @@ kvq::Geo make_geo(const kvq_cache *c) {
   g.ns = c->num_sink;
   g.bits = c->bits;
   g.pre_rope = c->pre_rope;
+  g.kpt = c->key_per_token;
   g.theta = c->rope_theta;
   g.capacity = c->capacity;
   g.max_groups = max_groups_of(c);
@@ -75,9 +78,9 @@ int from_cuda(cudaError_t e, uint64_t launched) {
 
 extern "C" {
 
-int32_t kvq_block_bytes(int32_t bits, int32_t head_dim) {
-  if (head_dim != kvq::kD || (bits != 2 && bits != 4)) return 0;
-  return kvq::block_bytes(bits);
+int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token) {
+  if (head_dim != kvq::kD || (bits != 2 && bits != 4) || (key_per_token != 0 && key_per_token != 1)) return 0;
+  return kvq::block_bytes(bits, key_per_token != 0);
 }
 
 int32_t kvq_max_groups(const kvq_cache *cache) {
@@ -89,7 +92,7 @@ int64_t kvq_buffer_bytes(const kvq_cache *c, int32_t which) {
   if (check_geometry(c)) return -1;
   const int64_t sh = static_cast<int64_t>(c->num_seqs) * c->num_kv_heads;
   switch (which) {
-    case KVQ_BUF_BLOCKS: return sh * max_groups_of(c) * kvq::block_bytes(c->bits);
+    case KVQ_BUF_BLOCKS: return sh * max_groups_of(c) * kvq::block_bytes(c->bits, c->key_per_token != 0);
     case KVQ_BUF_K_RES:
     case KVQ_BUF_V_RES: return sh * c->residual * kvq::kD * 2;
     case KVQ_BUF_K_SINK:

@@ -77,9 +77,9 @@ struct DecodeArgs {
 #define KVQ_DECODE_RING_4BIT 2
 #endif
 
-template <int BITS, int GQ, bool ROPE>
+template <int BITS, int GQ, bool ROPE, bool KPT>
 struct WarpSmem {
-  static constexpr int BB = block_bytes(BITS);
+  static constexpr int BB = block_bytes(BITS, KPT);
   static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2) : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
   static constexpr int BAR_OFF = NS * BB;
   static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
@@ -424,6 +424,27 @@ __device__ __forceinline__ void group_scores(const uint8_t *blk, const QkOperand
     for (int hh = 0; hh < 2; ++hh) z[2 * mt + hh] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[2 * mt + hh], beta);
 }
 
+// Scores of one packed group when keys are grouped per token: the B
+// fragments hold the query itself (fp16, exact; column 2h head h, column
+// 2h + 1 zero), built once per (sequence, KV head), and token t's scale s_t
+// and min m_t enter as z = s_t (q . c_t) kf + m_t (zscale sum_d q_d).
+template <int BITS>
+__device__ __forceinline__ void group_scores_kpt(const uint8_t *blk, const uint32_t (&bq)[8][2],
+                                                 const float (&kfac)[4], float zsq, int lane, float (&z)[4]) {
+  float acc[2][4];
+  qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
+  const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
+  const float *km = reinterpret_cast<const float *>(blk + off_km(BITS, true));
+  const int g = lane >> 2;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tau = 2 * mt + hh, t = 8 * tau + g;
+      z[tau] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[tau] * ks[t], zsq * km[t]);
+    }
+}
+
 // o += values of one group weighted by ps (score layout: token 8*tau + g,
 // head q).  The value mma's B column h carries head h's p_t * scale_t as one
 // fp16 (its rounding error, at most 2^-11 relative per weight, enters the
@@ -463,10 +484,10 @@ __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_
 #define KVQ_DECODE_MIN_BLOCKS_GQ4 3
 #endif
 
-template <int BITS, int GQ, bool ROPE>
+template <int BITS, int GQ, bool ROPE, bool KPT>
 __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
     decode_kernel(DecodeArgs a) {
-  using WS = WarpSmem<BITS, GQ, ROPE>;
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
   constexpr int NS = WS::NS, BB = WS::BB;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -777,10 +798,34 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
       if (g_lo < g_hi) {
         if (!ROPE) {
           QkOperand<GQ> qo;
-          qo.init(q_s, lane, a.zscale);
           float kfac[4];
+          uint32_t bqc[8][2];  // keys per token: the query's B fragments, fixed for the pair
+          float zsq = 0.f;     // keys per token: zscale * sum_d q_d of this lane's head
+          if (!KPT) {
+            qo.init(q_s, lane, a.zscale);
 #pragma unroll
-          for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
+            for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
+          } else {
+            const int hd = min(g >> 1, GQ - 1);
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float2 qv = *reinterpret_cast<const float2 *>(q_s + hd * kD + 16 * kt + 8 * j + 2 * q);
+                bqc[kt][j] = (g & 1) ? 0u : h2_as_u32(__floats2half2_rn(qv.x, qv.y));
+              }
+            float qs[GQ];
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              qs[hh] = q_s[hh * kD + lane] + q_s[hh * kD + lane + 32] + q_s[hh * kD + lane + 64] +
+                       q_s[hh * kD + lane + 96];
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) qs[hh] += __shfl_xor_sync(kFull, qs[hh], off);
+              if (hh == min(q, GQ - 1)) zsq = qs[hh] * a.zscale;
+            }
+#pragma unroll
+            for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * a.zscale;
+          }
           // two groups (64 tokens) per iteration: independent score mmas, one
           // softmax update, two value mmas
           for (int gi = g_lo; gi < g_hi; gi += 2) {
@@ -793,9 +838,15 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
             }
             const uint8_t *ba = ring + sa * BB, *bb = ring + sb * BB;
             float za[4], zb[4];
-            group_scores<BITS, GQ>(ba, qo, kfac, stage, lane, za);
+            if (KPT)
+              group_scores_kpt<BITS>(ba, bqc, kfac, zsq, lane, za);
+            else
+              group_scores<BITS, GQ>(ba, qo, kfac, stage, lane, za);
             if (two) {
-              group_scores<BITS, GQ>(bb, qo, kfac, stage, lane, zb);
+              if (KPT)
+                group_scores_kpt<BITS>(bb, bqc, kfac, zsq, lane, zb);
+              else
+                group_scores<BITS, GQ>(bb, qo, kfac, stage, lane, zb);
             } else {
               zb[0] = zb[1] = zb[2] = zb[3] = -INFINITY;
             }
@@ -806,10 +857,10 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
             const float m_new = fmaxf(m_run, mx);
             const float alpha = fast_exp2(m_run - m_new);
-            const float *vsa = reinterpret_cast<const float *>(ba + off_vs(BITS));
-            const float *vma = reinterpret_cast<const float *>(ba + off_vm(BITS));
-            const float *vsb = reinterpret_cast<const float *>(bb + off_vs(BITS));
-            const float *vmb = reinterpret_cast<const float *>(bb + off_vm(BITS));
+            const float *vsa = reinterpret_cast<const float *>(ba + off_vs(BITS, KPT));
+            const float *vma = reinterpret_cast<const float *>(ba + off_vm(BITS, KPT));
+            const float *vsb = reinterpret_cast<const float *>(bb + off_vs(BITS, KPT));
+            const float *vmb = reinterpret_cast<const float *>(bb + off_vm(BITS, KPT));
             float psa[4], psb[4], psum = 0.f, mus = 0.f;
 #pragma unroll
             for (int tau = 0; tau < 4; ++tau) {
@@ -1085,11 +1136,11 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 
 // Resident CTAs per SM of one instantiation on the current device, and the
 // device's SM count (cached per device ordinal).
-template <int BITS, int GQ, bool ROPE>
+template <int BITS, int GQ, bool ROPE, bool KPT>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
-  using WS = WarpSmem<BITS, GQ, ROPE>;
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
-  auto kern = decode_kernel<BITS, GQ, ROPE>;
+  auto kern = decode_kernel<BITS, GQ, ROPE, KPT>;
   static int resident[64] = {};
   static int sms[64] = {};
   bytes_out = bytes;
@@ -1124,10 +1175,10 @@ int set_decode_warps(int warps) {
 
 // Warps one launch spreads the work over: every resident warp of the device
 // (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
-template <int BITS, int GQ, bool ROPE>
+template <int BITS, int GQ, bool ROPE, bool KPT>
 static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   int per_sm = 0, n_sm = 0, bytes = 0;
-  cudaError_t e = kernel_slots<BITS, GQ, ROPE>(per_sm, n_sm, bytes);
+  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT>(per_sm, n_sm, bytes);
   if (e != cudaSuccess) return e;
   int nw = g_warps_override ? g_warps_override : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
   nw = max(nw, 1);
@@ -1136,13 +1187,15 @@ static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
     decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  decode_kernel<BITS, GQ, ROPE><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
+  decode_kernel<BITS, GQ, ROPE, KPT><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <int BITS, int GQ>
 static cudaError_t launch_g(const DecodeArgs &a, cudaStream_t stream) {
-  return a.geo.pre_rope ? launch_t<BITS, GQ, true>(a, stream) : launch_t<BITS, GQ, false>(a, stream);
+  // keys grouped per token are never stored pre-RoPE (rejected at the boundary)
+  if (a.geo.kpt) return launch_t<BITS, GQ, false, true>(a, stream);
+  return a.geo.pre_rope ? launch_t<BITS, GQ, true, false>(a, stream) : launch_t<BITS, GQ, false, false>(a, stream);
 }
 
 template <int BITS>

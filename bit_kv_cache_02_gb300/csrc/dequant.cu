@@ -22,8 +22,9 @@ __device__ __forceinline__ uint32_t tile_code(const uint8_t *tile, int row, int 
 }
 
 // grid = (group slot + 1, KV head, sequence); the last slot converts the
-// sink and the window.
-template <int BITS>
+// sink and the window.  KPT: key scale and min per token instead of per
+// channel.
+template <int BITS, bool KPT>
 __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict__ k_out, float *__restrict__ v_out) {
   const int s = blockIdx.z, h = blockIdx.y, gi = blockIdx.x;
   const int L = geo.seq_len[s];
@@ -34,17 +35,17 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
   float *vo = v_out + sh * geo.capacity * kD;
   if (gi < geo.max_groups) {
     if (gi >= sp.Lq / kG) return;
-    const uint8_t *blk = geo.blocks + (sh * geo.max_groups + gi) * static_cast<size_t>(block_bytes(BITS));
+    const uint8_t *blk = geo.blocks + (sh * geo.max_groups + gi) * static_cast<size_t>(block_bytes(BITS, KPT));
     const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
-    const float *km = reinterpret_cast<const float *>(blk + off_km(BITS));
-    const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
-    const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
+    const float *km = reinterpret_cast<const float *>(blk + off_km(BITS, KPT));
+    const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS, KPT));
+    const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS, KPT));
     const int p0 = sp.nsink + gi * kG;
     for (int idx = threadIdx.x; idx < kG * kD; idx += blockDim.x) {
       const int t = idx / kD, d = idx % kD;
       const uint32_t ck = tile_code<BITS>(blk + off_kc(BITS), t, d, kD);
       const uint32_t cv = tile_code<BITS>(blk + off_vc(BITS), d, t, kG);
-      ko[static_cast<size_t>(p0 + t) * kD + d] = fmaf(static_cast<float>(ck), ks[d], km[d]);
+      ko[static_cast<size_t>(p0 + t) * kD + d] = fmaf(static_cast<float>(ck), ks[KPT ? t : d], km[KPT ? t : d]);
       vo[static_cast<size_t>(p0 + t) * kD + d] = fmaf(static_cast<float>(cv), vs[t], vm[t]);
     }
   } else {
@@ -72,9 +73,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
 cudaError_t launch_dequant(const Geo &geo, float *k_out, float *v_out, cudaStream_t stream, uint64_t *launches) {
   dim3 grid(geo.max_groups + 1, geo.H, geo.S);
   if (geo.bits == 2)
-    dequant_kernel<2><<<grid, 256, 0, stream>>>(geo, k_out, v_out);
+    (geo.kpt ? dequant_kernel<2, true> : dequant_kernel<2, false>)<<<grid, 256, 0, stream>>>(geo, k_out, v_out);
   else
-    dequant_kernel<4><<<grid, 256, 0, stream>>>(geo, k_out, v_out);
+    (geo.kpt ? dequant_kernel<4, true> : dequant_kernel<4, false>)<<<grid, 256, 0, stream>>>(geo, k_out, v_out);
   ++*launches;
   return cudaGetLastError();
 }

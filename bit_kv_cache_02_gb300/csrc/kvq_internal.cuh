@@ -25,18 +25,24 @@ namespace kvq {
 constexpr int kD = 128;       // head dimension
 constexpr int kG = 32;        // tokens per group
 
+// Key metadata holds one (scale, min) per channel, or per token when keys
+// are grouped per token (kpt).
 __host__ __device__ constexpr int code_tile_bytes(int bits) { return kG * kD * bits / 8; }
-__host__ __device__ constexpr int block_bytes(int bits) { return 2 * code_tile_bytes(bits) + 8 * kD + 8 * kG; }
+__host__ __device__ constexpr int kmeta_n(bool kpt) { return kpt ? kG : kD; }
+__host__ __device__ constexpr int block_bytes(int bits, bool kpt = false) {
+  return 2 * code_tile_bytes(bits) + 8 * kmeta_n(kpt) + 8 * kG;
+}
 __host__ __device__ constexpr int off_kc(int) { return 0; }
 __host__ __device__ constexpr int off_vc(int bits) { return code_tile_bytes(bits); }
 __host__ __device__ constexpr int off_ks(int bits) { return 2 * code_tile_bytes(bits); }
-__host__ __device__ constexpr int off_km(int bits) { return off_ks(bits) + 4 * kD; }
-__host__ __device__ constexpr int off_vs(int bits) { return off_km(bits) + 4 * kD; }
-__host__ __device__ constexpr int off_vm(int bits) { return off_vs(bits) + 4 * kG; }
+__host__ __device__ constexpr int off_km(int bits, bool kpt = false) { return off_ks(bits) + 4 * kmeta_n(kpt); }
+__host__ __device__ constexpr int off_vs(int bits, bool kpt = false) { return off_km(bits, kpt) + 4 * kmeta_n(kpt); }
+__host__ __device__ constexpr int off_vm(int bits, bool kpt = false) { return off_vs(bits, kpt) + 4 * kG; }
 
 // Cache geometry and buffers as the kernels see them.
 struct Geo {
   int S, H, R, ns, bits, pre_rope;
+  int kpt;  // keys grouped per token
   float theta;
   int capacity;
   int max_groups;

@@ -102,6 +102,7 @@ struct __align__(128) QuantSmem {
   SliceQ kq[kD];             // key channel constants
   SliceQ vq[kG];             // value token constants
   uint32_t vstat[kG / 2][2]; // value (min, max) half2 of each token pair
+  uint32_t kvst[kG / 2][2];  // key (min, max) half2 of each token pair (keys grouped per token)
   __align__(128) uint8_t blk[block_bytes(4)];  // the packed block being built
 };
 
@@ -208,8 +209,9 @@ __device__ __forceinline__ uint32_t pack_word(const uint32_t (&x)[NF], const f2x
 // (s, h)) and write its block with a bulk copy issued by thread 0.  Before
 // the call thread 0 must have waited (bulk_wait_read) for the previous
 // block's copy out of sm.blk.  Three CTA barriers inside, the last one after
-// every read of the tiles.
-template <int BITS>
+// every read of the tiles.  KPT: keys grouped per token (scale and min over
+// each token's channels, like values) instead of per channel.
+template <int BITS, bool KPT>
 __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r, const Geo &geo, int s, int h,
                                                int i0) {
   constexpr int NU = 8 / BITS;  // fields per byte
@@ -224,20 +226,42 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   {
     *reinterpret_cast<uint4 *>(&sm.k[(2 * p) * 64 + 4 * c8]) = r.k[0];
     *reinterpret_cast<uint4 *>(&sm.k[(2 * p + 1) * 64 + 4 * c8]) = r.k[1];
-    const uint32_t ka[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
-    const uint32_t kb[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
-    uint32_t kmn[4], kmx[4];
+    if (!KPT) {
+      const uint32_t ka[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
+      const uint32_t kb[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
+      uint32_t kmn[4], kmx[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kmn[i] = h2min(ka[i], kb[i]);
-      kmx[i] = h2max(ka[i], kb[i]);
-      kmn[i] = h2min(kmn[i], __shfl_xor_sync(0xffffffffu, kmn[i], 16));  // the warp's other token pair
-      kmx[i] = h2max(kmx[i], __shfl_xor_sync(0xffffffffu, kmx[i], 16));
-    }
-    if (lane < 16) {
-      uint4 *ks = reinterpret_cast<uint4 *>(&sm.kstat[warp][4 * c8][0]);
-      ks[0] = make_uint4(kmn[0], kmx[0], kmn[1], kmx[1]);
-      ks[1] = make_uint4(kmn[2], kmx[2], kmn[3], kmx[3]);
+      for (int i = 0; i < 4; ++i) {
+        kmn[i] = h2min(ka[i], kb[i]);
+        kmx[i] = h2max(ka[i], kb[i]);
+        kmn[i] = h2min(kmn[i], __shfl_xor_sync(0xffffffffu, kmn[i], 16));  // the warp's other token pair
+        kmx[i] = h2max(kmx[i], __shfl_xor_sync(0xffffffffu, kmx[i], 16));
+      }
+      if (lane < 16) {
+        uint4 *ks = reinterpret_cast<uint4 *>(&sm.kstat[warp][4 * c8][0]);
+        ks[0] = make_uint4(kmn[0], kmx[0], kmn[1], kmx[1]);
+        ks[1] = make_uint4(kmn[2], kmx[2], kmn[3], kmx[3]);
+      }
+    } else {  // per-token keys: (token 2p, token 2p + 1) min/max over the 128 channels
+      const __half *ka = reinterpret_cast<const __half *>(&r.k[0]);
+      const __half *kb = reinterpret_cast<const __half *>(&r.k[1]);
+      __half2 kn2 = __halves2half2(ka[0], kb[0]), kx2 = kn2;
+#pragma unroll
+      for (int c = 1; c < 8; ++c) {
+        const __half2 pr = __halves2half2(ka[c], kb[c]);
+        kn2 = __hmin2(kn2, pr);
+        kx2 = __hmax2(kx2, pr);
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        const uint32_t a = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&kn2), o);
+        const uint32_t b = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&kx2), o);
+        kn2 = __hmin2(kn2, *reinterpret_cast<const __half2 *>(&a));
+        kx2 = __hmax2(kx2, *reinterpret_cast<const __half2 *>(&b));
+      }
+      if (c8 == 0)
+        *reinterpret_cast<uint2 *>(sm.kvst[p]) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&kn2), *reinterpret_cast<uint32_t *>(&kx2));
     }
     const __half *va = reinterpret_cast<const __half *>(&r.v[0]);
     const __half *vb = reinterpret_cast<const __half *>(&r.v[1]);
@@ -264,8 +288,16 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
           make_uint2(*reinterpret_cast<uint32_t *>(&mn2), *reinterpret_cast<uint32_t *>(&mx2));
   }
   __syncthreads();
-  // ---- key channel statistics over the 8 warps' partials; block scales
-  if (tid < kD) {
+  // ---- key channel statistics over the 8 warps' partials (or key token
+  // statistics); block scales
+  if (KPT && tid < kG) {
+    const float2 mnf = h2_to_f2_pos0(sm.kvst[tid >> 1][0]), mxf = h2_to_f2_pos0(sm.kvst[tid >> 1][1]);
+    const float lo = tid & 1 ? mnf.y : mnf.x, hi = tid & 1 ? mxf.y : mxf.x;
+    const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
+    sm.kq[tid] = make_slice(lo, sc, levels);
+    blkf[off_ks(BITS) / 4 + tid] = sc;
+    blkf[off_km(BITS, KPT) / 4 + tid] = lo;
+  } else if (!KPT && tid < kD) {
     const int cp = tid >> 1, e = tid & 1;
     uint32_t mn = sm.kstat[0][cp][0], mx = sm.kstat[0][cp][1];
 #pragma unroll
@@ -278,15 +310,15 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
     sm.kq[tid] = make_slice(lo, sc, levels);
     blkf[off_ks(BITS) / 4 + tid] = sc;
-    blkf[off_km(BITS) / 4 + tid] = lo;
-  } else if (tid < kD + kG) {  // value tokens
+    blkf[off_km(BITS, KPT) / 4 + tid] = lo;
+  } else if (tid >= kD && tid < kD + kG) {  // value tokens
     const int t = tid - kD;
     const float2 mnf = h2_to_f2_pos0(sm.vstat[t >> 1][0]), mxf = h2_to_f2_pos0(sm.vstat[t >> 1][1]);
     const float lo = t & 1 ? mnf.y : mnf.x, hi = t & 1 ? mxf.y : mxf.x;
     const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
     sm.vq[t] = make_slice(lo, sc, levels);
-    blkf[off_vs(BITS) / 4 + t] = sc;
-    blkf[off_vm(BITS) / 4 + t] = lo;
+    blkf[off_vs(BITS, KPT) / 4 + t] = sc;
+    blkf[off_vm(BITS, KPT) / 4 + t] = lo;
   }
   __syncthreads();
 
@@ -300,14 +332,16 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     const int jx = kt >> 2;
     f2x rcp[2], cc[2];
     float tol = 0.f;
+    if (!KPT) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const SliceQ a = sm.kq[16 * kt + 8 * j + 2 * q], b = sm.kq[16 * kt + 8 * j + 2 * q + 1];
-      rcp[j] = f2_pack(a.rcp, b.rcp);
-      cc[j] = f2_pack(a.c, b.c);
-      tol = fmaxf(tol, fmaxf(a.tol, b.tol));
+      for (int j = 0; j < 2; ++j) {
+        const SliceQ a = sm.kq[16 * kt + 8 * j + 2 * q], b = sm.kq[16 * kt + 8 * j + 2 * q + 1];
+        rcp[j] = f2_pack(a.rcp, b.rcp);
+        cc[j] = f2_pack(a.c, b.c);
+        tol = fmaxf(tol, fmaxf(a.tol, b.tol));
+      }
     }
-    const float thr = 0.5f - tol;
+    const float thr_ch = 0.5f - tol;
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
       const int g = 2 * warp + gi;
@@ -316,16 +350,25 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
         uint32_t x[2 * NU];
         f2x fr[2 * NU], fc[2 * NU];
         int pos[2 * NU];
+        float thr = thr_ch;
 #pragma unroll
-        for (int u = 0; u < NU; ++u)
+        for (int u = 0; u < NU; ++u) {
+          f2x tr = 0, tc = 0;
+          if (KPT) {  // both fields of a pair belong to token 8 tau + g
+            const SliceQ a = sm.kq[8 * (hw * NU + u) + g];
+            tr = f2_pack(a.rcp, a.rcp);
+            tc = f2_pack(a.c, a.c);
+            thr = fminf(thr, 0.5f - a.tol);
+          }
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
             const int j = jj ^ jx, tau = hw * NU + u, f = 2 * u + jj;
             x[f] = sm.k[(8 * tau + g) * 64 + 8 * kt + 4 * j + q];
-            fr[f] = jx ? rcp[jj ^ 1] : rcp[jj];
-            fc[f] = jx ? cc[jj ^ 1] : cc[jj];
+            fr[f] = KPT ? tr : (jx ? rcp[jj ^ 1] : rcp[jj]);
+            fc[f] = KPT ? tc : (jx ? cc[jj ^ 1] : cc[jj]);
             pos[f] = 8 * j + BITS * u;
           }
+        }
         bool near;
         uint32_t word = pack_word<2 * NU>(x, fr, fc, pos, thr, near);
         if (__any_sync(0xffffffffu, near) && near) {
@@ -335,7 +378,8 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
             const int tau = hw * NU + u, ch = 16 * kt + 8 * j + 2 * q + e;
             const uint32_t w2 = sm.k[(8 * tau + g) * 64 + (ch >> 1)];
             const float xv = __half2float(reinterpret_cast<const __half *>(&w2)[e]);
-            word |= exact_code<BITS>(xv, sm.kq[ch].mn, blkf[off_ks(BITS) / 4 + ch]) << (16 * e + 8 * j + BITS * u);
+            const int sl = KPT ? 8 * tau + g : ch;
+            word |= exact_code<BITS>(xv, sm.kq[sl].mn, blkf[off_ks(BITS) / 4 + sl]) << (16 * e + 8 * j + BITS * u);
           }
         }
         const int w = kt * WH + hw, L = 4 * g + q;
@@ -387,7 +431,7 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
             const int tau = hw * NU + u, tok = 16 * kt + 8 * j + 2 * q + e;
             const uint32_t w2 = sm.v[vword(32 * P + 8 * tau + g, tok >> 1)];
             const float xv = __half2float(reinterpret_cast<const __half *>(&w2)[e]);
-            word |= exact_code<BITS>(xv, sm.vq[tok].mn, blkf[off_vs(BITS) / 4 + tok]) << (16 * e + 8 * j + BITS * u);
+            word |= exact_code<BITS>(xv, sm.vq[tok].mn, blkf[off_vs(BITS, KPT) / 4 + tok]) << (16 * e + 8 * j + BITS * u);
           }
         }
         const int w = (2 * P + kt) * WH + hw, L = 4 * g + q;
@@ -399,8 +443,8 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   __syncthreads();
   if (tid == 0) {
     uint8_t *dst = geo.blocks + ((static_cast<size_t>(s) * geo.H + h) * geo.max_groups + i0 / kG) *
-                                    static_cast<size_t>(block_bytes(BITS));
-    bulk_s2g(dst, sm.blk, block_bytes(BITS));
+                                    static_cast<size_t>(block_bytes(BITS, KPT));
+    bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT));
   }
 }
 
@@ -413,7 +457,7 @@ constexpr int kLenMask = (1 << kLenBits) - 1;
 // t % gmax of (sequence, KV head) t / gmax (fewer than 2^31 tasks); CTA b
 // takes tasks b, b + grid, ... and loads the next task's rows while it
 // quantizes the current one.
-template <int BITS>
+template <int BITS, bool KPT>
 __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                        const __half *__restrict__ v_new,
                                                                        const int *__restrict__ new_len,
@@ -463,7 +507,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, 
     const bool more = find(nxt);
     if (more) load_group(rn, geo, nxt, k_new, v_new, max_new);
     if (threadIdx.x == 0) bulk_wait_read();  // the previous block's copy has left sm.blk
-    quantize_group<BITS>(sm, rc, geo, cur.s, cur.h, cur.i0);
+    quantize_group<BITS, KPT>(sm, rc, geo, cur.s, cur.h, cur.i0);
     if (!more) break;
     cur = nxt;
     rc = rn;
@@ -516,7 +560,7 @@ __device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1,
 // fills, the copy would overwrite window slots the sequence's other CTAs may
 // still be quantizing, so the CTAs arrive after quantizing and the last one
 // copies the new tokens of every head.
-template <int BITS>
+template <int BITS, bool KPT>
 __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                     const __half *__restrict__ v_new,
                                                                     const int *__restrict__ new_len, int max_new) {
@@ -593,7 +637,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, 
         load_group(rn, geo, g, k_new, v_new, max_new);
       }
       if (threadIdx.x == 0) bulk_wait_read();
-      quantize_group<BITS>(sm, rc, geo, s, h, i0);
+      quantize_group<BITS, KPT>(sm, rc, geo, s, h, i0);
       rc = rn;
     }
     // quantize_group ends with a barrier: every read of the window is done
@@ -637,7 +681,7 @@ int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R /
 
 // Persistent CTAs of the flush kernel on the current device: every resident
 // slot (cached per device ordinal).
-template <int BITS>
+template <int BITS, bool KPT>
 static cudaError_t flush_grid(int &ctas) {
   static int cache[64] = {};
   int dev = 0;
@@ -648,7 +692,7 @@ static cudaError_t flush_grid(int &ctas) {
     return cudaSuccess;
   }
   int per_sm = 0, n_sm = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_flush_kernel<BITS>, kQuantThreads, 0)) !=
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_flush_kernel<BITS, KPT>, kQuantThreads, 0)) !=
       cudaSuccess)
     return e;
   if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -662,25 +706,24 @@ cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __hal
   // a decode-sized append (at most one window fills): one kernel
   if (max_new <= geo.R && geo.capacity <= kLenMask && geo.H < (1 << (31 - kLenBits))) {
     dim3 grid(geo.H, geo.S);
-    if (geo.bits == 2)
-      step_append_kernel<2><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
-    else
-      step_append_kernel<4><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+    auto kern = geo.bits == 2 ? (geo.kpt ? step_append_kernel<2, true> : step_append_kernel<2, false>)
+                              : (geo.kpt ? step_append_kernel<4, true> : step_append_kernel<4, false>);
+    kern<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
     ++*launches;
     return cudaGetLastError();
   }
   const int gmax = max_flush_groups(geo.R, max_new);
   if (gmax > 0) {
     int ctas = 0;
-    cudaError_t e = geo.bits == 2 ? flush_grid<2>(ctas) : flush_grid<4>(ctas);
+    cudaError_t e = geo.bits == 2 ? (geo.kpt ? flush_grid<2, true>(ctas) : flush_grid<2, false>(ctas))
+                                  : (geo.kpt ? flush_grid<4, true>(ctas) : flush_grid<4, false>(ctas));
     if (e != cudaSuccess) return e;
     const long long ntask = static_cast<long long>(gmax) * geo.H * geo.S;
     if (ntask > 2147483647LL) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(min(static_cast<long long>(ctas), ntask));
-    if (geo.bits == 2)
-      quant_flush_kernel<2><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
-    else
-      quant_flush_kernel<4><<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
+    auto kern = geo.bits == 2 ? (geo.kpt ? quant_flush_kernel<2, true> : quant_flush_kernel<2, false>)
+                              : (geo.kpt ? quant_flush_kernel<4, true> : quant_flush_kernel<4, false>);
+    kern<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

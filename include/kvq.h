@@ -104,6 +104,10 @@ typedef struct kvq_cache {
   int32_t  pre_rope;       /* 1: keys stored pre-RoPE, rotated at read  */
   float    rope_theta;     /* RoPE base (e.g. 10000), used if pre_rope  */
   int32_t  capacity;       /* max tokens per sequence, >= 1             */
+  int32_t  key_per_token;  /* 0: keys grouped per channel over 32 tokens;
+                              1: per token over its D channels (the
+                              baseline KIVI compares against; not with
+                              pre_rope)                                 */
   uint8_t  *blocks;
   uint16_t *k_res, *v_res;
   uint16_t *k_sink, *v_sink;
@@ -111,9 +115,10 @@ typedef struct kvq_cache {
   int32_t  *status;
 } kvq_cache;
 
-/* Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128);
- * 0 for an unsupported (bits, head_dim). */
-int32_t kvq_block_bytes(int32_t bits, int32_t head_dim);
+/* Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128 with
+ * per-channel keys; 2560 / 4608 with per-token keys); 0 for an unsupported
+ * (bits, head_dim). */
+int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token);
 
 /* Quantized groups per (sequence, KV head) the cache can hold; -1 on bad
  * geometry. */

@@ -45,8 +45,9 @@ def _struct(kvq, **kw):
 
 
 def test_sizes(kvq):
-    assert kvq.lib.kvq_block_bytes(2, 128) == 3328 and kvq.lib.kvq_block_bytes(4, 128) == 5376
-    assert kvq.lib.kvq_block_bytes(3, 128) == 0 and kvq.lib.kvq_block_bytes(2, 64) == 0
+    assert kvq.lib.kvq_block_bytes(2, 128, 0) == 3328 and kvq.lib.kvq_block_bytes(4, 128, 0) == 5376
+    assert kvq.lib.kvq_block_bytes(2, 128, 1) == 2560 and kvq.lib.kvq_block_bytes(4, 128, 1) == 4608
+    assert kvq.lib.kvq_block_bytes(3, 128, 0) == 0 and kvq.lib.kvq_block_bytes(2, 64, 0) == 0
     st = _struct(kvq)
     # (1000 - 1) // 128 * 128 = 896 quantized tokens -> 28 groups
     assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == 28
@@ -56,11 +57,14 @@ def test_sizes(kvq):
     assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_SEQ_LEN) == 8
     st0 = _struct(kvq, num_sink=0)
     assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st0), kvq.BUF_K_SINK) == 0
+    stk = _struct(kvq, key_per_token=1)   # per-token key metadata: 2560-byte blocks
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(stk), kvq.BUF_BLOCKS) == 2 * 3 * 28 * 2560
 
 
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 64, -2), ("bits", 3, -2), ("group", 16, -2), ("residual", 100, -2),
     ("residual", 256, -2), ("num_sink", 2, -2), ("num_seqs", 0, -1), ("capacity", 0, -1),
+    ("key_per_token", 2, -1),
 ])
 def test_bad_geometry_rejected(kvq, field, value, code):
     st = _struct(kvq, **{field: value})
@@ -68,6 +72,15 @@ def test_bad_geometry_rejected(kvq, field, value, code):
     assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 3, 10) == -1
     fake = ctypes.c_void_p(1 << 20)
     assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == code
+
+
+def test_key_per_token_with_pre_rope_unsupported(kvq):
+    """Per-token key grouping is the ablation of the per-channel method and is
+    not combined with pre-RoPE keys."""
+    st = _struct(kvq, key_per_token=1, pre_rope=1)
+    assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -2
 
 
 def test_workspace_sizing(kvq):

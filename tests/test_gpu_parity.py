@@ -70,9 +70,9 @@ def _attn_close(got, want):
     return float(err.max())
 
 
-def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128):
-    cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope)
-    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns)
+def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False):
+    cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope, key_per_token=kpt)
+    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt)
     return cache, orc
 
 
@@ -209,6 +209,36 @@ def test_residual_window_sizes(kvq, R, bits, ns, pre_rope):
             q = _rand_q(S, 2 * H, seed=i)
             _attn_close(_attend(kvq, cache, q, T), orc.attention(q, pre_rope=pre_rope))
     assert pos == T
+
+
+@pytest.mark.parametrize("bits,gq,ns", [(2, 1, 0), (2, 4, 1), (4, 2, 0), (4, 1, 1)])
+def test_key_per_token_ablation(kvq, bits, gq, ns):
+    """Keys grouped per token (the ablation): a prefill (two-kernel path), then
+    per-token and chunked appends (one-kernel path) leave the oracle's bytes
+    (per-token key scales and mins in the blocks), and attention and
+    dequantization match."""
+    S, H, T = 3, 2, 420
+    k, v = _rand_kv(S, H, T, seed=70 + bits + gq)
+    cache, orc = _build(kvq, S, H, T + 8, bits, ns=ns, kpt=True)
+    assert cache.block_bytes == (2560 if bits == 2 else 4608)
+    lens = np.array([T, T - 29, 140])
+    _append(kvq, cache, orc, k[:, :, :200], v[:, :, :200], np.minimum(lens, 200))
+    pos = 200
+    for step in [1] * 70 + [64, 86]:
+        sl = np.clip(lens - pos, 0, step).astype(np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+    assert pos == T
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=gq)
+    _attn_close(_attend(kvq, cache, q, T), orc.attention(q))
+    K = torch.full((S, H, T + 8, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    for s, L in enumerate(lens):
+        np.testing.assert_array_max_ulp(K.cpu().numpy()[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
+        np.testing.assert_array_max_ulp(V.cpu().numpy()[s, :, :L], Vo[s, :, :L].astype(np.float32), maxulp=1)
 
 
 def test_decode_step_flush_then_attend(kvq):
