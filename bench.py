@@ -113,7 +113,7 @@ def decode_bytes(lengths, w):
     group block (K/V codes + fp32 metadata) once, every fp16 sink/window
     token (K and V) once, the query and the output."""
     from bit_kv_cache_02_gb300.kvq import block_bytes
-    bb = block_bytes(w.bits)
+    bb = block_bytes(w.bits, key_per_token=w.key_per_token)
     total = 0
     for L in lengths:
         ns = min(L, w.num_sink)
@@ -243,7 +243,7 @@ def prefill_bytes(lengths, w):
     write their share of the packed blocks; window and sink tokens are read
     and written as fp16."""
     from bit_kv_cache_02_gb300.kvq import block_bytes
-    bb = block_bytes(w.bits)
+    bb = block_bytes(w.bits, key_per_token=w.key_per_token)
     total = 0
     for L in lengths:
         L = int(L)
@@ -261,7 +261,7 @@ def build_caches(kvq, w, layers, pre, capacity, device):
     stream = torch.cuda.current_stream(device)
     for layer in range(layers):
         c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
-                        pre_rope=w.pre_rope, device=device)
+                        pre_rope=w.pre_rope, device=device, key_per_token=w.key_per_token)
         T = int(pre.max())
         k, v = synth.kv_tokens(w, layer, T, device=device)
         k, v = k.contiguous(), v.contiguous()
@@ -458,7 +458,7 @@ class OracleSample:
         k, v = synth.kv_tokens(ws, 0, self.ctx + extra)
         k, v = k.numpy(), v.numpy()
         c = oracle.OracleCache(n, 1, self.ctx + extra, self.w.bits, residual=self.w.residual,
-                               num_sink=self.w.num_sink)
+                               num_sink=self.w.num_sink, key_per_token=self.w.key_per_token)
         c.append(k[:, :, :self.ctx], v[:, :, :self.ctx], [self.ctx] * n)
         return ws, k, v, c
 
@@ -509,6 +509,7 @@ def main():
     config = {"workload": w.name, "layers": layers, "seqs_per_gpu": w.seqs, "q_heads": w.q_heads,
               "kv_heads": w.kv_heads, "head_dim": 128, "ctx": w.ctx, "bits": w.bits, "group": 32,
               "residual": w.residual, "num_sink": w.num_sink, "pre_rope": w.pre_rope,
+              "key_per_token": w.key_per_token,
               "ragged": bool(w.ragged_min), "parallelism": f"replicas{world}",
               "l2": "inputs larger than L2: each layer's packed cache is streamed once per step"}
 

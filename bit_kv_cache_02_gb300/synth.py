@@ -36,6 +36,7 @@ class Workload:
     outlier_mult: float = 15.0
     seed: int = 0
     decode_tokens: int = 1   # tokens appended before attending
+    key_per_token: bool = False  # keys grouped per token (the ablation of per-channel keys)
     extra: dict = field(default_factory=dict)
 
 
@@ -47,6 +48,9 @@ WORKLOADS = {
     "llama3_8b_gqa_4bit": Workload("llama3_8b_gqa_4bit", 32, 64, 32, 8, 8192, 4, ragged_min=1024),
     "long_1m": Workload("long_1m", 1, 1, 32, 32, 1 << 20, 2),
     "kvquant_prerope": Workload("kvquant_prerope", 32, 8, 32, 32, 16384, 2, num_sink=1, pre_rope=True),
+    # the Llama-2 shape with keys grouped per token (ablation row)
+    "llama2_7b_mha_key_per_token": Workload("llama2_7b_mha_key_per_token", 32, 16, 32, 32, 4096, 2,
+                                            key_per_token=True),
 }
 
 
