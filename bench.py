@@ -124,7 +124,7 @@ def decode_bytes(lengths, w):
     return total
 
 
-def kernel_source_hash(names=("decode.cu", "kvq_internal.cuh")):
+def kernel_source_hash(names=("decode_kernel.cuh", "kvq_internal.cuh")):
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(ROOT, "bit_kv_cache_02_gb300", "csrc", name), "rb") as f:
@@ -135,7 +135,7 @@ def kernel_source_hash(names=("decode.cu", "kvq_internal.cuh")):
 QUANT_SOURCES = ("quant.cu", "kvq_internal.cuh")
 
 
-def ncu_traffic(profile, algorithmic_bytes, sources=("decode.cu", "kvq_internal.cuh")):
+def ncu_traffic(profile, algorithmic_bytes, sources=("decode_kernel.cuh", "kvq_internal.cuh")):
     """DRAM bytes per call: the committed ncu summary's ratio of captured DRAM
     traffic to the captured launch's algorithmic bytes, scaled to this run's
     algorithmic bytes per call; None unless the summary was taken on the

@@ -25,6 +25,7 @@ int check_geometry(const kvq_cache *c) {
   if (c->pre_rope && !(c->rope_theta > 1.f && isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
   if (c->key_per_token != 0 && c->key_per_token != 1) return KVQ_ERR_INVALID_ARG;
   if (c->key_per_token && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
+  if (c->block_table && c->num_blocks < 0) return KVQ_ERR_INVALID_ARG;
   if (c->num_seqs > 65535 || c->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
@@ -38,7 +39,12 @@ int max_groups_of(const kvq_cache *c) {
 int check_buffers(const kvq_cache *c) {
   int e = check_geometry(c);
   if (e) return e;
-  if ((!c->blocks && max_groups_of(c) > 0) || !c->k_res || !c->v_res || !c->seq_len) return KVQ_ERR_INVALID_ARG;
+  const bool need_pool = c->block_table ? c->num_blocks > 0 : max_groups_of(c) > 0;
+  if ((!c->blocks && need_pool) || !c->k_res || !c->v_res || !c->seq_len) return KVQ_ERR_INVALID_ARG;
+  // a paged cache that can hold groups needs at least one pool block (reads
+  // through a bad table entry fall back to block 0)
+  if (c->block_table && max_groups_of(c) > 0 && c->num_blocks < 1) return KVQ_ERR_INVALID_ARG;
+  if (c->block_table && !aligned(c->block_table, 4)) return KVQ_ERR_ALIGNMENT;
   if (c->num_sink && (!c->k_sink || !c->v_sink)) return KVQ_ERR_INVALID_ARG;
   if (!aligned(c->blocks, 128) || !aligned(c->k_res, 16) || !aligned(c->v_res, 16) || !aligned(c->seq_len, 4))
     return KVQ_ERR_ALIGNMENT;
@@ -66,6 +72,8 @@ kvq::Geo make_geo(const kvq_cache *c) {
   g.v_sink = reinterpret_cast<__half *>(c->v_sink);
   g.seq_len = c->seq_len;
   g.status = c->status;
+  g.table = c->block_table;
+  g.num_blocks = c->block_table ? c->num_blocks : 0;
   return g;
 }
 
@@ -92,7 +100,10 @@ int64_t kvq_buffer_bytes(const kvq_cache *c, int32_t which) {
   if (check_geometry(c)) return -1;
   const int64_t sh = static_cast<int64_t>(c->num_seqs) * c->num_kv_heads;
   switch (which) {
-    case KVQ_BUF_BLOCKS: return sh * max_groups_of(c) * kvq::block_bytes(c->bits, c->key_per_token != 0);
+    case KVQ_BUF_BLOCKS:
+      return (c->block_table ? static_cast<int64_t>(c->num_blocks) : sh * max_groups_of(c)) *
+             kvq::block_bytes(c->bits, c->key_per_token != 0);
+    case KVQ_BUF_BLOCK_TABLE: return c->block_table ? sh * max_groups_of(c) * 4 : 0;
     case KVQ_BUF_K_RES:
     case KVQ_BUF_V_RES: return sh * c->residual * kvq::kD * 2;
     case KVQ_BUF_K_SINK:

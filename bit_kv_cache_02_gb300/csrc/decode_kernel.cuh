@@ -1,0 +1,1152 @@
+// Split-K decode attention read directly from the quantized cache.
+//
+// Source: "KV cache quantization", "Keys are harder than values" (the
+// grouped part and the full-precision part of the cache are combined when
+// computing attention scores; keys stored before RoPE are rotated after
+// dequantization); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV
+// Cache", second and third paragraphs (what the groups and the window hold).
+//
+// The work of every (sequence, KV head) pair -- 32-token passes over its
+// fp16 sink + window tokens, then its packed groups -- is laid out as one
+// line of units, and each warp of a single wave of persistent CTAs takes an
+// equal, contiguous range of that line (stream-K): ranges cross pair
+// boundaries, so the split of each pair's token axis follows from the load
+// balance rather than from a fixed chunk size.  A warp streams its groups
+// through a small ring of shared-memory slots filled by one-dimensional bulk
+// copies completing on per-slot mbarriers, fetching across pair boundaries
+// so the next pair's first groups are in flight while the current one ends.
+// It leaves a partial (max, sum, unnormalized output) per query head for
+// each pair it touches; the warp that completes a pair's partial count
+// merges them with a log-sum-exp and writes the fp16 output.  No CTA-wide
+// synchronization happens after start-up.
+
+// Scores over a group use mma.sync m16n8k16 with the 32 tokens as M, the
+// channels as K and the query as N: the A operand comes straight from the
+// packed words (an AND mask leaves each code as an fp16 subnormal
+// code * 2^(b*u - 24)), and the B operand is q_d * scale_d split into an fp16
+// high part and an fp16 low part (columns 2h and 2h+1 for query head h), so
+// the fp32 accumulator sees q * scale to about 22 bits.  The per-channel
+// minimum enters through beta = sum_d q_d * min_d.  The value side is the
+// same with channels as M and tokens as K: o_d = sum_t (p_t scale_t) c_td +
+// sum_t p_t min_t.  B columns of query heads that do not exist (a KV head
+// with fewer than four query heads) carry arbitrary finite values; their
+// accumulator columns are never read.  With keys stored pre-RoPE the scores
+// are instead formed per token on the CUDA cores (dequantize, rotate, dot),
+// because the rotation differs per token.
+#pragma once
+
+#include <math.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int kWarps = 4;              // independent warps per CTA
+constexpr int kRopeOffStride = 65;     // padded row of the in-group rotation table
+constexpr unsigned kFull = 0xffffffffu;
+
+struct PlanHeader;
+
+struct DecodeArgs {
+  Geo geo;
+  int Hq;
+  const __half *q;          // [S][Hq][D]
+  __half *out;              // [S][Hq][D]
+  float zscale;             // softmax scale * log2(e)
+  float *part_o;            // [slots][GQ][D] unnormalized partial outputs
+  float2 *part_ml;          // [slots][GQ] (max, sum) in log2 units
+  int *counters;            // [S][Hkv] partials finished: zero on entry, left zero on exit
+  long long *base;          // [S + 1] first work unit of each sequence (plan kernel), or
+                            // null when the decode kernel plans by itself
+  PlanHeader *plan;         // total work units (plan kernel)
+  int nw;                   // warps sharing the work
+  size_t pass_slot0;        // first partial slot of the window passes
+  int tail_passes;          // window/sink passes per (sequence, KV head) at most, 32 tokens each
+  int max_len;              // host bound on seq_len the plan was sized for
+  const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
+  const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
+};
+
+// Shared memory of one warp: a ring of NS group blocks, one mbarrier per
+// slot, the query of the current pair (fp32, GQ heads), whose space the
+// score operand staging reuses once the query sits in registers, and (keys
+// stored pre-RoPE) the per-group channel-pair coefficients.
+// Ring slots (group blocks in flight) per warp.
+#ifndef KVQ_DECODE_RING_2BIT
+#define KVQ_DECODE_RING_2BIT 4
+#endif
+#ifndef KVQ_DECODE_RING_4BIT
+#define KVQ_DECODE_RING_4BIT 2
+#endif
+
+template <int BITS, int GQ, bool ROPE, bool KPT>
+struct WarpSmem {
+  static constexpr int BB = block_bytes(BITS, KPT);
+  static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2) : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
+  static constexpr int BAR_OFF = NS * BB;
+  static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
+  static constexpr int COEF_OFF = Q_OFF + GQ * kD * 4;            // [GQ][64] float4, then [GQ][64] float2
+  static constexpr int BYTES = (COEF_OFF + (ROPE ? GQ * 64 * 24 : 0) + 127) / 128 * 128;
+  static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
+};
+
+// Post-scale of a key score row tau (0..3 = token 8*tau + g) and of a value
+// output row (channel 16*mt + 8*h + g): undo the code << (b*u) * 2^-24.
+template <int BITS>
+static __device__ __forceinline__ float key_row_scale(int tau) {
+  const int u = BITS == 2 ? tau : (tau & 1);
+  return __int_as_float((127 + 24 - BITS * u) << 23);
+}
+template <int BITS>
+static __device__ __forceinline__ float val_row_scale(int mt, int hh) {
+  const int u = BITS == 2 ? 2 * (mt & 1) + hh : hh;
+  return __int_as_float((127 + 24 - BITS * u) << 23);
+}
+
+// fp16 pair of (x0, x1) when lo_sel == 0, or of the rounding remainder
+// (x - fp16(x)) when lo_sel == 1: the high and low parts of a two-term split.
+static __device__ __forceinline__ uint32_t split_part(float x0, float x1, float lo_sel) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 f = __half22float2(h);
+  return h2_as_u32(__floats2half2_rn(fmaf(-lo_sel, f.x, x0), fmaf(-lo_sel, f.y, x1)));
+}
+
+// Query side of the score mma.  Per group, lane L forms q_d * scale_d for
+// the four channels 16 kt + 8 j + 2 c + {0, 1} (kt = L % 8, c = L / 8,
+// j = 0, 1) of every query head, splits each product into an fp16 high part
+// and the fp16 rounding remainder, and stages both in shared memory in the
+// order of the B fragments: row (2 head + part) * 4 + c holds, for k-tiles
+// 0..7 and j = 0, 1, the channel pair (kt, j, c), 64 bytes per row with the
+// 16-byte chunks XOR-swizzled by (row / 2) % 4 so that neither the 8-byte
+// stores nor the 16-byte fragment loads meet a bank conflict.  Lane (g, q)
+// then loads B column g (query head g / 2, high part for even g, low part for
+// odd g; columns of heads that do not exist repeat the last head) with four
+// 16-byte loads.  beta = sum_d q_d min_d of head q is reduced across the warp.
+// Both use the normalized query q / 2^e (e per head, from frexp of its
+// largest |q_d|), so the products stay inside the fp16 range; qscale undoes
+// it together with the softmax scale.
+template <int GQ>
+struct QkOperand {
+  float qv[GQ][4];  // channels c0, c0 + 1, c0 + 8, c0 + 9 of each head
+  float qscale;     // zscale * 2^e of head (lane & 3)
+
+  static __device__ __forceinline__ int chan0(int lane) { return 16 * (lane & 7) + 2 * (lane >> 3); }
+  static __device__ __forceinline__ int swz(int row, int chunk) { return row * 16 + 4 * (chunk ^ ((row >> 1) & 3)); }
+
+  __device__ __forceinline__ void init(const float *q_s, int lane, float zscale) {
+    const int c0 = chan0(lane);
+    int ex_mine = 0;
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+      const float2 a = *reinterpret_cast<const float2 *>(q_s + h * kD + c0);
+      const float2 b = *reinterpret_cast<const float2 *>(q_s + h * kD + c0 + 8);
+      qv[h][0] = a.x;
+      qv[h][1] = a.y;
+      qv[h][2] = b.x;
+      qv[h][3] = b.y;
+      float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+      int ex;
+      frexpf(amax, &ex);  // |q / 2^ex| < 1
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[h][i] = ldexpf(qv[h][i], -ex);
+      if (h == min(lane & 3, GQ - 1)) ex_mine = ex;
+    }
+    qscale = ldexpf(zscale, ex_mine);
+  }
+
+  // stage: GQ * 512 bytes of this warp's shared memory, 16-byte aligned.
+  __device__ __forceinline__ void build(const float *ks, const float *km, uint32_t *stage, int lane,
+                                        uint32_t (&bq)[8][2], float &beta) const {
+    const int c0 = chan0(lane), kt = lane & 7, c = lane >> 3;
+    const float2 s0 = *reinterpret_cast<const float2 *>(ks + c0);
+    const float2 s1 = *reinterpret_cast<const float2 *>(ks + c0 + 8);
+    const float2 m0 = *reinterpret_cast<const float2 *>(km + c0);
+    const float2 m1 = *reinterpret_cast<const float2 *>(km + c0 + 8);
+    float bp[GQ];
+    __syncwarp();  // earlier reads of the stage (or of the query it aliases) are done
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+      const float x0 = qv[h][0] * s0.x, x1 = qv[h][1] * s0.y, x2 = qv[h][2] * s1.x, x3 = qv[h][3] * s1.y;
+      const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+      const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+      const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y), l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
+      const int rh = (2 * h) * 4 + c, rl = (2 * h + 1) * 4 + c;
+      *reinterpret_cast<uint2 *>(stage + swz(rh, kt >> 1) + 2 * (kt & 1)) = make_uint2(h2_as_u32(h01), h2_as_u32(h23));
+      *reinterpret_cast<uint2 *>(stage + swz(rl, kt >> 1) + 2 * (kt & 1)) = make_uint2(h2_as_u32(l01), h2_as_u32(l23));
+      bp[h] = fmaf(qv[h][0], m0.x, fmaf(qv[h][1], m0.y, fmaf(qv[h][2], m1.x, qv[h][3] * m1.y)));
+    }
+    __syncwarp();
+    {
+      const int g = lane >> 2, q = lane & 3;
+      const int row = (2 * min(g >> 1, GQ - 1) + (g & 1)) * 4 + q;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + swz(row, i));
+        bq[2 * i][0] = w.x;
+        bq[2 * i][1] = w.y;
+        bq[2 * i + 1][0] = w.z;
+        bq[2 * i + 1][1] = w.w;
+      }
+    }
+    // beta of every head summed over the warp: halving exchanges leave one
+    // head's total per lane group, then lane (g, q) fetches head q's
+    if (GQ == 1) {
+      float v = bp[0];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = v * qscale;
+    } else if (GQ == 2) {
+      const bool up = lane & 16;
+      float v = (up ? bp[1] : bp[0]) + __shfl_xor_sync(kFull, up ? bp[0] : bp[1], 16);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = __shfl_sync(kFull, v, 16 * min(lane & 3, 1)) * qscale;  // lanes 0..15: head 0, 16..31: head 1
+    } else {
+      const bool b4 = lane & 16, b3 = lane & 8;
+      const float t0 = __shfl_xor_sync(kFull, b4 ? bp[0] : bp[2 % GQ], 16);
+      const float t1 = __shfl_xor_sync(kFull, b4 ? bp[1] : bp[3 % GQ], 16);
+      const float k0 = (b4 ? bp[2 % GQ] : bp[0]) + t0, k1 = (b4 ? bp[3 % GQ] : bp[1]) + t1;
+      float v = (b3 ? k1 : k0) + __shfl_xor_sync(kFull, b3 ? k0 : k1, 8);
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      beta = __shfl_sync(kFull, v, 8 * (lane & 3)) * qscale;  // lane 8h holds head h = 2 b4 + b3
+    }
+  }
+};
+
+// o[mt] += A(value codes) * bp for one group: o rows are channels 16mt+g and
+// 16mt+8+g, columns 2q / 2q+1 (high / low part of query head q).
+template <int BITS>
+static __device__ __forceinline__ void pv_mma(const uint8_t *vc, int lane, const uint32_t (&bp)[2][2], float (&o)[8][4]) {
+  if (BITS == 2) {
+    const uint4 w0 = *reinterpret_cast<const uint4 *>(vc + (0 * 32 + lane) * 16);
+    const uint4 w1 = *reinterpret_cast<const uint4 *>(vc + (1 * 32 + lane) * 16);
+    const uint32_t vw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int P = 0; P < 4; ++P)
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t wd = vw[2 * P + kt], wd8 = wd >> 8;
+        mma16816(o[2 * P], wd & 0x00030003u, wd & 0x000C000Cu, wd8 & 0x00030003u, wd8 & 0x000C000Cu, bp[kt][0],
+                 bp[kt][1]);
+        mma16816(o[2 * P + 1], wd & 0x00300030u, wd & 0x00C000C0u, wd8 & 0x00300030u, wd8 & 0x00C000C0u,
+                 bp[kt][0], bp[kt][1]);
+      }
+  } else {
+    uint32_t vw[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(vc + (i * 32 + lane) * 16);
+      vw[4 * i] = w.x;
+      vw[4 * i + 1] = w.y;
+      vw[4 * i + 2] = w.z;
+      vw[4 * i + 3] = w.w;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t wd = vw[4 * (mt >> 1) + 2 * kt + (mt & 1)], wd8 = wd >> 8;
+        mma16816(o[mt], wd & 0x000F000Fu, wd & 0x00F000F0u, wd8 & 0x000F000Fu, wd8 & 0x00F000F0u, bp[kt][0],
+                 bp[kt][1]);
+      }
+  }
+}
+
+// Score accumulators of the group's 32 tokens: acc[mt] rows g / g+8 are
+// tokens 16mt + g / 16mt + 8 + g, columns 2q / 2q+1 the parts of head q.
+template <int BITS>
+static __device__ __forceinline__ void qk_mma(const uint8_t *kc, int lane, const uint32_t (&bq)[8][2], float (&acc)[2][4]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  if (BITS == 2) {
+    const uint4 w0 = *reinterpret_cast<const uint4 *>(kc + (0 * 32 + lane) * 16);
+    const uint4 w1 = *reinterpret_cast<const uint4 *>(kc + (1 * 32 + lane) * 16);
+    const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int kt = 0; kt < 8; ++kt) {
+      const uint32_t wd = kw[kt], wd8 = kw[kt] >> 8;
+      mma16816(acc[0], wd & 0x00030003u, wd & 0x000C000Cu, wd8 & 0x00030003u, wd8 & 0x000C000Cu, bq[kt][0],
+               bq[kt][1]);
+      mma16816(acc[1], wd & 0x00300030u, wd & 0x00C000C0u, wd8 & 0x00300030u, wd8 & 0x00C000C0u, bq[kt][0],
+               bq[kt][1]);
+    }
+  } else {
+    uint32_t kw[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(kc + (i * 32 + lane) * 16);
+      kw[4 * i] = w.x;
+      kw[4 * i + 1] = w.y;
+      kw[4 * i + 2] = w.z;
+      kw[4 * i + 3] = w.w;
+    }
+#pragma unroll
+    for (int kt = 0; kt < 8; ++kt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t wd = kw[2 * kt + mt], wd8 = wd >> 8;
+        mma16816(acc[mt], wd & 0x000F000Fu, wd & 0x00F000F0u, wd8 & 0x000F000Fu, wd8 & 0x00F000F0u, bq[kt][0],
+                 bq[kt][1]);
+      }
+  }
+}
+
+// Token t's packed key word for channel tile kt and lane-column qq (used by
+// the pre-RoPE path, one lane per token).
+template <int BITS>
+static __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, int kt, int qq) {
+  constexpr int NU = 8 / BITS;
+  const int tau = t >> 3;
+  const int w = kt * (4 / NU) + tau / NU;
+  const int lane = 4 * (t & 7) + qq;
+  return reinterpret_cast<const uint32_t *>(kc)[((w >> 2) * 32 + lane) * 4 + (w & 3)];
+}
+
+// ------------------------------------------------------------ work schedule
+//
+// The decode work of a (sequence, KV head) pair is a run of units: first
+// kPassUnits units per 32-token pass over its fp16 sink + window tokens, then
+// one unit per packed group.  Pairs are laid out sequence-major: sequence s
+// starts at unit base[s] = Hkv * (units per head of the sequences before
+// it), the line holds W units in all.  Each warp derives base[] and W from
+// seq_len itself (warp scans), or, for large batches, reads them from a plan
+// kernel.  Warp gw of NW takes units [gw W / NW, (gw + 1) W / NW): equal work, contiguous
+// across pair boundaries.  A warp leaves one partial result per pair it
+// touches (slot gw + pair) plus one per window pass it runs; the warp that
+// completes a pair's count merges them.
+#ifndef KVQ_PASS_UNITS
+#define KVQ_PASS_UNITS 4
+#endif
+constexpr int kPassUnits = KVQ_PASS_UNITS;
+constexpr int kInlinePlanSeqs = 256;  // larger batches use the plan kernel
+
+struct PlanHeader {
+  long long total;  // W
+};
+
+// Units of sequence s per KV head (0 when there is nothing to attend).
+static __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Split &spl, int &tp, int &ng) {
+  const int L = a.geo.seq_len[s];
+  tp = ng = 0;
+  spl.nsink = spl.Lq = spl.r = 0;
+  if (L <= 0 || L > a.geo.capacity || L > a.max_len) return 0;
+  spl = split_len(L, a.geo.ns, a.geo.R);
+  ng = spl.Lq / kG;
+  tp = (spl.nsink + spl.r + 31) / 32;
+  return kPassUnits * tp + ng;
+}
+
+// The warp whose unit range holds unit x.
+static __device__ __forceinline__ int owner_warp(long long x, long long W, int NW) {
+  return static_cast<int>(((x + 1) * NW - 1) / W);
+}
+
+// Warps with a non-empty unit range that intersect [P0, P1).
+static __device__ __forceinline__ int touching_warps(long long P0, long long P1, long long W, int NW) {
+  const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
+  if (W >= NW) return w1 - w0 + 1;
+  int n = 0;
+  for (int w = w0; w <= w1; ++w) n += (w * W / NW) < ((w + 1) * W / NW);
+  return n;
+}
+
+// Scores of one packed group for this lane: z[tau] = log2-domain logit of
+// token 8*tau + g for query head q.
+template <int BITS, int GQ>
+static __device__ __forceinline__ void group_scores(const uint8_t *blk, const QkOperand<GQ> &qo, const float (&kfac)[4],
+                                             uint32_t *stage, int lane, float (&z)[4]) {
+  uint32_t bq[8][2];
+  float beta;
+  qo.build(reinterpret_cast<const float *>(blk + off_ks(BITS)), reinterpret_cast<const float *>(blk + off_km(BITS)),
+           stage, lane, bq, beta);
+  float acc[2][4];
+  qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) z[2 * mt + hh] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[2 * mt + hh], beta);
+}
+
+// Scores of one packed group when keys are grouped per token: the B
+// fragments hold the query itself (fp16, exact; column 2h head h, column
+// 2h + 1 zero), built once per (sequence, KV head), and token t's scale s_t
+// and min m_t enter as z = s_t (q . c_t) kf + m_t (zscale sum_d q_d).
+template <int BITS>
+static __device__ __forceinline__ void group_scores_kpt(const uint8_t *blk, const uint32_t (&bq)[8][2],
+                                                 const float (&kfac)[4], float zsq, int lane, float (&z)[4]) {
+  float acc[2][4];
+  qk_mma<BITS>(blk + off_kc(BITS), lane, bq, acc);
+  const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
+  const float *km = reinterpret_cast<const float *>(blk + off_km(BITS, true));
+  const int g = lane >> 2;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tau = 2 * mt + hh, t = 8 * tau + g;
+      z[tau] = fmaf(acc[mt][2 * hh] + acc[mt][2 * hh + 1], kfac[tau] * ks[t], zsq * km[t]);
+    }
+}
+
+// o += values of one group weighted by ps (score layout: token 8*tau + g,
+// head q).  The value mma's B column h carries head h's p_t * scale_t as one
+// fp16 (its rounding error, at most 2^-11 relative per weight, enters the
+// output linearly); o columns 2q and 2q+1 of this lane are heads 2q, 2q+1.
+template <int BITS>
+static __device__ __forceinline__ void group_values(const uint8_t *blk, const float (&ps)[4], int lane, float (&o)[8][4]) {
+  const int q = lane & 3, gcol = lane >> 2;
+  uint32_t bp[2][2];
+#pragma unroll
+  for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + gcol) & 31);
+      const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + gcol) & 31);
+      bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
+    }
+  pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
+}
+
+// Scale the o columns of heads 2q and 2q+1 by their softmax rescale factors.
+static __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_hi) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    o[i][0] *= a_lo;
+    o[i][1] *= a_hi;
+    o[i][2] *= a_lo;
+    o[i][3] *= a_hi;
+  }
+}
+
+// Resident CTAs per SM the register budget is cut for (tensor-core path,
+// query groups of one or two heads).
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 4
+#endif
+#ifndef KVQ_DECODE_MIN_BLOCKS_GQ4
+#define KVQ_DECODE_MIN_BLOCKS_GQ4 3
+#endif
+
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+__global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
+    decode_kernel(DecodeArgs a) {
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
+  constexpr int NS = WS::NS, BB = WS::BB;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  uint8_t *ring = smem + warp * WS::BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + WS::BAR_OFF);
+  float *q_s = reinterpret_cast<float *>(ring + WS::Q_OFF);              // [GQ][D]
+  uint32_t *stage = reinterpret_cast<uint32_t *>(q_s);                   // score operand staging
+  float2 *roff_s = reinterpret_cast<float2 *>(smem + kWarps * WS::BYTES);  // [32][65]
+  const Geo &geo = a.geo;
+
+  if (ROPE) {
+    for (int i = threadIdx.x; i < kG * 64; i += blockDim.x)
+      roff_s[(i >> 6) * kRopeOffStride + (i & 63)] = a.rope_off[i];
+  }
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the only CTA-wide barrier: from here each warp runs alone
+
+  const int NW = a.nw, gw = blockIdx.x * kWarps + warp;
+  if (gw >= NW) return;
+  const bool head_valid = q < GQ;
+  const int H = geo.H, S = geo.S;
+
+  // ---- the work line: total units W, and the sequence s_first holding this
+  // warp's first unit with its first unit sbase.  Small batches plan here,
+  // every warp on its own (one coalesced read of seq_len per 32 sequences);
+  // large ones read the plan kernel's prefix.
+  long long W, ua, ub, sbase = 0;
+  int s_first = 0;
+  if (a.base == nullptr) {
+    for (int s2 = gw; s2 < S; s2 += NW) {  // rows of sequences with nothing to attend
+      const int L = geo.seq_len[s2];
+      if (L > 0 && L <= geo.capacity && L <= a.max_len) continue;
+      if (lane == 0 && L > a.max_len) set_status(geo.status, KVQ_STATUS_MAX_LEN);
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(s2) * a.Hq * kD);
+      for (int i = lane; i < a.Hq * kD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    long long tot = 0;
+    for (int s2 = lane; s2 < S; s2 += 32) {
+      Split spl;
+      int tp, ng;
+      tot += seq_units(a, s2, spl, tp, ng);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFull, tot, off);
+    W = tot * H;
+    ua = gw * W / NW;
+    ub = (gw + 1) * W / NW;
+    if (ua >= ub) return;
+    long long run = 0;  // units of the sequences before chunk c, per KV head
+    for (int c = 0; c < S; c += 32) {
+      Split spl;
+      int tp, ng;
+      const long long v = c + lane < S ? seq_units(a, c + lane, spl, tp, ng) : 0;
+      long long incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long t = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += t;
+      }
+      const unsigned m = __ballot_sync(kFull, c + lane < S && (run + incl) * H > ua);
+      if (m) {
+        const int idx = __ffs(m) - 1;
+        s_first = c + idx;
+        sbase = (run + __shfl_sync(kFull, incl - v, idx)) * H;
+        break;
+      }
+      run += __shfl_sync(kFull, incl, 31);
+    }
+  } else {
+    W = a.plan->total;
+    ua = gw * W / NW;
+    ub = (gw + 1) * W / NW;
+    if (ua >= ub) return;
+    // the last s with base[s] <= ua, by a 32-way search (base[0] = 0 <= ua
+    // keeps the answer in [lo, lo + n))
+    int lo = 0, n = S;
+    while (n > 32) {
+      const int step = (n + 31) / 32;
+      const int idx = lo + lane * step;
+      const unsigned m = __ballot_sync(kFull, idx < lo + n && a.base[idx] <= ua);
+      const int nlo = lo + (31 - __clz(m)) * step;
+      n = min(step, lo + n - nlo);
+      lo = nlo;
+    }
+    const unsigned m = __ballot_sync(kFull, lane < n && a.base[lo + lane] <= ua);
+    s_first = lo + 31 - __clz(m);
+    sbase = a.base[s_first];
+  }
+
+  // ---- fetch cursor: walks the packed groups of [ua, ub) in consumer order
+  // (fbase: first unit of sequence fs; its unit counts are re-derived from
+  // seq_len at each pair change rather than held in registers)
+  uint32_t fseq = 0, cseq = 0;  // ring groups issued / consumed
+  int fs = s_first, fh, fg = 0, fg_end = 0;
+  long long fbase = sbase;
+  bool fdone = false;
+  {
+    Split spl;
+    int tp, ng;
+    fh = static_cast<int>((ua - fbase) / max(seq_units(a, fs, spl, tp, ng), 1));
+  }
+  auto fetch_pair = [&]() {  // the group range of pair (fs, fh); false past ub
+    Split spl;
+    int tp, ng;
+    const int u = seq_units(a, fs, spl, tp, ng);
+    const long long P0 = fbase + static_cast<long long>(fh) * u;
+    const long long gb = P0 + kPassUnits * tp;
+    fg = static_cast<int>(min(max(ua - gb, 0LL), static_cast<long long>(ng)));
+    fg_end = static_cast<int>(min(max(ub - gb, 0LL), static_cast<long long>(ng)));
+    if (PAGED && fg < fg_end) {  // check this range's table entries once
+      const int *te = geo.table + (static_cast<size_t>(fs) * H + fh) * geo.max_groups;
+      bool bad = false;
+      for (int i = fg + lane; i < fg_end; i += 32)
+        bad |= static_cast<unsigned>(te[i]) >= static_cast<unsigned>(geo.num_blocks);
+      if (__any_sync(kFull, bad) && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
+    }
+    return P0 < ub;
+  };
+  auto fetch_next_pair = [&]() {
+    while (!fdone) {
+      if (++fh == H) {
+        Split spl;
+        int tp, ng;
+        fbase += static_cast<long long>(H) * seq_units(a, fs, spl, tp, ng);
+        fh = 0;
+        if (++fs >= S) {
+          fdone = true;
+          break;
+        }
+      }
+      if (!fetch_pair()) {
+        fdone = true;
+        break;
+      }
+      if (fg < fg_end) break;
+    }
+  };
+  if (!fetch_pair()) fdone = true;
+  if (!fdone && fg >= fg_end) fetch_next_pair();
+  auto top_up = [&]() {
+    while (!fdone && fseq - cseq < static_cast<uint32_t>(NS)) {
+      if (lane == 0) {
+        const uint32_t slot = fseq % NS;
+        // paged: an entry outside the pool reads pool block 0 (reported when
+        // the pair's range was entered)
+        size_t blk = (static_cast<size_t>(fs) * H + fh) * geo.max_groups + fg;
+        if constexpr (PAGED) {
+          const unsigned pb = static_cast<unsigned>(geo.table[blk]);
+          blk = pb < static_cast<unsigned>(geo.num_blocks) ? pb : 0u;
+        }
+        const uint8_t *src = geo.blocks + blk * BB;
+        fence_proxy_async();  // generic reads of the slot before the async write
+        mbar_arrive_expect_tx(&full[slot], BB);
+        bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
+      }
+      ++fseq;
+      if (++fg >= fg_end) fetch_next_pair();
+    }
+  };
+  top_up();
+
+  // ---- consumer: pairs in order (cbase: first unit of sequence s)
+  bool ok = true;
+  int s = s_first;
+  long long cbase = sbase;
+  Split spl;
+  int tp, ng;
+  int u = seq_units(a, s, spl, tp, ng);
+  int h = static_cast<int>((ua - cbase) / max(u, 1));
+  while (ok) {
+    if (u == 0) {  // sequence with nothing to attend: skip it
+      if (++s >= S) break;
+      h = 0;
+      u = seq_units(a, s, spl, tp, ng);
+      continue;
+    }
+    const long long P0 = cbase + static_cast<long long>(h) * u, P1 = P0 + u;
+    if (P0 >= ub) break;
+    const long long lo = max(ua, P0), hi = min(ub, P1);
+    const int pair = s * H + h;
+    const size_t orow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * kD;
+    __syncwarp();  // the previous pair's reads of q_s are done
+    for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
+    __syncwarp();
+    int npart = 0;
+
+    // ------------------ window / sink passes whose first unit is ours
+    for (int k = 0; k < tp; ++k) {
+      const long long x = P0 + static_cast<long long>(kPassUnits) * k;
+      if (x < lo || x >= hi) continue;
+      const int T = spl.nsink + spl.r;
+      const int t0 = 32 * k;
+      const int nt = min(32, T - t0);
+      const size_t sh = static_cast<size_t>(pair);
+      const int i = t0 + lane;
+      const bool valid = lane < nt;
+      float dot[GQ];
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
+      if (valid) {
+        int pos;
+        const __half *kp;
+        if (i < spl.nsink) {
+          pos = i;
+          kp = geo.k_sink + (sh * geo.ns + i) * kD;
+        } else {
+          const int slot = i - spl.nsink;
+          pos = spl.nsink + spl.Lq + slot;
+          kp = geo.k_res + (sh * geo.R + slot) * kD;
+        }
+        const int sidx = pos - geo.ns;  // stream index (negative for the sink)
+        // the key row in flight at once (in two halves for four query heads,
+        // whose register budget is tighter); two dot chains per head
+        constexpr int KH = GQ == 4 ? 2 : 1;  // load rounds
+        float dot2[GQ];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) dot2[hh] = 0.f;
+#pragma unroll
+        for (int kh = 0; kh < KH; ++kh) {
+        uint4 kr[16 / KH];
+#pragma unroll
+        for (int c = 0; c < 8 / KH; ++c) {
+          kr[c] = *reinterpret_cast<const uint4 *>(kp + 8 * (c + kh * 8 / KH));
+          kr[c + 8 / KH] = *reinterpret_cast<const uint4 *>(kp + 64 + 8 * (c + kh * 8 / KH));
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8 / KH; ++cc) {
+          const int c = cc + kh * 8 / KH;
+          const __half *ha = reinterpret_cast<const __half *>(&kr[cc]);           // channels 8c ..
+          const __half *hb = reinterpret_cast<const __half *>(&kr[cc + 8 / KH]);  // channels 64 + 8c ..
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int ch = 8 * c + e;
+            float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
+            if (ROPE && sidx >= 0) {
+              const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
+              const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
+              const float cs = bs.x * of.x - bs.y * of.y;
+              const float sn = bs.y * of.x + bs.x * of.y;
+              const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
+              k1 = r1;
+              k2 = r2;
+            }
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              float &d = (e & 1) ? dot2[hh] : dot[hh];
+              d = fmaf(q_s[hh * kD + ch], k1, fmaf(q_s[hh * kD + ch + 64], k2, d));
+            }
+          }
+        }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) dot[hh] += dot2[hh];
+      }
+      float p[GQ], mh[GQ], lh[GQ], acc[GQ][4];
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        const float zz = valid ? dot[hh] * a.zscale : -INFINITY;
+        float mx = zz;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        p[hh] = valid ? fast_exp2(zz - mx) : 0.f;
+        float sum = p[hh];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+        mh[hh] = mx;
+        lh[hh] = sum;
+        acc[hh][0] = acc[hh][1] = acc[hh][2] = acc[hh][3] = 0.f;
+      }
+      // values: lane holds channels 4*lane .. 4*lane+3; VB rows in flight at once
+      constexpr int VB = GQ == 4 ? 8 : 32;
+      for (int tb = 0; tb < nt; tb += VB) {
+        uint2 raw[VB];
+#pragma unroll
+        for (int uu = 0; uu < VB; ++uu) {
+          const int it = t0 + tb + uu;
+          raw[uu] = make_uint2(0u, 0u);
+          if (tb + uu < nt) {
+            const __half *vp = it < spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
+                                              : geo.v_res + (sh * geo.R + (it - spl.nsink)) * kD;
+            raw[uu] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < VB; ++uu) {
+          const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].x));
+          const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&raw[uu].y));
+#pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) {
+            const float pt = __shfl_sync(kFull, p[hh], (tb + uu) & 31);
+            acc[hh][0] = fmaf(pt, v01.x, acc[hh][0]);
+            acc[hh][1] = fmaf(pt, v01.y, acc[hh][1]);
+            acc[hh][2] = fmaf(pt, v23.x, acc[hh][2]);
+            acc[hh][3] = fmaf(pt, v23.y, acc[hh][3]);
+          }
+        }
+      }
+      const size_t slot = a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k;
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) {
+        float *po = a.part_o + (slot * GQ + hh) * kD;
+        *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        if (lane == 0) a.part_ml[slot * GQ + hh] = make_float2(mh[hh], lh[hh]);
+      }
+      ++npart;
+    }
+
+    // ------------------------------------------- packed groups of our range
+    {
+      const long long gb = P0 + static_cast<long long>(kPassUnits) * tp;
+      const int g_lo = static_cast<int>(min(max(lo - gb, 0LL), static_cast<long long>(ng)));
+      const int g_hi = static_cast<int>(min(max(hi - gb, 0LL), static_cast<long long>(ng)));
+      float o[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float m_run = -INFINITY, l_run = 0.f, mu_run = 0.f;
+      if (g_lo < g_hi) {
+        if (!ROPE) {
+          QkOperand<GQ> qo;
+          float kfac[4];
+          uint32_t bqc[8][2];  // keys per token: the query's B fragments, fixed for the pair
+          float zsq = 0.f;     // keys per token: zscale * sum_d q_d of this lane's head
+          if (!KPT) {
+            qo.init(q_s, lane, a.zscale);
+#pragma unroll
+            for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * qo.qscale;
+          } else {
+            const int hd = min(g >> 1, GQ - 1);
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float2 qv = *reinterpret_cast<const float2 *>(q_s + hd * kD + 16 * kt + 8 * j + 2 * q);
+                bqc[kt][j] = (g & 1) ? 0u : h2_as_u32(__floats2half2_rn(qv.x, qv.y));
+              }
+            float qs[GQ];
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              qs[hh] = q_s[hh * kD + lane] + q_s[hh * kD + lane + 32] + q_s[hh * kD + lane + 64] +
+                       q_s[hh * kD + lane + 96];
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) qs[hh] += __shfl_xor_sync(kFull, qs[hh], off);
+              if (hh == min(q, GQ - 1)) zsq = qs[hh] * a.zscale;
+            }
+#pragma unroll
+            for (int tau = 0; tau < 4; ++tau) kfac[tau] = key_row_scale<BITS>(tau) * a.zscale;
+          }
+          // two groups (64 tokens) per iteration: independent score mmas, one
+          // softmax update, two value mmas
+          for (int gi = g_lo; gi < g_hi; gi += 2) {
+            const bool two = gi + 1 < g_hi;
+            const uint32_t sa = cseq % NS, sb = (cseq + 1) % NS;
+            if (!mbar_wait_bounded(&full[sa], (cseq / NS) & 1) ||
+                (two && !mbar_wait_bounded(&full[sb], ((cseq + 1) / NS) & 1))) {
+              ok = false;
+              break;
+            }
+            const uint8_t *ba = ring + sa * BB, *bb = ring + sb * BB;
+            float za[4], zb[4];
+            if (KPT)
+              group_scores_kpt<BITS>(ba, bqc, kfac, zsq, lane, za);
+            else
+              group_scores<BITS, GQ>(ba, qo, kfac, stage, lane, za);
+            if (two) {
+              if (KPT)
+                group_scores_kpt<BITS>(bb, bqc, kfac, zsq, lane, zb);
+              else
+                group_scores<BITS, GQ>(bb, qo, kfac, stage, lane, zb);
+            } else {
+              zb[0] = zb[1] = zb[2] = zb[3] = -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(fmaxf(za[0], za[1]), fmaxf(za[2], za[3])),
+                             fmaxf(fmaxf(zb[0], zb[1]), fmaxf(zb[2], zb[3])));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = fast_exp2(m_run - m_new);
+            const float *vsa = reinterpret_cast<const float *>(ba + off_vs(BITS, KPT));
+            const float *vma = reinterpret_cast<const float *>(ba + off_vm(BITS, KPT));
+            const float *vsb = reinterpret_cast<const float *>(bb + off_vs(BITS, KPT));
+            const float *vmb = reinterpret_cast<const float *>(bb + off_vm(BITS, KPT));
+            float psa[4], psb[4], psum = 0.f, mus = 0.f;
+#pragma unroll
+            for (int tau = 0; tau < 4; ++tau) {
+              const float pa = fast_exp2(za[tau] - m_new);
+              psum += pa;
+              psa[tau] = pa * vsa[8 * tau + g];
+              mus = fmaf(pa, vma[8 * tau + g], mus);
+            }
+            if (two) {
+#pragma unroll
+              for (int tau = 0; tau < 4; ++tau) {
+                const float pb = fast_exp2(zb[tau] - m_new);
+                psum += pb;
+                psb[tau] = pb * vsb[8 * tau + g];
+                mus = fmaf(pb, vmb[8 * tau + g], mus);
+              }
+            }
+            l_run = fmaf(l_run, alpha, psum);
+            mu_run = fmaf(mu_run, alpha, mus);
+            m_run = m_new;
+            if (__any_sync(kFull, head_valid && alpha != 1.f))
+              rescale_o(o, __shfl_sync(kFull, alpha, (2 * q) & 31), __shfl_sync(kFull, alpha, (2 * q + 1) & 31));
+            group_values<BITS>(ba, psa, lane, o);
+            if (two) group_values<BITS>(bb, psb, lane, o);
+            __syncwarp();
+            cseq += two ? 2 : 1;
+            top_up();
+          }
+        } else {
+          // pre-RoPE keys, one lane per token t.  With (C0, S0) the rotation of
+          // the group's first position p0 and (Ct, St) that of the offset t, the
+          // query rotated back to p0 (a = q'_i, b = q'_{i+64}) gives
+          //   q . R(p0 + t) k = sum_i Ct (a k_i + b k_{i+64}) + St (b k_i - a k_{i+64}),
+          // and with k = code * scale + min the per-pair coefficients of
+          //   X = c1 (a s_i) + c2 (b s_{i+64}) + (a m_i + b m_{i+64}),
+          //   Y = c1 (b s_i) - c2 (a s_{i+64}) + (b m_i - a m_{i+64})
+          // are formed once per group (two pairs per lane) for all 32 tokens.
+          float4 *coef = reinterpret_cast<float4 *>(ring + WS::COEF_OFF);            // [GQ][64]
+          float2 *coef0 = reinterpret_cast<float2 *>(ring + WS::COEF_OFF + GQ * 64 * 16);  // [GQ][64]
+          float m_all[GQ];
+#pragma unroll
+          for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
+          for (int gi = g_lo; gi < g_hi; ++gi) {
+            const uint32_t slot = cseq % NS;
+            if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1)) {
+              ok = false;
+              break;
+            }
+            const uint8_t *blk = ring + slot * BB;
+            const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
+            const float *km = reinterpret_cast<const float *>(blk + off_km(BITS));
+            const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
+            const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
+            const uint8_t *kc = blk + off_kc(BITS);
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+              const int i = lane + 32 * r2;
+              const float2 b0 = a.rope_base[static_cast<size_t>(gi) * 64 + i];  // (cos, sin) of p0 theta_i
+              const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
+#pragma unroll
+              for (int hh = 0; hh < GQ; ++hh) {
+                const float qa = q_s[hh * kD + i], qb = q_s[hh * kD + i + 64];
+                const float av = fmaf(qa, b0.x, qb * b0.y), bv = fmaf(qb, b0.x, -qa * b0.y);
+                coef[hh * 64 + i] = make_float4(av * s1, bv * s2, bv * s1, -av * s2);
+                coef0[hh * 64 + i] = make_float2(fmaf(av, m1, bv * m2), fmaf(bv, m1, -av * m2));
+              }
+            }
+            __syncwarp();
+            const int t = lane;
+            const int tau = t >> 3, uu = tau % (8 / BITS);
+            float dot[GQ];
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
+#pragma unroll 1
+            for (int qq = 0; qq < 4; ++qq) {
+              // this token's words of lane 4 (t % 8) + qq: word kt (2-bit) or
+              // 2 kt + tau / 2 (4-bit) holds channels 16 kt + 8 j + 2 qq + e
+              constexpr int WPL = BITS * 4;  // words per lane
+              const uint4 *lw = reinterpret_cast<const uint4 *>(kc) + (4 * (t & 7) + qq);
+              uint32_t wv[WPL];
+#pragma unroll
+              for (int m = 0; m < WPL / 4; ++m) {
+                const uint4 c4 = lw[32 * m];
+                wv[4 * m] = c4.x;
+                wv[4 * m + 1] = c4.y;
+                wv[4 * m + 2] = c4.z;
+                wv[4 * m + 3] = c4.w;
+              }
+#pragma unroll
+              for (int kt = 0; kt < 4; ++kt) {
+                const uint32_t wa = BITS == 2 ? wv[kt] : ((tau >> 1) ? wv[2 * kt + 1] : wv[2 * kt]);
+                const uint32_t wb = BITS == 2 ? wv[kt + 4] : ((tau >> 1) ? wv[2 * (kt + 4) + 1] : wv[2 * (kt + 4)]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    const int i = 16 * kt + 8 * j + 2 * qq + e;
+                    const int sh = 16 * e + 8 * j + BITS * uu;
+                    // code -> fp32 on the FMA pipe: the field under 2^23
+                    const float c1 = __uint_as_float(((wa >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                    const float c2 = __uint_as_float(((wb >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                    const float2 cs = roff_s[t * kRopeOffStride + i];
+#pragma unroll
+                    for (int hh = 0; hh < GQ; ++hh) {
+                      const float4 cf = coef[hh * 64 + i];
+                      const float2 c0 = coef0[hh * 64 + i];
+                      const float X = fmaf(c1, cf.x, fmaf(c2, cf.y, c0.x));
+                      const float Y = fmaf(c1, cf.z, fmaf(c2, cf.w, c0.y));
+                      dot[hh] = fmaf(cs.x, X, fmaf(cs.y, Y, dot[hh]));
+                    }
+                  }
+              }
+            }
+            const float vsc = vs[t], vmn = vm[t];
+            float ps[GQ];
+            float alpha_q = 1.f, psum_q = 0.f, mus_q = 0.f, m_q = m_run, a_lo = 1.f, a_hi = 1.f;
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+              const float zz = dot[hh] * a.zscale;
+              float mx = zz;
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+              const float m_new = fmaxf(m_all[hh], mx);
+              const float alpha = fast_exp2(m_all[hh] - m_new);
+              m_all[hh] = m_new;
+              const float p = fast_exp2(zz - m_new);
+              ps[hh] = p * vsc;
+              float pl = p, pm = p * vmn;
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) {
+                pl += __shfl_xor_sync(kFull, pl, off);
+                pm += __shfl_xor_sync(kFull, pm, off);
+              }
+              if (hh == q) {
+                alpha_q = alpha;
+                psum_q = pl;
+                mus_q = pm;
+                m_q = m_new;
+              }
+              if (hh == 2 * q) a_lo = alpha;
+              if (hh == 2 * q + 1) a_hi = alpha;
+            }
+            l_run = fmaf(l_run, alpha_q, g == 0 ? psum_q : 0.f);
+            mu_run = fmaf(mu_run, alpha_q, g == 0 ? mus_q : 0.f);
+            m_run = m_q;
+            rescale_o(o, a_lo, a_hi);
+            uint32_t bp[2][2];
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                  const float a0 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q);
+                  const float a1 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q + 1);
+                  if (hh == g) {
+                    v0 = a0;
+                    v1 = a1;
+                  }
+                }
+                bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
+              }
+            pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
+            __syncwarp();
+            ++cseq;
+            top_up();
+          }
+        }
+      }
+      if (!ok) break;
+      // this warp's partial of the pair's packed groups (empty if it had none)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l_run += __shfl_xor_sync(kFull, l_run, off);
+        mu_run += __shfl_xor_sync(kFull, mu_run, off);
+      }
+      const size_t slot = static_cast<size_t>(gw) + pair;
+      const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (2 * q + c < GQ) {
+          float *po = a.part_o + (slot * GQ + 2 * q + c) * kD;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+              po[16 * mt + 8 * rr + g] = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
+        }
+      }
+      if (head_valid && g == 0) a.part_ml[slot * GQ + q] = make_float2(m_run, l_run);
+      ++npart;
+    }
+
+    // ---- the warp completing the pair's count merges its partials; lane
+    // 0's acq_rel add publishes this warp's partials (ordered before it by
+    // the warp barrier) and observes every other warp's
+    __syncwarp();
+    const int expect = tp + touching_warps(P0, P1, W, NW);
+    int last = 0;
+    if (lane == 0) last = atom_add_acq_rel(&a.counters[pair], npart) + npart == expect;
+    if (__shfl_sync(kFull, last, 0)) {
+      __threadfence();
+      if (lane == 0) a.counters[pair] = 0;  // ready for the next call
+      const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
+      for (int hh = 0; hh < GQ; ++hh) {
+        float M = -INFINITY;
+        for (int k = lane; k < tp; k += 32)
+          M = fmaxf(M, __ldcg(&a.part_ml[(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k) * GQ + hh]).x);
+        for (int w = w0 + lane; w <= w1; w += 32)
+          if (w * W / NW < (w + 1) * W / NW)
+            M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(w) + pair) * GQ + hh]).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto add = [&](size_t sl) {
+          const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
+          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
+          const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+          Ls = fmaf(ml.y, wgt, Ls);
+          acc.x = fmaf(ov.x, wgt, acc.x);
+          acc.y = fmaf(ov.y, wgt, acc.y);
+          acc.z = fmaf(ov.z, wgt, acc.z);
+          acc.w = fmaf(ov.w, wgt, acc.w);
+        };
+        if (M != -INFINITY) {
+          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k);
+#pragma unroll 4
+          for (int w = w0; w <= w1; ++w)
+            if (w * W / NW < (w + 1) * W / NW) add(static_cast<size_t>(w) + pair);
+        }
+        const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
+        __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
+        op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      }
+    }
+    if (P1 >= ub) break;
+    if (++h == H) {
+      h = 0;
+      cbase += static_cast<long long>(H) * u;
+      if (++s >= S) break;
+      u = seq_units(a, s, spl, tp, ng);
+    }
+  }
+  if (!ok) {
+    set_status(geo.status, KVQ_STATUS_TIMEOUT);
+    // let this warp's copies still in flight land before it exits
+    for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+// Defined in decode.cu: the plan kernel's launch, and the warp count set by
+// kvq_set_decode_warps (0: every resident warp).
+cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t stream);
+int decode_warps_override();
+
+// Defined in decode_paged.cu: the launch of the paged-layout kernels.
+cudaError_t launch_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
+
+// Resident CTAs per SM of one instantiation on the current device, and the
+// device's SM count (cached per device ordinal).
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
+  constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
+  auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED>;
+  static int resident[64] = {};
+  static int sms[64] = {};
+  bytes_out = bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  per_sm = dev < 64 ? resident[dev] : 0;
+  n_sm = dev < 64 ? sms[dev] : 0;
+  if (per_sm == 0) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, bytes)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    per_sm = max(per_sm, 1);
+    if (dev < 64) {
+      resident[dev] = per_sm;
+      sms[dev] = n_sm;
+    }
+  }
+  return cudaSuccess;
+}
+
+// Warps one launch spreads the work over: every resident warp of the device
+// (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
+  int per_sm = 0, n_sm = 0, bytes = 0;
+  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED>(per_sm, n_sm, bytes);
+  if (e != cudaSuccess) return e;
+  const int over = decode_warps_override();
+  int nw = over ? over : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
+  nw = max(nw, 1);
+  a.nw = nw;
+  if (a.base != nullptr) {
+    if ((e = launch_plan(a, stream)) != cudaSuccess) return e;
+  }
+  decode_kernel<BITS, GQ, ROPE, KPT, PAGED><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int BITS, int GQ, bool PAGED>
+static cudaError_t launch_g(const DecodeArgs &a, cudaStream_t stream) {
+  // keys grouped per token are never stored pre-RoPE (rejected at the boundary)
+  if (a.geo.kpt) return launch_t<BITS, GQ, false, true, PAGED>(a, stream);
+  return a.geo.pre_rope ? launch_t<BITS, GQ, true, false, PAGED>(a, stream)
+                        : launch_t<BITS, GQ, false, false, PAGED>(a, stream);
+}
+
+template <int BITS, bool PAGED>
+static cudaError_t launch_b(const DecodeArgs &a, int gq, cudaStream_t stream) {
+  switch (gq) {
+    case 1: return launch_g<BITS, 1, PAGED>(a, stream);
+    case 2: return launch_g<BITS, 2, PAGED>(a, stream);
+    default: return launch_g<BITS, 4, PAGED>(a, stream);
+  }
+}
+
+}  // namespace kvq

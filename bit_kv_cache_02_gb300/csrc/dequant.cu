@@ -35,7 +35,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
   float *vo = v_out + sh * geo.capacity * kD;
   if (gi < geo.max_groups) {
     if (gi >= sp.Lq / kG) return;
-    const uint8_t *blk = geo.blocks + (sh * geo.max_groups + gi) * static_cast<size_t>(block_bytes(BITS, KPT));
+    const uint8_t *blk = group_block(geo, s, h, gi, block_bytes(BITS, KPT));
+    if (!blk) {
+      if (threadIdx.x == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
+      return;
+    }
     const float *ks = reinterpret_cast<const float *>(blk + off_ks(BITS));
     const float *km = reinterpret_cast<const float *>(blk + off_km(BITS, KPT));
     const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS, KPT));

@@ -50,7 +50,19 @@ struct Geo {
   __half *k_res, *v_res, *k_sink, *v_sink;
   int *seq_len;
   int *status;
+  const int *table;  // paged layout: logical group -> pool block (null: contiguous)
+  int num_blocks;    // pool blocks when paged
 };
+
+// Block of logical group g of (s, h) (bb bytes per block), or null when the
+// block table sends it outside the pool.
+__device__ __forceinline__ uint8_t *group_block(const Geo &geo, int s, int h, int g, int bb) {
+  const size_t lg = (static_cast<size_t>(s) * geo.H + h) * geo.max_groups + g;
+  if (!geo.table) return geo.blocks + lg * bb;
+  const int pb = geo.table[lg];
+  if (pb < 0 || pb >= geo.num_blocks) return nullptr;
+  return geo.blocks + static_cast<size_t>(pb) * bb;
+}
 
 // Stream bookkeeping of a sequence holding L tokens.
 struct Split {

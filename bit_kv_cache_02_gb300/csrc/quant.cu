@@ -442,9 +442,11 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   fence_proxy_async();  // this thread's block writes, before the bulk copy reads them
   __syncthreads();
   if (tid == 0) {
-    uint8_t *dst = geo.blocks + ((static_cast<size_t>(s) * geo.H + h) * geo.max_groups + i0 / kG) *
-                                    static_cast<size_t>(block_bytes(BITS, KPT));
-    bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT));
+    uint8_t *dst = group_block(geo, s, h, i0 / kG, block_bytes(BITS, KPT));
+    if (dst)
+      bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT));
+    else
+      set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
   }
 }
 

@@ -22,7 +22,8 @@ KVQ_STATUS_CAPACITY = 1
 KVQ_STATUS_BAD_LEN = 2
 KVQ_STATUS_TIMEOUT = 4
 KVQ_STATUS_MAX_LEN = 8
-BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN = range(6)
+KVQ_STATUS_BAD_BLOCK = 16
+BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN, BUF_BLOCK_TABLE = range(7)
 
 EXPORTED = (
     "kvq_block_bytes", "kvq_max_groups", "kvq_buffer_bytes", "kv_quant_append",
@@ -37,10 +38,10 @@ class CacheStruct(ctypes.Structure):
         ("num_seqs", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
         ("bits", c_int32), ("group", c_int32), ("residual", c_int32),
         ("num_sink", c_int32), ("pre_rope", c_int32), ("rope_theta", c_float),
-        ("capacity", c_int32), ("key_per_token", c_int32),
+        ("capacity", c_int32), ("key_per_token", c_int32), ("num_blocks", c_int32),
         ("blocks", c_void_p), ("k_res", c_void_p), ("v_res", c_void_p),
         ("k_sink", c_void_p), ("v_sink", c_void_p), ("seq_len", c_void_p),
-        ("status", c_void_p),
+        ("status", c_void_p), ("block_table", c_void_p),
     ]
 
 
@@ -106,9 +107,14 @@ class KVCache:
     """
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits=2, residual=128, num_sink=0,
-                 pre_rope=False, rope_theta=10000.0, head_dim=128, device="cuda", key_per_token=False):
+                 pre_rope=False, rope_theta=10000.0, head_dim=128, device="cuda", key_per_token=False,
+                 num_blocks=None):
+        """num_blocks: a paged layout with a pool of that many blocks and a
+        block table [S][Hkv][max_groups] (int32, filled with -1: the caller
+        assigns pool blocks before the appends that need them)."""
         st = CacheStruct(num_seqs, num_kv_heads, head_dim, bits, 32, residual, num_sink,
-                         int(bool(pre_rope)), float(rope_theta), capacity, int(bool(key_per_token)))
+                         int(bool(pre_rope)), float(rope_theta), capacity, int(bool(key_per_token)),
+                         int(num_blocks or 0))
         self.num_seqs, self.num_kv_heads, self.capacity = num_seqs, num_kv_heads, capacity
         self.bits, self.residual, self.num_sink, self.head_dim = bits, residual, num_sink, head_dim
         self.pre_rope, self.rope_theta = bool(pre_rope), rope_theta
@@ -125,8 +131,15 @@ class KVCache:
             return n
 
         S, H, D = num_seqs, num_kv_heads, head_dim
-        self.blocks = torch.zeros(nbytes(BUF_BLOCKS), dtype=torch.uint8, device=device)
-        assert self.blocks.numel() == S * H * self.max_groups * self.block_bytes
+        self.paged = num_blocks is not None
+        self.num_blocks = int(num_blocks) if self.paged else S * H * self.max_groups
+        self.block_table = None
+        if self.paged:
+            tbl = torch.full((S * H * self.max_groups + 1,), -1, dtype=torch.int32, device=device)
+            self.block_table = tbl[:-1].view(S, H, self.max_groups)
+            st.block_table = tbl.data_ptr()
+        self.blocks = torch.zeros(max(nbytes(BUF_BLOCKS), 128), dtype=torch.uint8, device=device)
+        assert nbytes(BUF_BLOCKS) == self.num_blocks * self.block_bytes
         self.k_res = torch.zeros((S, H, residual, D), dtype=torch.float16, device=device)
         self.v_res = torch.zeros_like(self.k_res)
         self.k_sink = torch.zeros((S, H, max(num_sink, 1), D), dtype=torch.float16, device=device)
@@ -144,8 +157,21 @@ class KVCache:
         return ctypes.byref(self.struct)
 
     def blocks_view(self):
-        """blocks as [S][H][max_groups][block_bytes] (a view)."""
-        return self.blocks.view(self.num_seqs, self.num_kv_heads, self.max_groups, self.block_bytes)
+        """blocks as [S][H][max_groups][block_bytes] (a view; contiguous layout)."""
+        assert not self.paged
+        return self.blocks[:self.num_blocks * self.block_bytes].view(
+            self.num_seqs, self.num_kv_heads, self.max_groups, self.block_bytes)
+
+    def logical_blocks(self):
+        """[S][H][max_groups][block_bytes] in logical order (a copy through the
+        block table when paged; entries outside the pool give zeros)."""
+        if not self.paged:
+            return self.blocks_view().clone()
+        pool = self.blocks[:self.num_blocks * self.block_bytes].view(self.num_blocks, self.block_bytes)
+        idx = self.block_table.long()
+        ok = (idx >= 0) & (idx < self.num_blocks)
+        out = pool[idx.clamp(0, max(self.num_blocks - 1, 0))]
+        return out * ok[..., None].to(out.dtype)
 
 
 def kv_quant_append(cache: KVCache, k_new, v_new, new_len, max_new: int, stream=None):

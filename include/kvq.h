@@ -53,6 +53,9 @@ extern "C" {
 #define KVQ_STATUS_BAD_LEN     2  /* new_len < 0 or > max_new: sequence skipped     */
 #define KVQ_STATUS_TIMEOUT     4  /* a bounded pipeline wait gave up                */
 #define KVQ_STATUS_MAX_LEN     8  /* seq_len > max_len at kv_decode_attn: row zeroed */
+#define KVQ_STATUS_BAD_BLOCK  16  /* a block-table entry outside [0, num_blocks):
+                                     its group was not written (append) or pool
+                                     block 0 was read in its place (decode)   */
 
 /* which buffer for kvq_buffer_bytes() */
 #define KVQ_BUF_BLOCKS   0
@@ -61,6 +64,7 @@ extern "C" {
 #define KVQ_BUF_K_SINK   3
 #define KVQ_BUF_V_SINK   4
 #define KVQ_BUF_SEQ_LEN  5
+#define KVQ_BUF_BLOCK_TABLE 6  /* paged layout only */
 
 /*
  * Cache descriptor.  Plain data; every pointer is a caller-owned device
@@ -87,6 +91,15 @@ extern "C" {
  *   seq_len  [S] int32: tokens stored per sequence.  The caller zeroes it
  *            for an empty cache; kv_quant_append advances it.
  *   status   optional device int32 (may be NULL), see KVQ_STATUS_*.
+ *   block_table  optional device int32 [S][Hkv][max_groups] (may be NULL).
+ *            When set the layout is paged: `blocks` is a pool of num_blocks
+ *            blocks and logical group g of (s, h) lives in pool block
+ *            block_table[(s*Hkv + h)*max_groups + g].  The caller assigns
+ *            the entries (a paged serving engine hands out pool blocks as
+ *            sequences grow) before the appends that fill them; only groups
+ *            below seq_len are read.  An entry outside [0, num_blocks) is
+ *            never dereferenced: KVQ_STATUS_BAD_BLOCK is set.  4-byte
+ *            aligned.  NULL: the contiguous layout above.
  *
  * Token p of a sequence is in the sink if p < num_sink.  The remaining
  * n = L - num_sink tokens form the stream: the first Lq = n - (n mod
@@ -108,11 +121,13 @@ typedef struct kvq_cache {
                               1: per token over its D channels (the
                               baseline KIVI compares against; not with
                               pre_rope)                                 */
+  int32_t  num_blocks;     /* pool size when block_table is set         */
   uint8_t  *blocks;
   uint16_t *k_res, *v_res;
   uint16_t *k_sink, *v_sink;
   int32_t  *seq_len;
   int32_t  *status;
+  int32_t  *block_table;   /* NULL: contiguous blocks                    */
 } kvq_cache;
 
 /* Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128 with

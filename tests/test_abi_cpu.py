@@ -59,6 +59,11 @@ def test_sizes(kvq):
     assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st0), kvq.BUF_K_SINK) == 0
     stk = _struct(kvq, key_per_token=1)   # per-token key metadata: 2560-byte blocks
     assert kvq.lib.kvq_buffer_bytes(ctypes.byref(stk), kvq.BUF_BLOCKS) == 2 * 3 * 28 * 2560
+    stp = _struct(kvq, num_blocks=100)    # paged: a pool of 100 blocks plus the table
+    stp.block_table = 1 << 20
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(stp), kvq.BUF_BLOCKS) == 100 * 3328
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(stp), kvq.BUF_BLOCK_TABLE) == 2 * 3 * 28 * 4
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_BLOCK_TABLE) == 0
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -72,6 +77,20 @@ def test_bad_geometry_rejected(kvq, field, value, code):
     assert kvq.lib.kv_decode_workspace_bytes(ctypes.byref(st), 3, 10) == -1
     fake = ctypes.c_void_p(1 << 20)
     assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == code
+
+
+def test_paged_validation(kvq):
+    """A paged cache needs a pool when it can hold groups and an aligned table."""
+    st = _struct(kvq, num_blocks=0)
+    base = 1 << 30
+    st.blocks, st.k_res, st.v_res = base, base + 4096, base + 8192
+    st.k_sink, st.v_sink, st.seq_len = base + 12288, base + 16384, base + 20480
+    st.block_table = base + 24576
+    fake = ctypes.c_void_p(base + (1 << 24))
+    assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -1
+    st.num_blocks = 10
+    st.block_table = base + 24578
+    assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -5
 
 
 def test_key_per_token_with_pre_rope_unsupported(kvq):

@@ -47,7 +47,7 @@ def _compare_state(cache, orc, heads=None):
     assert int(cache.status.item()) == 0
     sl = cache.seq_len.cpu().numpy()
     np.testing.assert_array_equal(sl, orc.seq_len)
-    blocks = cache.blocks_view().cpu().numpy()
+    blocks = cache.logical_blocks().cpu().numpy()
     kres, vres = cache.k_res.cpu().numpy(), cache.v_res.cpu().numpy()
     ksink, vsink = cache.k_sink.cpu().numpy(), cache.v_sink.cpu().numpy()
     for s in range(orc.S):
@@ -70,8 +70,9 @@ def _attn_close(got, want):
     return float(err.max())
 
 
-def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False):
-    cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope, key_per_token=kpt)
+def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False, num_blocks=None):
+    cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope, key_per_token=kpt,
+                        num_blocks=num_blocks)
     orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt)
     return cache, orc
 
@@ -239,6 +240,67 @@ def test_key_per_token_ablation(kvq, bits, gq, ns):
     for s, L in enumerate(lens):
         np.testing.assert_array_max_ulp(K.cpu().numpy()[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
         np.testing.assert_array_max_ulp(V.cpu().numpy()[s, :, :L], Vo[s, :, :L].astype(np.float32), maxulp=1)
+
+
+@pytest.mark.parametrize("bits,gq,ns,kpt", [(2, 1, 0, False), (4, 4, 1, False), (2, 2, 1, True)])
+def test_paged_layout(kvq, bits, gq, ns, kpt):
+    """Block-paged layout: logical groups scattered over a larger pool by a
+    random block table.  Prefill, per-token and chunked appends leave the
+    oracle's bytes in logical order, attention and dequantization match, and
+    pool blocks no group maps to stay untouched."""
+    S, H, T = 3, 2, 600
+    k, v = _rand_kv(S, H, T, seed=90 + bits + gq)
+    cache, orc = _build(kvq, S, H, T + 8, bits, ns=ns, kpt=kpt, num_blocks=S * H * 20 + 37)
+    rng = np.random.default_rng(bits + gq)
+    perm = rng.permutation(cache.num_blocks)[:S * H * cache.max_groups].astype(np.int32)
+    cache.block_table.copy_(torch.from_numpy(perm.reshape(S, H, cache.max_groups)).cuda())
+    pool0 = cache.blocks.clone()
+    lens = np.array([T, T - 77, 260])
+    _append(kvq, cache, orc, k[:, :, :300], v[:, :, :300], np.minimum(lens, 300))
+    pos = 300
+    for step in [1] * 40 + [128, 95, 37]:
+        sl = np.clip(lens - pos, 0, step).astype(np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+    assert pos == T
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=gq)
+    _attn_close(_attend(kvq, cache, q, T), orc.attention(q))
+    K = torch.full((S, H, T + 8, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    for s, L in enumerate(lens):
+        np.testing.assert_array_max_ulp(K.cpu().numpy()[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
+    unused = np.setdiff1d(np.arange(cache.num_blocks), perm)
+    bb = cache.block_bytes
+    pool = cache.blocks[:cache.num_blocks * bb].view(cache.num_blocks, bb).cpu()
+    assert torch.equal(pool[unused], pool0[:cache.num_blocks * bb].view(cache.num_blocks, bb).cpu()[unused])
+
+
+def test_paged_bad_table_entry_sets_status(kvq):
+    """A block-table entry outside the pool is never dereferenced: the group
+    is not written, decode reads pool block 0 in its place, and
+    KVQ_STATUS_BAD_BLOCK is set; groups with valid entries are intact."""
+    S, H, T = 2, 1, 300
+    k, v = _rand_kv(S, H, T, seed=5)
+    cache, orc = _build(kvq, S, H, T + 8, 2, num_blocks=S * H * 8)
+    tbl = np.arange(S * H * cache.max_groups, dtype=np.int32).reshape(S, H, cache.max_groups)
+    tbl[1, 0, 3] = cache.num_blocks + 5     # group 3 of sequence 1: outside the pool
+    tbl[1, 0, 5] = -2                       # and a negative entry
+    cache.block_table.copy_(torch.from_numpy(tbl).cuda())
+    _append(kvq, cache, orc, k, v, [T, T])
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) & kvq.KVQ_STATUS_BAD_BLOCK
+    got = cache.logical_blocks().cpu().numpy()
+    np.testing.assert_array_equal(got[0, 0, :8], orc.blocks[0, 0, :8])
+    np.testing.assert_array_equal(got[1, 0, :3], orc.blocks[1, 0, :3])
+    np.testing.assert_array_equal(got[1, 0, 4], orc.blocks[1, 0, 4])
+    cache.status.zero_()
+    q = _rand_q(S, H, seed=1)
+    out = _attend(kvq, cache, q, T)
+    assert int(cache.status.item()) & kvq.KVQ_STATUS_BAD_BLOCK
+    _attn_close(out[:1], orc.attention(q)[:1])          # sequence 0 is unaffected
 
 
 def test_decode_step_flush_then_attend(kvq):
