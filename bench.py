@@ -261,7 +261,11 @@ def build_caches(kvq, w, layers, pre, capacity, device):
     stream = torch.cuda.current_stream(device)
     for layer in range(layers):
         c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
-                        pre_rope=w.pre_rope, device=device, key_per_token=w.key_per_token)
+                        pre_rope=w.pre_rope, device=device, key_per_token=w.key_per_token,
+                        paged=w.paged)
+        if w.paged:
+            tbl = synth.block_table(w, layer, w.seqs, w.kv_heads, c.max_groups)
+            c.block_table.copy_(torch.from_numpy(tbl).to(device))
         T = int(pre.max())
         k, v = synth.kv_tokens(w, layer, T, device=device)
         k, v = k.contiguous(), v.contiguous()
@@ -510,6 +514,7 @@ def main():
               "kv_heads": w.kv_heads, "head_dim": 128, "ctx": w.ctx, "bits": w.bits, "group": 32,
               "residual": w.residual, "num_sink": w.num_sink, "pre_rope": w.pre_rope,
               "key_per_token": w.key_per_token,
+              "paged": w.paged,
               "ragged": bool(w.ragged_min), "parallelism": f"replicas{world}",
               "l2": "inputs larger than L2: each layer's packed cache is streamed once per step"}
 

@@ -108,10 +108,11 @@ class KVCache:
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits=2, residual=128, num_sink=0,
                  pre_rope=False, rope_theta=10000.0, head_dim=128, device="cuda", key_per_token=False,
-                 num_blocks=None):
-        """num_blocks: a paged layout with a pool of that many blocks and a
-        block table [S][Hkv][max_groups] (int32, filled with -1: the caller
-        assigns pool blocks before the appends that need them)."""
+                 num_blocks=None, paged=False):
+        """num_blocks (or paged=True, for a pool of one block per logical
+        group): a paged layout with a pool of that many blocks and a block
+        table [S][Hkv][max_groups] (int32, filled with -1: the caller assigns
+        pool blocks before the appends that need them)."""
         st = CacheStruct(num_seqs, num_kv_heads, head_dim, bits, 32, residual, num_sink,
                          int(bool(pre_rope)), float(rope_theta), capacity, int(bool(key_per_token)),
                          int(num_blocks or 0))
@@ -123,6 +124,10 @@ class KVCache:
         if self.max_groups < 0:
             raise KvqError(-2, "kvq_max_groups")
         self.block_bytes = block_bytes(bits, head_dim, key_per_token)
+        self.paged = paged or num_blocks is not None
+        if self.paged and num_blocks is None:
+            num_blocks = num_seqs * num_kv_heads * self.max_groups
+        st.num_blocks = int(num_blocks or 0)
 
         def nbytes(which):
             n = lib.kvq_buffer_bytes(ctypes.byref(st), which)
@@ -131,7 +136,6 @@ class KVCache:
             return n
 
         S, H, D = num_seqs, num_kv_heads, head_dim
-        self.paged = num_blocks is not None
         self.num_blocks = int(num_blocks) if self.paged else S * H * self.max_groups
         self.block_table = None
         if self.paged:

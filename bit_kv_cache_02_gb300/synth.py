@@ -37,6 +37,7 @@ class Workload:
     seed: int = 0
     decode_tokens: int = 1   # tokens appended before attending
     key_per_token: bool = False  # keys grouped per token (the ablation of per-channel keys)
+    paged: bool = False      # group blocks in a shared pool behind a shuffled block table
     extra: dict = field(default_factory=dict)
 
 
@@ -51,6 +52,8 @@ WORKLOADS = {
     # the Llama-2 shape with keys grouped per token (ablation row)
     "llama2_7b_mha_key_per_token": Workload("llama2_7b_mha_key_per_token", 32, 16, 32, 32, 4096, 2,
                                             key_per_token=True),
+    # the Llama-2 shape with its group blocks paged through a shuffled table
+    "llama2_7b_mha_paged": Workload("llama2_7b_mha_paged", 32, 16, 32, 32, 4096, 2, paged=True),
 }
 
 
@@ -60,6 +63,14 @@ def context_lengths(w: Workload, layer_seed_offset: int = 0) -> np.ndarray:
         rng = np.random.default_rng([w.seed, 7])
         return rng.integers(w.ragged_min, w.ctx + 1, size=w.seqs).astype(np.int32)
     return np.full(w.seqs, w.ctx, np.int32)
+
+
+def block_table(w: Workload, layer: int, seqs: int, heads: int, max_groups: int) -> np.ndarray:
+    """[seqs][heads][max_groups] int32: a seeded random assignment of the
+    logical group blocks to the blocks of a pool of exactly that many."""
+    rng = np.random.default_rng([w.seed, 13, layer])
+    n = seqs * heads * max_groups
+    return rng.permutation(n).astype(np.int32).reshape(seqs, heads, max_groups)
 
 
 def outlier_channels(w: Workload, layer: int) -> np.ndarray:

@@ -36,7 +36,10 @@ def _run(kvq, name, pairs):
     T = int(lens.max())
     cap = T + 8
     cache = kvq.KVCache(w.seqs, w.kv_heads, cap, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
-                        pre_rope=w.pre_rope, device=dev)
+                        pre_rope=w.pre_rope, device=dev, key_per_token=w.key_per_token, paged=w.paged)
+    if w.paged:
+        tbl = synth.block_table(w, 0, w.seqs, w.kv_heads, cache.max_groups)
+        cache.block_table.copy_(torch.from_numpy(tbl).to(dev))
     k, v = synth.kv_tokens(w, 0, T, device=dev)
     kvq.kv_quant_append(cache, k.contiguous(), v.contiguous(), torch.as_tensor(lens, device=dev), T)
     k1, v1 = synth.kv_tokens(w, 0, 1, device=dev, stream_id=1)
@@ -49,13 +52,14 @@ def _run(kvq, name, pairs):
     torch.cuda.synchronize()
     assert int(cache.status.item()) == 0
     gq = w.q_heads // w.kv_heads
-    blocks = cache.blocks_view()
+    blocks = cache.logical_blocks()
     got = out.cpu().numpy().astype(np.float64)
     qh = q.cpu().numpy()
     worst = 0.0
     for s, h in pairs:
         L = int(lens[s])
-        orc = oracle.OracleCache(1, 1, cap, w.bits, residual=w.residual, num_sink=w.num_sink)
+        orc = oracle.OracleCache(1, 1, cap, w.bits, residual=w.residual, num_sink=w.num_sink,
+                                 key_per_token=w.key_per_token)
         ks = k[s:s + 1, h:h + 1, :L].cpu().numpy()
         vs = v[s:s + 1, h:h + 1, :L].cpu().numpy()
         orc.append(ks, vs, [L])
@@ -102,3 +106,10 @@ def test_kvquant_prerope_sink(kvq):
 def test_long_context_1m(kvq):
     """One sequence x 32 heads, 2^20 context tokens (+1), split-K decode."""
     _run(kvq, "long_1m", [(0, 13)])
+
+
+@pytest.mark.parametrize("name", ["llama2_7b_mha_key_per_token", "llama2_7b_mha_paged"])
+def test_llama2_7b_mha_variants(kvq, name):
+    """The Llama-2 shape with keys grouped per token, and with its group
+    blocks paged through a shuffled block table."""
+    _run(kvq, name, [(0, 0), (15, 31), (9, 12)])
