@@ -24,7 +24,9 @@ Sources, cited by page title and section throughout:
   computing attention scores); section "What they report" (asymmetric 2-bit
   scheme, attention-sink token kept in fp16).
 * "2-Bit KV Cache Quantization: Memory You Save, Recall You Risk"
-  (groundy.com): section "The capacity math" (2 vs 16 bits per element).
+  (groundy.com): section "The capacity math" (2 vs 16 bits per element);
+  section "Method map: three ways to shrink the cache" (Walsh-Hadamard
+  rotation as a design decision of a robust low-bit path).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, invariants, hand-derived golden fixtures or brute force;
@@ -44,6 +46,9 @@ from .kivi import (  # noqa: F401
     quantize_keys_per_token,
     dequantize,
     rope_rotate,
+    hadamard_rotate,
+    hadamard_matrix,
+    hadamard_unrotate,
     OracleCache,
     dense_attention,
 )

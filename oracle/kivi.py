@@ -21,6 +21,10 @@ Method, by source (page title, section):
   quantization", "Keys are harder than values" (RoPE bullet).
 * First token kept in fp16 (attention sink): "KV cache quantization",
   "What they report" (KVQuant paragraph).
+* Optional Walsh-Hadamard rotation of each key and value vector before it is
+  quantized (a training-free rotation named as a design decision of a robust
+  low-bit path): "2-Bit KV Cache Quantization: Memory You Save, Recall You
+  Risk", "Method map: three ways to shrink the cache".
 
 Readings taken where the pages are silent:
 min/max and scale in fp32, scale = (max - min) / (2^b - 1) by one IEEE
@@ -29,7 +33,12 @@ subtraction and one IEEE division, scale == 0 gives code 0; one (scale, min)
 per value token over all head_dim channels; the window flushes the moment it
 holds R tokens; the sink keeps both K and V of token 0; RoPE is rotate-half
 over channel pairs (i, i + D/2) with omega_i = theta^(-2i/D) at absolute
-positions; softmax scale defaults to 1/sqrt(D).
+positions; softmax scale defaults to 1/sqrt(D).  The rotation is the
+Sylvester-ordered Walsh-Hadamard transform scaled by 1/D, evaluated as the
+fast transform in fp32 (strides 1, 2, ..., D/2 in that order) and rounded to
+fp16; it applies to the tokens as they are quantized (the sink and the
+full-precision window keep the tokens as given), and the dequantized group
+rows are rotated back by H (H H = D I).
 """
 
 from __future__ import annotations
@@ -252,6 +261,51 @@ def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM, key_per_token: bool =
 
 
 # --------------------------------------------------------------------------
+# Walsh-Hadamard rotation (applied to tokens as they are quantized)
+# --------------------------------------------------------------------------
+
+def hadamard_rotate(x):
+    """fp16(H x / D) of each D-vector of fp16 `x` (last axis), H the
+    Sylvester Walsh-Hadamard matrix, H[i][j] = (-1)^popcount(i & j).
+
+    Evaluated as the fast transform in fp32: for stride = 1, 2, ..., D/2 in
+    that order, every element pair (i, i + stride) with the stride bit of i
+    clear becomes (a + b, a - b) (one IEEE fp32 add or subtract each); the
+    result is scaled by 1/D (a power of two: exact) and rounded to fp16
+    (half to even).  Since every |entry| of H x / D is at most max |x|, the
+    result never leaves the fp16 range.
+    """
+    y = np.asarray(x, np.float16).astype(np.float32)
+    D = y.shape[-1]
+    assert D & (D - 1) == 0
+    lead = y.shape[:-1]
+    stride = 1
+    while stride < D:
+        t = y.reshape(lead + (D // (2 * stride), 2, stride))
+        a, b = t[..., 0, :], t[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (D,))
+        stride *= 2
+    return (y * np.float32(1.0 / D)).astype(np.float16)
+
+
+def hadamard_matrix(D: int):
+    """H[i][j] = (-1)^popcount(i & j) in fp64, from the definition."""
+    i = np.arange(D)
+    bits = np.bitwise_and(i[:, None], i[None, :])
+    par = np.zeros_like(bits)
+    while bits.any():
+        par ^= bits & 1
+        bits >>= 1
+    return np.where(par == 1, -1.0, 1.0)
+
+
+def hadamard_unrotate(y):
+    """x = H y in fp64 (the inverse of y = H x / D)."""
+    y = np.asarray(y, np.float64)
+    return y @ hadamard_matrix(y.shape[-1]).T
+
+
+# --------------------------------------------------------------------------
 # RoPE (applied to dequantized pre-RoPE keys)
 # --------------------------------------------------------------------------
 
@@ -289,15 +343,18 @@ class OracleCache:
     key_per_token switches keys to the per-token grouping the KIVI page's
     first paragraph describes as the baseline (one scale and min per token
     over its D channels, like values): the ablation of per-channel keys.
+    hadamard rotates every key and value token by hadamard_rotate as its
+    window is quantized; the blocks then hold the rotated tokens' codes.
     """
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits, residual=128,
-                 num_sink=0, head_dim=HEAD_DIM, key_per_token=False):
+                 num_sink=0, head_dim=HEAD_DIM, key_per_token=False, hadamard=False):
         assert bits in (2, 4) and residual % GROUP == 0 and residual > 0
         assert num_sink in (0, 1) and capacity >= 1
         self.S, self.H, self.D = num_seqs, num_kv_heads, head_dim
         self.bits, self.R, self.ns, self.capacity = bits, residual, num_sink, capacity
         self.kpt = bool(key_per_token)
+        self.rot = bool(hadamard)
         stream_cap = max(capacity - num_sink, 0)
         self.max_groups = (stream_cap // residual) * residual // GROUP
         self.bb = block_bytes(bits, head_dim, self.kpt)
@@ -339,6 +396,8 @@ class OracleCache:
         H, D, R = self.H, self.D, self.R
         kg = self.k_res[s].reshape(H, R // GROUP, GROUP, D)
         vg = self.v_res[s].reshape(H, R // GROUP, GROUP, D)
+        if self.rot:
+            kg, vg = hadamard_rotate(kg), hadamard_rotate(vg)
         if self.kpt:
             kc, ks, km = quantize_keys_per_token(kg, self.bits)  # per token
         else:
@@ -358,7 +417,8 @@ class OracleCache:
 
     def keys_values(self, s, h):
         """Dequantized pre-RoPE keys and values of (s, h) in position order,
-        fp64 [L][D] each: sink (exact), groups (code*scale+min), window (exact)."""
+        fp64 [L][D] each: sink (exact), groups (code*scale+min, rotated back
+        by H when the cache rotates), window (exact)."""
         ns, Lq, r = self.split(s)
         ks = [self.k_sink[s, h, :ns].astype(np.float64)]
         vs = [self.v_sink[s, h, :ns].astype(np.float64)]
@@ -370,6 +430,8 @@ class OracleCache:
             else:
                 ks.append(dequantize(kc, ksc[:, None, :], kmn[:, None, :]).reshape(-1, self.D))
             vs.append(dequantize(vc, vsc[:, :, None], vmn[:, :, None]).reshape(-1, self.D))
+            if self.rot:
+                ks[-1], vs[-1] = hadamard_unrotate(ks[-1]), hadamard_unrotate(vs[-1])
         ks.append(self.k_res[s, h, :r].astype(np.float64))
         vs.append(self.v_res[s, h, :r].astype(np.float64))
         return np.concatenate(ks, 0), np.concatenate(vs, 0)

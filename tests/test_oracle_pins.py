@@ -488,3 +488,156 @@ def test_ablation_ordering_on_outlier_keys():
         c.append(k, v, [T])
         errs[name] = float(np.abs(c.attention(q)[0].astype(np.float64) - exact).mean())
     assert errs["channel_R128"] < errs["channel_R32"] < errs["token_R128"], errs
+
+
+# ---------------------------------------------------------------- Hadamard
+
+
+def test_hadamard_matrix_is_sylvester_and_orthogonal():
+    """The matrix from its definition equals scipy's Sylvester construction,
+    is symmetric, and H H = D I."""
+    linalg = pytest.importorskip("scipy.linalg")
+    for D in (2, 8, 128):
+        H = oracle.hadamard_matrix(D)
+        np.testing.assert_array_equal(H, linalg.hadamard(D).astype(np.float64))
+        np.testing.assert_array_equal(H, H.T)
+        np.testing.assert_array_equal(H @ H, D * np.eye(D))
+
+
+def test_hadamard_rotate_exact_on_small_integers():
+    """Integer inputs of magnitude <= 8 keep every fp32 partial sum exact, and
+    H x / 128 is then a multiple of 2^-7 of magnitude <= 8, exact in fp16: the
+    fast transform must equal the matrix product bit for bit.  Basis vector
+    e_j maps to row j of H times 2^-7."""
+    rng = np.random.default_rng(21)
+    x = rng.integers(-8, 9, (64, 128)).astype(np.float16)
+    want = (x.astype(np.float64) @ oracle.hadamard_matrix(128).T / 128).astype(np.float16)
+    np.testing.assert_array_equal(oracle.hadamard_rotate(x).view(np.uint16), want.view(np.uint16))
+    eye = np.eye(128, dtype=np.float16)
+    np.testing.assert_array_equal(oracle.hadamard_rotate(eye).astype(np.float64),
+                                  oracle.hadamard_matrix(128) / 128)
+
+
+def test_hadamard_rotate_within_one_ulp_of_exact():
+    """On fp16 data with outlier channels the fp32 transform then fp16
+    rounding lands within one fp16 ulp of the fp64 product rounded once, and
+    on it for nearly every element."""
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((200, 128)).astype(np.float32)
+    x[:, [3, 17, 64, 101]] *= 20
+    x = x.astype(np.float16)
+    got = oracle.hadamard_rotate(x)
+    exact = x.astype(np.float64) @ oracle.hadamard_matrix(128).T / 128
+    once = exact.astype(np.float16)
+    ulp = np.spacing(np.abs(once).astype(np.float16)).astype(np.float64)
+    assert (np.abs(got.astype(np.float64) - once.astype(np.float64)) <= ulp).all()
+    assert (got == once).mean() > 0.99
+    # the rotation never leaves the input's range
+    assert np.abs(got.astype(np.float64)).max() <= np.abs(x.astype(np.float64)).max()
+
+
+def test_hadamard_unrotate_inverts_rotation():
+    """H (H x / D) = x: unrotating the rotated fp16 vectors gives x back
+    within the fp16 rounding of the rotated entries (each at most half an
+    ulp, summed over D entries of H)."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((50, 128)).astype(np.float16)
+    y = oracle.hadamard_rotate(x)
+    back = oracle.hadamard_unrotate(y)
+    half_ulp = np.spacing(np.abs(y)).astype(np.float64).max(-1, keepdims=True) / 2
+    assert (np.abs(back - x.astype(np.float64)) <= 128 * half_ulp).all()
+
+
+def test_hadamard_cache_streaming_window_and_error_bound():
+    """With the rotation: prefill equals token-by-token appends, the sink and
+    the window hold the tokens as given, and the quantized rows come back
+    within the rotated-domain half-scale bound carried through the
+    orthogonal transform: ||x_hat - x|| <= sqrt(D) (||scale / 2|| + ||fp16
+    rounding of the rotated row||)."""
+    rng = np.random.default_rng(24)
+    S, H, T = 2, 2, 230
+    k = rng.standard_normal((S, H, T, 128)).astype(np.float32)
+    k[..., [5, 77]] *= 15
+    k = k.astype(np.float16)
+    v = rng.standard_normal((S, H, T, 128)).astype(np.float16)
+    for kpt in (False, True):
+        a = oracle.OracleCache(S, H, 256, 2, residual=64, num_sink=1, key_per_token=kpt, hadamard=True)
+        a.append(k, v, [T, T - 5])
+        b = oracle.OracleCache(S, H, 256, 2, residual=64, num_sink=1, key_per_token=kpt, hadamard=True)
+        for t in range(T):
+            b.append(k[:, :, t:t + 1], v[:, :, t:t + 1], [1, int(t < T - 5)])
+        np.testing.assert_array_equal(a.blocks, b.blocks)
+        ns, Lq, r = a.split(1)
+        kh, vh = a.keys_values(1, 0)
+        np.testing.assert_array_equal(kh[:ns], k[1, 0, :ns].astype(np.float64))
+        np.testing.assert_array_equal(kh[ns + Lq:], k[1, 0, ns + Lq:ns + Lq + r].astype(np.float64))
+        np.testing.assert_array_equal(vh[ns + Lq:], v[1, 0, ns + Lq:ns + Lq + r].astype(np.float64))
+        # value rows (per token in the rotated domain)
+        xv = v[1, 0, ns:ns + Lq]
+        yv = oracle.hadamard_rotate(xv)
+        _, sv, _ = oracle.quantize_value_tokens(yv, 2)
+        yexact = xv.astype(np.float64) @ oracle.hadamard_matrix(128).T / 128
+        rnd = np.linalg.norm(yv.astype(np.float64) - yexact, axis=-1)
+        err = np.linalg.norm(vh[ns:ns + Lq] - xv.astype(np.float64), axis=-1)
+        bound = np.sqrt(128) * (np.sqrt(128) * sv.astype(np.float64) / 2 + rnd) * (1 + 1e-6)
+        assert (err <= bound).all()
+        plain = oracle.OracleCache(S, H, 256, 2, residual=64, num_sink=1, key_per_token=kpt)
+        plain.append(k, v, [T, T - 5])
+        assert not np.array_equal(a.blocks, plain.blocks)  # the rotation reached the codes
+
+
+def test_hadamard_attention_in_rotated_domain():
+    """Decode over a rotating cache can score the groups with H q against the
+    rotated dequantized rows and rotate their value sum back by H: the
+    result equals the oracle's attention over the unrotated rows.  A cache
+    short enough to stay in full precision is unaffected by the rotation."""
+    rng = np.random.default_rng(25)
+    T = 200
+    k = rng.standard_normal((1, 1, T, 128)).astype(np.float16)
+    v = rng.standard_normal((1, 1, T, 128)).astype(np.float16)
+    q = rng.standard_normal((1, 3, 128)).astype(np.float16)
+    c = oracle.OracleCache(1, 1, 256, 2, residual=64, hadamard=True)
+    c.append(k, v, [T])
+    ns, Lq, r = c.split(0)
+    kc, ks, km, vc, vs, vm = oracle.kivi.unpack_block(c.blocks[0, 0, :Lq // 32], 2)
+    ky = oracle.dequantize(kc, ks[:, None, :], km[:, None, :]).reshape(-1, 128)
+    vy = oracle.dequantize(vc, vs[:, :, None], vm[:, :, None]).reshape(-1, 128)
+    H = oracle.hadamard_matrix(128)
+    scale = 1 / np.sqrt(128)
+    got = c.attention(q)[0].astype(np.float64)
+    for j in range(3):
+        qj = q[0, j].astype(np.float64)
+        zg = ky @ (H @ qj) * scale
+        zw = k[0, 0, Lq:].astype(np.float64) @ qj * scale
+        m = max(zg.max(), zw.max())
+        pg, pw = np.exp(zg - m), np.exp(zw - m)
+        o = H @ (pg @ vy) + pw @ v[0, 0, Lq:].astype(np.float64)
+        o /= pg.sum() + pw.sum()
+        assert np.abs(got[j] - o).max() <= 1e-3 * np.abs(o).max() + 1e-3
+    short = oracle.OracleCache(1, 1, 256, 2, residual=64, hadamard=True)
+    plain = oracle.OracleCache(1, 1, 256, 2, residual=64)
+    for cc in (short, plain):
+        cc.append(k[:, :, :63], v[:, :, :63], [63])
+    np.testing.assert_array_equal(short.attention(q), plain.attention(q))
+
+
+def test_hadamard_helps_per_token_keys_on_outlier_channels():
+    """The point of the rotation: spreading fixed outlier channels over all
+    channels shrinks per-token key ranges, so per-token key groups after the
+    rotation give a smaller mean attention error than without it."""
+    rng = np.random.default_rng(26)
+    T, Hq = 250, 64
+    k = rng.standard_normal((1, 1, T, 128)).astype(np.float32)
+    k[..., [3, 17, 64, 101]] *= 20
+    k = k.astype(np.float16)
+    v = rng.standard_normal((1, 1, T, 128)).astype(np.float16)
+    q = rng.standard_normal((1, Hq, 128)).astype(np.float16)
+    scale = 1 / np.sqrt(128)
+    exact = np.stack([oracle.dense_attention(q[0, j].astype(np.float64), k[0, 0].astype(np.float64),
+                                             v[0, 0].astype(np.float64), scale) for j in range(Hq)])
+    errs = {}
+    for rot in (False, True):
+        c = oracle.OracleCache(1, 1, 256, 2, residual=32, key_per_token=True, hadamard=rot)
+        c.append(k, v, [T])
+        errs[rot] = float(np.abs(c.attention(q)[0].astype(np.float64) - exact).mean())
+    assert errs[True] < 0.8 * errs[False], errs
