@@ -262,7 +262,7 @@ def build_caches(kvq, w, layers, pre, capacity, device):
     for layer in range(layers):
         c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
                         pre_rope=w.pre_rope, device=device, key_per_token=w.key_per_token,
-                        paged=w.paged)
+                        paged=w.paged, hadamard=w.hadamard)
         if w.paged:
             tbl = synth.block_table(w, layer, w.seqs, w.kv_heads, c.max_groups)
             c.block_table.copy_(torch.from_numpy(tbl).to(device))
@@ -462,7 +462,8 @@ class OracleSample:
         k, v = synth.kv_tokens(ws, 0, self.ctx + extra)
         k, v = k.numpy(), v.numpy()
         c = oracle.OracleCache(n, 1, self.ctx + extra, self.w.bits, residual=self.w.residual,
-                               num_sink=self.w.num_sink, key_per_token=self.w.key_per_token)
+                               num_sink=self.w.num_sink, key_per_token=self.w.key_per_token,
+                               hadamard=self.w.hadamard)
         c.append(k[:, :, :self.ctx], v[:, :, :self.ctx], [self.ctx] * n)
         return ws, k, v, c
 
@@ -515,6 +516,7 @@ def main():
               "residual": w.residual, "num_sink": w.num_sink, "pre_rope": w.pre_rope,
               "key_per_token": w.key_per_token,
               "paged": w.paged,
+              "hadamard": w.hadamard,
               "ragged": bool(w.ragged_min), "parallelism": f"replicas{world}",
               "l2": "inputs larger than L2: each layer's packed cache is streamed once per step"}
 

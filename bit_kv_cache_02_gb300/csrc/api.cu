@@ -25,6 +25,8 @@ int check_geometry(const kvq_cache *c) {
   if (c->pre_rope && !(c->rope_theta > 1.f && isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
   if (c->key_per_token != 0 && c->key_per_token != 1) return KVQ_ERR_INVALID_ARG;
   if (c->key_per_token && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
+  if (c->hadamard != 0 && c->hadamard != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->hadamard && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
   if (c->block_table && c->num_blocks < 0) return KVQ_ERR_INVALID_ARG;
   if (c->num_seqs > 65535 || c->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
@@ -62,6 +64,7 @@ kvq::Geo make_geo(const kvq_cache *c) {
   g.bits = c->bits;
   g.pre_rope = c->pre_rope;
   g.kpt = c->key_per_token;
+  g.rot = c->hadamard;
   g.theta = c->rope_theta;
   g.capacity = c->capacity;
   g.max_groups = max_groups_of(c);

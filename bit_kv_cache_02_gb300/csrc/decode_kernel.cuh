@@ -371,8 +371,9 @@ static __device__ __forceinline__ void group_scores(const uint8_t *blk, const Qk
 }
 
 // Scores of one packed group when keys are grouped per token: the B
-// fragments hold the query itself (fp16, exact; column 2h head h, column
-// 2h + 1 zero), built once per (sequence, KV head), and token t's scale s_t
+// fragments hold the query itself split into fp16 high and low parts
+// (column 2h and 2h + 1 of head h; the low part is zero for an fp16 query,
+// nonzero for a rotated one), built once per (sequence, KV head), and token t's scale s_t
 // and min m_t enter as z = s_t (q . c_t) kf + m_t (zscale sum_d q_d).
 template <int BITS>
 static __device__ __forceinline__ void group_scores_kpt(const uint8_t *blk, const uint32_t (&bq)[8][2],
@@ -395,22 +396,72 @@ static __device__ __forceinline__ void group_scores_kpt(const uint8_t *blk, cons
 // head q).  The value mma's B column h carries head h's p_t * scale_t as one
 // fp16 (its rounding error, at most 2^-11 relative per weight, enters the
 // output linearly); o columns 2q and 2q+1 of this lane are heads 2q, 2q+1.
-template <int BITS>
+// LO (rotating caches, at most four query heads): columns 4 + h carry the
+// fp16 rounding remainder of head h's weights, so the weights enter to
+// about 22 bits.  The Walsh-Hadamard transform that turns the rotated value
+// sums back concentrates every token's code part sum_d code * scale into
+// channel 0 (about D times a typical entry), where a single fp16 weight's
+// 2^-12 relative error would otherwise exceed the output tolerance.
+template <int BITS, bool LO>
 static __device__ __forceinline__ void group_values(const uint8_t *blk, const float (&ps)[4], int lane, float (&o)[8][4]) {
   const int q = lane & 3, gcol = lane >> 2;
+  const int src = LO ? (gcol & 3) : gcol;
   uint32_t bp[2][2];
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + gcol) & 31);
-      const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + gcol) & 31);
-      bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
+      const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + src) & 31);
+      const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + src) & 31);
+      bp[kt][j] = LO ? split_part(v0, v1, gcol >= 4 ? 1.f : 0.f) : h2_as_u32(__floats2half2_rn(v0, v1));
     }
   pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
 }
 
-// Scale the o columns of heads 2q and 2q+1 by their softmax rescale factors.
+// In-place H v of a query head's 128 fp32 channels in shared memory (H the
+// Sylvester Walsh-Hadamard matrix): lane L holds channels L + 32 j; strides
+// 1 .. 16 pair lanes, 32 and 64 pair registers.  Kept out of line: it runs
+// once per (pair, warp) and must not weigh on the kernel's register budget.
+static __device__ __noinline__ void hadamard_q(float *v, int lane) {
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = v[lane + 32 * j];
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float o = __shfl_xor_sync(kFull, x[j], m);
+      x[j] = upper ? o - x[j] : x[j] + o;
+    }
+  }
+  float y0 = x[0] + x[1], y1 = x[0] - x[1], y2 = x[2] + x[3], y3 = x[2] - x[3];
+  x[0] = y0 + y2;
+  x[2] = y0 - y2;
+  x[1] = y1 + y3;
+  x[3] = y1 - y3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[lane + 32 * j] = x[j];
+}
+
+// H v of one head's 128 channels held four per lane (lane L has channels
+// 4 L .. 4 L + 3): strides 1 and 2 pair registers, 4 .. 64 pair lanes
+// L ^ 1 .. L ^ 16.  Out of line, like hadamard_q.
+static __device__ __noinline__ float4 hadamard_lane4(float4 v, int lane) {
+  float y0 = v.x + v.y, y1 = v.x - v.y, y2 = v.z + v.w, y3 = v.z - v.w;
+  v = make_float4(y0 + y2, y1 + y3, y0 - y2, y1 - y3);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+    const float4 o = make_float4(__shfl_xor_sync(kFull, v.x, m), __shfl_xor_sync(kFull, v.y, m),
+                                 __shfl_xor_sync(kFull, v.z, m), __shfl_xor_sync(kFull, v.w, m));
+    v = upper ? make_float4(o.x - v.x, o.y - v.y, o.z - v.z, o.w - v.w)
+              : make_float4(v.x + o.x, v.y + o.y, v.z + o.z, v.w + o.w);
+  }
+  return v;
+}
+
+// Scale the o columns 2q and 2q+1 by their softmax rescale factors.
 static __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, float a_hi) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -430,7 +481,7 @@ static __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, f
 #define KVQ_DECODE_MIN_BLOCKS_GQ4 3
 #endif
 
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
 __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
     decode_kernel(DecodeArgs a) {
   using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
@@ -760,6 +811,11 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
           float kfac[4];
           uint32_t bqc[8][2];  // keys per token: the query's B fragments, fixed for the pair
           float zsq = 0.f;     // keys per token: zscale * sum_d q_d of this lane's head
+          if (ROT) {  // groups hold y = H x / D: score them with H q (q . x = H q . y)
+            __syncwarp();
+            for (int hh = 0; hh < GQ; ++hh) hadamard_q(q_s + hh * kD, lane);
+            __syncwarp();
+          }
           if (!KPT) {
             qo.init(q_s, lane, a.zscale);
 #pragma unroll
@@ -771,7 +827,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const float2 qv = *reinterpret_cast<const float2 *>(q_s + hd * kD + 16 * kt + 8 * j + 2 * q);
-                bqc[kt][j] = (g & 1) ? 0u : h2_as_u32(__floats2half2_rn(qv.x, qv.y));
+                bqc[kt][j] = split_part(qv.x, qv.y, (g & 1) ? 1.f : 0.f);  // (zero low part for fp16 q)
               }
             float qs[GQ];
 #pragma unroll
@@ -842,8 +898,8 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
             m_run = m_new;
             if (__any_sync(kFull, head_valid && alpha != 1.f))
               rescale_o(o, __shfl_sync(kFull, alpha, (2 * q) & 31), __shfl_sync(kFull, alpha, (2 * q + 1) & 31));
-            group_values<BITS>(ba, psa, lane, o);
-            if (two) group_values<BITS>(bb, psb, lane, o);
+            group_values<BITS, ROT>(ba, psa, lane, o);
+            if (two) group_values<BITS, ROT>(bb, psb, lane, o);
             __syncwarp();
             cseq += two ? 2 : 1;
             top_up();
@@ -999,6 +1055,15 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
       }
       const size_t slot = static_cast<size_t>(gw) + pair;
       const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
+      // (a rotating cache leaves this partial in the rotated value domain;
+      // the merge rotates the groups' sum back.  Its weights' low parts
+      // sit in columns 4 .. 7, two lanes up: fold them in.)
+      if (ROT) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_down_sync(kFull, o[mt][i], 2);
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (2 * q + c < GQ) {
@@ -1035,23 +1100,25 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
         float Ls = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        auto add = [&](size_t sl) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accg = acc;  // window passes, groups
+        auto add = [&](size_t sl, float4 &to) {
           const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
           const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
           const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
           Ls = fmaf(ml.y, wgt, Ls);
-          acc.x = fmaf(ov.x, wgt, acc.x);
-          acc.y = fmaf(ov.y, wgt, acc.y);
-          acc.z = fmaf(ov.z, wgt, acc.z);
-          acc.w = fmaf(ov.w, wgt, acc.w);
+          to.x = fmaf(ov.x, wgt, to.x);
+          to.y = fmaf(ov.y, wgt, to.y);
+          to.z = fmaf(ov.z, wgt, to.z);
+          to.w = fmaf(ov.w, wgt, to.w);
         };
         if (M != -INFINITY) {
-          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k);
+          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k, acc);
 #pragma unroll 4
           for (int w = w0; w <= w1; ++w)
-            if (w * W / NW < (w + 1) * W / NW) add(static_cast<size_t>(w) + pair);
+            if (w * W / NW < (w + 1) * W / NW) add(static_cast<size_t>(w) + pair, accg);
         }
+        if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
+        acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);
         const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
         __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
         op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
@@ -1080,16 +1147,20 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
 cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t stream);
 int decode_warps_override();
 
-// Defined in decode_paged.cu: the launch of the paged-layout kernels.
+// Defined in decode_paged.cu, decode_rot.cu and decode_rot_paged.cu: the
+// launches of the paged-layout kernels and of the kernels for caches whose
+// tokens are Walsh-Hadamard rotated (contiguous and paged).
 cudaError_t launch_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
+cudaError_t launch_rot(const DecodeArgs &a, int gq, cudaStream_t stream);
+cudaError_t launch_rot_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
 
 // Resident CTAs per SM of one instantiation on the current device, and the
 // device's SM count (cached per device ordinal).
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
   using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
-  auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED>;
+  auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT>;
   static int resident[64] = {};
   static int sms[64] = {};
   bytes_out = bytes;
@@ -1116,10 +1187,10 @@ static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
 
 // Warps one launch spreads the work over: every resident warp of the device
 // (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
 static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   int per_sm = 0, n_sm = 0, bytes = 0;
-  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED>(per_sm, n_sm, bytes);
+  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED, ROT>(per_sm, n_sm, bytes);
   if (e != cudaSuccess) return e;
   const int over = decode_warps_override();
   int nw = over ? over : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
@@ -1128,24 +1199,27 @@ static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   if (a.base != nullptr) {
     if ((e = launch_plan(a, stream)) != cudaSuccess) return e;
   }
-  decode_kernel<BITS, GQ, ROPE, KPT, PAGED><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
+  decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <int BITS, int GQ, bool PAGED>
+template <int BITS, int GQ, bool PAGED, bool ROT>
 static cudaError_t launch_g(const DecodeArgs &a, cudaStream_t stream) {
-  // keys grouped per token are never stored pre-RoPE (rejected at the boundary)
-  if (a.geo.kpt) return launch_t<BITS, GQ, false, true, PAGED>(a, stream);
-  return a.geo.pre_rope ? launch_t<BITS, GQ, true, false, PAGED>(a, stream)
-                        : launch_t<BITS, GQ, false, false, PAGED>(a, stream);
+  // keys grouped per token, and rotating caches, are never stored pre-RoPE
+  // (rejected at the boundary)
+  if (a.geo.kpt) return launch_t<BITS, GQ, false, true, PAGED, ROT>(a, stream);
+  if constexpr (!ROT) {
+    if (a.geo.pre_rope) return launch_t<BITS, GQ, true, false, PAGED, false>(a, stream);
+  }
+  return launch_t<BITS, GQ, false, false, PAGED, ROT>(a, stream);
 }
 
-template <int BITS, bool PAGED>
+template <int BITS, bool PAGED, bool ROT>
 static cudaError_t launch_b(const DecodeArgs &a, int gq, cudaStream_t stream) {
   switch (gq) {
-    case 1: return launch_g<BITS, 1, PAGED>(a, stream);
-    case 2: return launch_g<BITS, 2, PAGED>(a, stream);
-    default: return launch_g<BITS, 4, PAGED>(a, stream);
+    case 1: return launch_g<BITS, 1, PAGED, ROT>(a, stream);
+    case 2: return launch_g<BITS, 2, PAGED, ROT>(a, stream);
+    default: return launch_g<BITS, 4, PAGED, ROT>(a, stream);
   }
 }
 

@@ -2,7 +2,9 @@
 //
 // Source: asymmetric codes x_hat = code * scale + min ("KV cache
 // quantization", "What they report"); keys per channel / values per token
-// (KIVI page, second paragraph).  Keys are returned pre-RoPE.
+// (KIVI page, second paragraph).  Keys are returned pre-RoPE.  When the
+// cache rotates its tokens (Walsh-Hadamard, include/kvq.h) the group rows
+// are rotated back, x_hat = H y_hat, in fp32.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -45,12 +47,38 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
     const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS, KPT));
     const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS, KPT));
     const int p0 = sp.nsink + gi * kG;
+    __shared__ float rows[2 * kG][kD];  // rotated layout: key rows, then value rows
     for (int idx = threadIdx.x; idx < kG * kD; idx += blockDim.x) {
       const int t = idx / kD, d = idx % kD;
       const uint32_t ck = tile_code<BITS>(blk + off_kc(BITS), t, d, kD);
       const uint32_t cv = tile_code<BITS>(blk + off_vc(BITS), d, t, kG);
-      ko[static_cast<size_t>(p0 + t) * kD + d] = fmaf(static_cast<float>(ck), ks[KPT ? t : d], km[KPT ? t : d]);
-      vo[static_cast<size_t>(p0 + t) * kD + d] = fmaf(static_cast<float>(cv), vs[t], vm[t]);
+      const float kx = fmaf(static_cast<float>(ck), ks[KPT ? t : d], km[KPT ? t : d]);
+      const float vx = fmaf(static_cast<float>(cv), vs[t], vm[t]);
+      if (geo.rot) {
+        rows[t][d] = kx;
+        rows[kG + t][d] = vx;
+      } else {
+        ko[static_cast<size_t>(p0 + t) * kD + d] = kx;
+        vo[static_cast<size_t>(p0 + t) * kD + d] = vx;
+      }
+    }
+    if (geo.rot) {  // x = H y: butterflies (a, b) -> (a + b, a - b) per stride
+      for (int st = 1; st < kD; st <<= 1) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < 2 * kG * (kD / 2); i += blockDim.x) {
+          const int row = i / (kD / 2), b = i % (kD / 2);
+          const int lo = (b / st) * 2 * st + b % st;
+          const float x0 = rows[row][lo], x1 = rows[row][lo + st];
+          rows[row][lo] = x0 + x1;
+          rows[row][lo + st] = x0 - x1;
+        }
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < kG * kD; idx += blockDim.x) {
+        const int t = idx / kD, d = idx % kD;
+        ko[static_cast<size_t>(p0 + t) * kD + d] = rows[t][d];
+        vo[static_cast<size_t>(p0 + t) * kD + d] = rows[kG + t][d];
+      }
     }
   } else {
     const int n = sp.nsink + sp.r;

@@ -43,6 +43,7 @@ __host__ __device__ constexpr int off_vm(int bits, bool kpt = false) { return of
 struct Geo {
   int S, H, R, ns, bits, pre_rope;
   int kpt;  // keys grouped per token
+  int rot;  // tokens Walsh-Hadamard rotated before quantization
   float theta;
   int capacity;
   int max_groups;

@@ -205,14 +205,58 @@ __device__ __forceinline__ uint32_t pack_word(const uint32_t (&x)[NF], const f2x
   return __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x5410);
 }
 
-// Quantize and pack the group held in `r` (tokens from stream index i0 of
+// Walsh-Hadamard rotation of one token row, fp16(H x / 128) (the rotation
+// lever of "2-Bit KV Cache Quantization: Memory You Save, Recall You Risk",
+// "Method map: three ways to shrink the cache"; H the Sylvester matrix).
+// The 16 threads c8 of a token pair hold its 128 channels, thread c8 the
+// channels 8 c8 .. 8 c8 + 7, so strides 1, 2, 4 are butterflies inside a
+// thread and strides 8, 16, 32, 64 pair thread c8 with c8 ^ 1, ^ 2, ^ 4, ^ 8.
+// Strides run in ascending order and each butterfly (a, b) -> (a + b, a - b)
+// is one fp32 add or subtract, so the result is the same fp32 value however
+// the channels are spread; the scale 1/128 is exact and fp16 rounds once.
+__device__ __forceinline__ uint4 hadamard_row(uint4 x, int c8) {
+  float f[8];
+  const __half2 *xh = reinterpret_cast<const __half2 *>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(xh[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+#pragma unroll
+  for (int st = 1; st < 8; st <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (!(i & st)) {
+        const float a = f[i], b = f[i + st];
+        f[i] = __fadd_rn(a, b);
+        f[i + st] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+    const bool upper = (c8 & m) != 0;  // this thread holds the b of each butterfly
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, f[i], m);
+      f[i] = upper ? __fsub_rn(o, f[i]) : __fadd_rn(f[i], o);
+    }
+  }
+  uint4 y;
+  __half2 *yh = reinterpret_cast<__half2 *>(&y);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) yh[i] = __floats2half2_rn(f[2 * i] * 0.0078125f, f[2 * i + 1] * 0.0078125f);
+  return y;
+}
+
+// Quantize and pack the group held in `rin` (tokens from stream index i0 of
 // (s, h)) and write its block with a bulk copy issued by thread 0.  Before
 // the call thread 0 must have waited (bulk_wait_read) for the previous
 // block's copy out of sm.blk.  Three CTA barriers inside, the last one after
 // every read of the tiles.  KPT: keys grouped per token (scale and min over
-// each token's channels, like values) instead of per channel.
-template <int BITS, bool KPT>
-__device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r, const Geo &geo, int s, int h,
+// each token's channels, like values) instead of per channel.  ROT: the
+// rows are Walsh-Hadamard rotated first (every thread of the CTA calls this).
+template <int BITS, bool KPT, bool ROT>
+__device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &rin, const Geo &geo, int s, int h,
                                                int i0) {
   constexpr int NU = 8 / BITS;  // fields per byte
   constexpr int WH = 4 / NU;    // words per (lane, k-tile)
@@ -221,6 +265,14 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   const int p = tid >> 4, c8 = tid & 15;
   float *blkf = reinterpret_cast<float *>(sm.blk);
   uint32_t *blkw = reinterpret_cast<uint32_t *>(sm.blk);
+  GroupRegs r = rin;
+  if (ROT) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      r.k[t] = hadamard_row(r.k[t], c8);
+      r.v[t] = hadamard_row(r.v[t], c8);
+    }
+  }
 
   // ---- tiles, partial key statistics, value token statistics
   {
@@ -459,7 +511,7 @@ constexpr int kLenMask = (1 << kLenBits) - 1;
 // t % gmax of (sequence, KV head) t / gmax (fewer than 2^31 tasks); CTA b
 // takes tasks b, b + grid, ... and loads the next task's rows while it
 // quantizes the current one.
-template <int BITS, bool KPT>
+template <int BITS, bool KPT, bool ROT>
 __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                        const __half *__restrict__ v_new,
                                                                        const int *__restrict__ new_len,
@@ -509,7 +561,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, 
     const bool more = find(nxt);
     if (more) load_group(rn, geo, nxt, k_new, v_new, max_new);
     if (threadIdx.x == 0) bulk_wait_read();  // the previous block's copy has left sm.blk
-    quantize_group<BITS, KPT>(sm, rc, geo, cur.s, cur.h, cur.i0);
+    quantize_group<BITS, KPT, ROT>(sm, rc, geo, cur.s, cur.h, cur.i0);
     if (!more) break;
     cur = nxt;
     rc = rn;
@@ -562,7 +614,7 @@ __device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1,
 // fills, the copy would overwrite window slots the sequence's other CTAs may
 // still be quantizing, so the CTAs arrive after quantizing and the last one
 // copies the new tokens of every head.
-template <int BITS, bool KPT>
+template <int BITS, bool KPT, bool ROT>
 __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                     const __half *__restrict__ v_new,
                                                                     const int *__restrict__ new_len, int max_new) {
@@ -639,7 +691,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, 
         load_group(rn, geo, g, k_new, v_new, max_new);
       }
       if (threadIdx.x == 0) bulk_wait_read();
-      quantize_group<BITS, KPT>(sm, rc, geo, s, h, i0);
+      quantize_group<BITS, KPT, ROT>(sm, rc, geo, s, h, i0);
       rc = rn;
     }
     // quantize_group ends with a barrier: every read of the window is done
@@ -681,51 +733,60 @@ __global__ void __launch_bounds__(256) append_tail_kernel(Geo geo, const __half 
 // most max_new tokens: a window holding R-1 tokens plus max_new new ones.
 int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R / kG); }
 
-// Persistent CTAs of the flush kernel on the current device: every resident
-// slot (cached per device ordinal).
-template <int BITS, bool KPT>
-static cudaError_t flush_grid(int &ctas) {
-  static int cache[64] = {};
+using FlushKernel = void (*)(Geo, const __half *, const __half *, const int *, int, int);
+using StepKernel = void (*)(Geo, const __half *, const __half *, const int *, int);
+
+// Instantiations by (bits, keys per token, rotation).
+static int variant(const Geo &geo) { return (geo.bits == 4 ? 4 : 0) + (geo.kpt ? 2 : 0) + (geo.rot ? 1 : 0); }
+static const FlushKernel kFlushKernels[8] = {
+    quant_flush_kernel<2, false, false>, quant_flush_kernel<2, false, true>, quant_flush_kernel<2, true, false>,
+    quant_flush_kernel<2, true, true>,   quant_flush_kernel<4, false, false>, quant_flush_kernel<4, false, true>,
+    quant_flush_kernel<4, true, false>,  quant_flush_kernel<4, true, true>};
+static const StepKernel kStepKernels[8] = {
+    step_append_kernel<2, false, false>, step_append_kernel<2, false, true>, step_append_kernel<2, true, false>,
+    step_append_kernel<2, true, true>,   step_append_kernel<4, false, false>, step_append_kernel<4, false, true>,
+    step_append_kernel<4, true, false>,  step_append_kernel<4, true, true>};
+
+// Persistent CTAs of flush kernel variant v on the current device: every
+// resident slot (cached per variant and device ordinal).
+static cudaError_t flush_grid(int v, int &ctas) {
+  static int cache[8][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && cache[dev]) {
-    ctas = cache[dev];
+  if (dev < 64 && cache[v][dev]) {
+    ctas = cache[v][dev];
     return cudaSuccess;
   }
   int per_sm = 0, n_sm = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_flush_kernel<BITS, KPT>, kQuantThreads, 0)) !=
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kFlushKernels[v], kQuantThreads, 0)) !=
       cudaSuccess)
     return e;
   if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   ctas = max(per_sm, 1) * n_sm;
-  if (dev < 64) cache[dev] = ctas;
+  if (dev < 64) cache[v][dev] = ctas;
   return cudaSuccess;
 }
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                 int max_new, cudaStream_t stream, uint64_t *launches) {
+  const int v = variant(geo);
   // a decode-sized append (at most one window fills): one kernel
   if (max_new <= geo.R && geo.capacity <= kLenMask && geo.H < (1 << (31 - kLenBits))) {
     dim3 grid(geo.H, geo.S);
-    auto kern = geo.bits == 2 ? (geo.kpt ? step_append_kernel<2, true> : step_append_kernel<2, false>)
-                              : (geo.kpt ? step_append_kernel<4, true> : step_append_kernel<4, false>);
-    kern<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+    kStepKernels[v]<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
     ++*launches;
     return cudaGetLastError();
   }
   const int gmax = max_flush_groups(geo.R, max_new);
   if (gmax > 0) {
     int ctas = 0;
-    cudaError_t e = geo.bits == 2 ? (geo.kpt ? flush_grid<2, true>(ctas) : flush_grid<2, false>(ctas))
-                                  : (geo.kpt ? flush_grid<4, true>(ctas) : flush_grid<4, false>(ctas));
+    cudaError_t e = flush_grid(v, ctas);
     if (e != cudaSuccess) return e;
     const long long ntask = static_cast<long long>(gmax) * geo.H * geo.S;
     if (ntask > 2147483647LL) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(min(static_cast<long long>(ctas), ntask));
-    auto kern = geo.bits == 2 ? (geo.kpt ? quant_flush_kernel<2, true> : quant_flush_kernel<2, false>)
-                              : (geo.kpt ? quant_flush_kernel<4, true> : quant_flush_kernel<4, false>);
-    kern<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
+    kFlushKernels[v]<<<grid, kQuantThreads, 0, stream>>>(geo, k_new, v_new, new_len, max_new, gmax);
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

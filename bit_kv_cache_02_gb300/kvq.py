@@ -38,7 +38,7 @@ class CacheStruct(ctypes.Structure):
         ("num_seqs", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
         ("bits", c_int32), ("group", c_int32), ("residual", c_int32),
         ("num_sink", c_int32), ("pre_rope", c_int32), ("rope_theta", c_float),
-        ("capacity", c_int32), ("key_per_token", c_int32), ("num_blocks", c_int32),
+        ("capacity", c_int32), ("key_per_token", c_int32), ("num_blocks", c_int32), ("hadamard", c_int32),
         ("blocks", c_void_p), ("k_res", c_void_p), ("v_res", c_void_p),
         ("k_sink", c_void_p), ("v_sink", c_void_p), ("seq_len", c_void_p),
         ("status", c_void_p), ("block_table", c_void_p),
@@ -108,18 +108,20 @@ class KVCache:
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits=2, residual=128, num_sink=0,
                  pre_rope=False, rope_theta=10000.0, head_dim=128, device="cuda", key_per_token=False,
-                 num_blocks=None, paged=False):
+                 num_blocks=None, paged=False, hadamard=False):
         """num_blocks (or paged=True, for a pool of one block per logical
         group): a paged layout with a pool of that many blocks and a block
         table [S][Hkv][max_groups] (int32, filled with -1: the caller assigns
-        pool blocks before the appends that need them)."""
+        pool blocks before the appends that need them).  hadamard: tokens are
+        Walsh-Hadamard rotated before quantization (include/kvq.h)."""
         st = CacheStruct(num_seqs, num_kv_heads, head_dim, bits, 32, residual, num_sink,
                          int(bool(pre_rope)), float(rope_theta), capacity, int(bool(key_per_token)),
-                         int(num_blocks or 0))
+                         int(num_blocks or 0), int(bool(hadamard)))
         self.num_seqs, self.num_kv_heads, self.capacity = num_seqs, num_kv_heads, capacity
         self.bits, self.residual, self.num_sink, self.head_dim = bits, residual, num_sink, head_dim
         self.pre_rope, self.rope_theta = bool(pre_rope), rope_theta
         self.key_per_token = bool(key_per_token)
+        self.hadamard = bool(hadamard)
         self.max_groups = lib.kvq_max_groups(ctypes.byref(st))
         if self.max_groups < 0:
             raise KvqError(-2, "kvq_max_groups")

@@ -38,6 +38,7 @@ class Workload:
     decode_tokens: int = 1   # tokens appended before attending
     key_per_token: bool = False  # keys grouped per token (the ablation of per-channel keys)
     paged: bool = False      # group blocks in a shared pool behind a shuffled block table
+    hadamard: bool = False   # tokens Walsh-Hadamard rotated before quantization
     extra: dict = field(default_factory=dict)
 
 
@@ -54,6 +55,10 @@ WORKLOADS = {
                                             key_per_token=True),
     # the Llama-2 shape with its group blocks paged through a shuffled table
     "llama2_7b_mha_paged": Workload("llama2_7b_mha_paged", 32, 16, 32, 32, 4096, 2, paged=True),
+    # the Llama-2 shape with Walsh-Hadamard rotated tokens, per-channel and per-token keys
+    "llama2_7b_mha_hadamard": Workload("llama2_7b_mha_hadamard", 32, 16, 32, 32, 4096, 2, hadamard=True),
+    "llama2_7b_mha_key_per_token_hadamard": Workload("llama2_7b_mha_key_per_token_hadamard", 32, 16, 32, 32,
+                                                     4096, 2, key_per_token=True, hadamard=True),
 }
 
 

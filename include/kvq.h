@@ -105,6 +105,17 @@ extern "C" {
  * n = L - num_sink tokens form the stream: the first Lq = n - (n mod
  * residual) are quantized (Lq/32 blocks), the last n mod residual sit in the
  * window at slots 0.. in order.
+ *
+ * hadamard (the training-free rotation lever of "2-Bit KV Cache
+ * Quantization: Memory You Save, Recall You Risk", "Method map: three ways
+ * to shrink the cache"): a token's D-vector x is quantized as y = fp16(H x
+ * / D), H the Sylvester Walsh-Hadamard matrix (H[i][j] = (-1)^popcount(i &
+ * j)), evaluated as the fast transform in fp32 with strides 1, 2, ..., D/2
+ * in that order (each butterfly (a, b) -> (a + b, a - b)), then scaled by
+ * 1/D and rounded to fp16; |y| <= max |x|.  The blocks hold the codes of y;
+ * the sink and the window keep tokens as given.  Decode scores the groups
+ * with H q and rotates their weighted value sum back by H (H H = D I), so
+ * its output is attention over x_hat = H y_hat; kv_dequant returns x_hat.
  */
 typedef struct kvq_cache {
   int32_t  num_seqs;       /* S, >= 1                                   */
@@ -122,6 +133,9 @@ typedef struct kvq_cache {
                               baseline KIVI compares against; not with
                               pre_rope)                                 */
   int32_t  num_blocks;     /* pool size when block_table is set         */
+  int32_t  hadamard;       /* 1: every key and value token is rotated by
+                              the Walsh-Hadamard transform before it is
+                              quantized (see below; not with pre_rope)  */
   uint8_t  *blocks;
   uint16_t *k_res, *v_res;
   uint16_t *k_sink, *v_sink;

@@ -69,7 +69,7 @@ def test_sizes(kvq):
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 64, -2), ("bits", 3, -2), ("group", 16, -2), ("residual", 100, -2),
     ("residual", 256, -2), ("num_sink", 2, -2), ("num_seqs", 0, -1), ("capacity", 0, -1),
-    ("key_per_token", 2, -1),
+    ("key_per_token", 2, -1), ("hadamard", 2, -1),
 ])
 def test_bad_geometry_rejected(kvq, field, value, code):
     st = _struct(kvq, **{field: value})
@@ -100,6 +100,25 @@ def test_key_per_token_with_pre_rope_unsupported(kvq):
     assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == -1
     fake = ctypes.c_void_p(1 << 20)
     assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -2
+
+
+def test_hadamard_with_pre_rope_unsupported(kvq):
+    """The rotation is not combined with pre-RoPE keys (it does not commute
+    with the per-position RoPE rotation); with per-token keys it is fine."""
+    st = _struct(kvq, hadamard=1, pre_rope=1)
+    assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == -1
+    fake = ctypes.c_void_p(1 << 20)
+    assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -2
+    assert kvq.lib.kvq_max_groups(ctypes.byref(_struct(kvq, hadamard=1, key_per_token=1))) == 28
+
+
+def test_struct_layout_matches_header(kvq):
+    """The ctypes mirror has the header's field order and offsets: 13 int32
+    or float fields, then eight pointers from byte 56."""
+    names = [f[0] for f in kvq.CacheStruct._fields_]
+    assert names[:13] == ["num_seqs", "num_kv_heads", "head_dim", "bits", "group", "residual", "num_sink",
+                          "pre_rope", "rope_theta", "capacity", "key_per_token", "num_blocks", "hadamard"]
+    assert kvq.CacheStruct.blocks.offset == 56 and ctypes.sizeof(kvq.CacheStruct) == 56 + 8 * 8
 
 
 def test_workspace_sizing(kvq):

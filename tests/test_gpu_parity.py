@@ -70,10 +70,10 @@ def _attn_close(got, want):
     return float(err.max())
 
 
-def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False, num_blocks=None):
+def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False, num_blocks=None, rot=False):
     cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope, key_per_token=kpt,
-                        num_blocks=num_blocks)
-    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt)
+                        num_blocks=num_blocks, hadamard=rot)
+    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt, hadamard=rot)
     return cache, orc
 
 
@@ -240,6 +240,49 @@ def test_key_per_token_ablation(kvq, bits, gq, ns):
     for s, L in enumerate(lens):
         np.testing.assert_array_max_ulp(K.cpu().numpy()[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
         np.testing.assert_array_max_ulp(V.cpu().numpy()[s, :, :L], Vo[s, :, :L].astype(np.float32), maxulp=1)
+
+
+@pytest.mark.parametrize("bits,gq,ns,kpt,paged", [(2, 1, 0, False, False), (4, 4, 1, False, False),
+                                                  (2, 2, 1, True, False), (4, 1, 0, True, True),
+                                                  (2, 4, 1, True, False)])
+def test_hadamard_rotation(kvq, bits, gq, ns, kpt, paged):
+    """Walsh-Hadamard rotation before quantization: the fp32 fast transform
+    and fp16 rounding of the quantize kernels leave the oracle's codes,
+    scales and mins byte for byte (prefill, per-token and chunked appends);
+    attention matches; dequantization rotates back within 2^-20 ||x_hat||
+    per row (one fma and seven fp32 butterfly stages, each within 2^-24 sum
+    |y_hat| <= 2^-24 ||x_hat||), and sink and window rows are exact."""
+    S, H, T = 3, 2, 450
+    k, v = _rand_kv(S, H, T, seed=110 + bits + gq + 2 * ns)
+    nb = S * H * 16 + 5 if paged else None
+    cache, orc = _build(kvq, S, H, T + 8, bits, ns=ns, kpt=kpt, num_blocks=nb, rot=True)
+    if paged:
+        rng = np.random.default_rng(bits)
+        perm = rng.permutation(cache.num_blocks)[:S * H * cache.max_groups].astype(np.int32)
+        cache.block_table.copy_(torch.from_numpy(perm.reshape(S, H, cache.max_groups)).cuda())
+    lens = np.array([T, T - 41, 161])
+    _append(kvq, cache, orc, k[:, :, :230], v[:, :, :230], np.minimum(lens, 230))
+    pos = 230
+    for step in [1] * 60 + [128, 32]:
+        sl = np.clip(lens - pos, 0, step).astype(np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+    assert pos == T
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=gq + 7)
+    _attn_close(_attend(kvq, cache, q, T), orc.attention(q))
+    K = torch.full((S, H, T + 8, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    for got, want in ((K.cpu().numpy().astype(np.float64), Ko), (V.cpu().numpy().astype(np.float64), Vo)):
+        for s, L in enumerate(lens):
+            g, w = got[s, :, :L], want[s, :, :L]
+            tol = 2.0 ** -20 * np.linalg.norm(w, axis=-1, keepdims=True)
+            assert (np.abs(g - w) <= tol).all(), f"dequant of sequence {s}: {np.abs(g - w).max():.3e}"
+            ns_s, Lq, r = orc.split(s)
+            np.testing.assert_array_equal(g[:, :ns_s], w[:, :ns_s])
+            np.testing.assert_array_equal(g[:, ns_s + Lq:], w[:, ns_s + Lq:])
 
 
 @pytest.mark.parametrize("bits,gq,ns,kpt", [(2, 1, 0, False), (4, 4, 1, False), (2, 2, 1, True)])
