@@ -22,7 +22,8 @@ Sources, cited by page title and section throughout:
   values" (per-channel keys, per-token values, Pre-RoPE key quantization with
   RoPE applied after dequantization, grouped + residual split combined when
   computing attention scores); section "What they report" (asymmetric 2-bit
-  scheme, attention-sink token kept in fp16).
+  scheme, attention-sink token kept in fp16, per-vector dense-and-sparse
+  outlier isolation).
 * "2-Bit KV Cache Quantization: Memory You Save, Recall You Risk"
   (groundy.com): section "The capacity math" (2 vs 16 bits per element);
   section "Method map: three ways to shrink the cache" (Walsh-Hadamard
@@ -44,6 +45,7 @@ from .kivi import (  # noqa: F401
     quantize_key_group,
     quantize_value_tokens,
     quantize_keys_per_token,
+    quantize_dense_sparse,
     dequantize,
     rope_rotate,
     hadamard_rotate,

@@ -21,6 +21,9 @@ Method, by source (page title, section):
   quantization", "Keys are harder than values" (RoPE bullet).
 * First token kept in fp16 (attention sink): "KV cache quantization",
   "What they report" (KVQuant paragraph).
+* Optional per-vector dense-and-sparse split: each vector's outlier is kept
+  apart so that it does not skew the vector's quantization range ("KV cache
+  quantization", "What they report", KVQuant paragraph).
 * Optional Walsh-Hadamard rotation of each key and value vector before it is
   quantized (a training-free rotation named as a design decision of a robust
   low-bit path): "2-Bit KV Cache Quantization: Memory You Save, Recall You
@@ -38,7 +41,11 @@ Sylvester-ordered Walsh-Hadamard transform scaled by 1/D, evaluated as the
 fast transform in fp32 (strides 1, 2, ..., D/2 in that order) and rounded to
 fp16; it applies to the tokens as they are quantized (the sink and the
 full-precision window keep the tokens as given), and the dequantized group
-rows are rotated back by H (H H = D I).
+rows are rotated back by H (H H = D I).  The dense-and-sparse split takes,
+in every quantization slice (a key channel's 32 tokens, or a token's D
+channels), the one element of largest magnitude (the first in slice order on
+ties) as the outlier: it is kept exactly in fp16 with its index, the slice's
+min and max are taken over the other elements, and the outlier's code is 0.
 """
 
 from __future__ import annotations
@@ -83,6 +90,41 @@ def quantize_asymmetric(x, axis: int, bits: int):
     return (c.astype(np.uint8),
             np.squeeze(scale, axis=axis).astype(np.float32),
             np.squeeze(mn, axis=axis).astype(np.float32))
+
+
+def quantize_dense_sparse(x, axis: int, bits: int):
+    """Dense-and-sparse quantization of fp16 `x`, one slice per position
+    along the other axes: the slice's largest-|x| element (the first in
+    slice order on ties) is the outlier, kept exactly as (index, fp16 value);
+    the other elements are quantized as by `quantize_asymmetric`, with min
+    and max taken over them alone; the outlier's code is 0.
+
+    Returns (codes, scale, min, index uint8, value fp16), the last four with
+    `axis` removed.
+    """
+    x16 = np.asarray(x, dtype=np.float16)
+    x32 = x16.astype(np.float32)
+    idx = np.argmax(np.abs(x32), axis=axis)           # first maximum
+    n = x32.shape[axis]
+    pos = np.expand_dims(idx, axis) == np.arange(n).reshape([-1 if a == axis % x32.ndim else 1
+                                                             for a in range(x32.ndim)])
+    mn = np.where(pos, np.float32(np.inf), x32).min(axis=axis, keepdims=True) + np.float32(0)
+    mx = np.where(pos, np.float32(-np.inf), x32).max(axis=axis, keepdims=True) + np.float32(0)
+    levels = np.float32(2 ** bits - 1)
+    scale = (mx - mn) / levels
+    d = x32 - mn
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = d / scale
+    c = np.rint(y)
+    c = np.where(scale == 0, np.float32(0), c)
+    c = np.clip(c, np.float32(0), levels)
+    c = np.where(pos, np.float32(0), c)
+    val = np.take_along_axis(x16, np.expand_dims(idx, axis), axis=axis)
+    return (c.astype(np.uint8),
+            np.squeeze(scale, axis=axis).astype(np.float32),
+            np.squeeze(mn, axis=axis).astype(np.float32),
+            idx.astype(np.uint8),
+            np.squeeze(val, axis=axis))
 
 
 def quantize_key_group(k_group, bits: int):
@@ -211,17 +253,29 @@ def unpack_tile(buf, bits: int, rows: int, cols: int):
     return (vals & mask).astype(np.uint8).reshape(buf.shape[:-1] + (rows, cols))
 
 
-def block_bytes(bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False) -> int:
+def block_bytes(bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False,
+                outliers: bool = False) -> int:
     """Bytes of one 32-token group block: K codes, V codes (32*D*b/8 each),
     K scale and K min (fp32 per channel; per token when keys are grouped per
-    token), V scale and V min (fp32 per token)."""
+    token), V scale and V min (fp32 per token); with the dense-and-sparse
+    split, one 32-bit outlier entry per key slice and per value token."""
     kmeta = GROUP if key_per_token else head_dim
-    return 2 * (GROUP * head_dim * bits // 8) + 2 * 4 * kmeta + 2 * 4 * GROUP
+    sparse = 4 * (kmeta + GROUP) if outliers else 0
+    return 2 * (GROUP * head_dim * bits // 8) + 2 * 4 * kmeta + 2 * 4 * GROUP + sparse
 
 
-def pack_block(kc, ks, km, vc, vs, vm, bits: int, key_per_token: bool = False):
+def sparse_entries(idx, val):
+    """32-bit outlier entries: the fp16 value's bits in bits 0-15, the index
+    within the slice in bits 16-23."""
+    return (np.asarray(val, np.float16).view(np.uint16).astype(np.uint32)
+            | (np.asarray(idx, np.uint32) << 16))
+
+
+def pack_block(kc, ks, km, vc, vs, vm, bits: int, key_per_token: bool = False, sparse=None):
     """One group block.  kc: [32 tok][D] key codes, ks/km: [D] ([32] when
-    keys are grouped per token); vc: [32 tok][D] value codes, vs/vm: [32]."""
+    keys are grouped per token); vc: [32 tok][D] value codes, vs/vm: [32];
+    sparse: None, or (key outlier index, key outlier value, value outlier
+    index, value outlier value), each per key slice / per value token."""
     D = kc.shape[-1]
     kbytes = GROUP * D * bits // 8
     km_n = GROUP if key_per_token else D
@@ -233,14 +287,21 @@ def pack_block(kc, ks, km, vc, vs, vm, bits: int, key_per_token: bool = False):
         np.asarray(vs, np.float32).view(np.uint8).reshape(vs.shape[:-1] + (4 * GROUP,)),
         np.asarray(vm, np.float32).view(np.uint8).reshape(vm.shape[:-1] + (4 * GROUP,)),
     ]
+    if sparse is not None:
+        ki, kv, vi, vv = sparse
+        parts.append(sparse_entries(ki, kv).view(np.uint8).reshape(ki.shape[:-1] + (4 * km_n,)))
+        parts.append(sparse_entries(vi, vv).view(np.uint8).reshape(vi.shape[:-1] + (4 * GROUP,)))
     out = np.concatenate(parts, axis=-1)
-    assert out.shape[-1] == block_bytes(bits, D, key_per_token) and parts[0].shape[-1] == kbytes
+    assert out.shape[-1] == block_bytes(bits, D, key_per_token, sparse is not None)
+    assert parts[0].shape[-1] == kbytes
     return out
 
 
-def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False):
+def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM, key_per_token: bool = False,
+                 outliers: bool = False):
     """Inverse of `pack_block`: returns (kc [32][D], ks [D], km [D] (both
-    [32] for per-token keys), vc [32][D], vs [32], vm [32])."""
+    [32] for per-token keys), vc [32][D], vs [32], vm [32]), followed with
+    outliers by (key index, key value, value index, value value)."""
     D = head_dim
     buf = np.ascontiguousarray(buf, np.uint8)
     cb = GROUP * D * bits // 8
@@ -257,7 +318,18 @@ def unpack_block(buf, bits: int, head_dim: int = HEAD_DIM, key_per_token: bool =
     km = f32(GROUP if key_per_token else D)
     vs = f32(GROUP)
     vm = f32(GROUP)
-    return kc, ks, km, np.swapaxes(vcT, -1, -2), vs, vm
+    dense = (kc, ks, km, np.swapaxes(vcT, -1, -2), vs, vm)
+    if not outliers:
+        return dense
+
+    def entries(n):
+        nonlocal o
+        e = np.ascontiguousarray(buf[..., o:o + 4 * n]).view(np.uint32)
+        o += 4 * n
+        return (e >> 16).astype(np.uint8), (e & 0xFFFF).astype(np.uint16).view(np.float16)
+    ki, kv = entries(GROUP if key_per_token else D)
+    vi, vv = entries(GROUP)
+    return dense + (ki, kv, vi, vv)
 
 
 # --------------------------------------------------------------------------
@@ -345,19 +417,22 @@ class OracleCache:
     over its D channels, like values): the ablation of per-channel keys.
     hadamard rotates every key and value token by hadamard_rotate as its
     window is quantized; the blocks then hold the rotated tokens' codes.
+    outliers applies the dense-and-sparse split (quantize_dense_sparse) to
+    every key slice and value token.
     """
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits, residual=128,
-                 num_sink=0, head_dim=HEAD_DIM, key_per_token=False, hadamard=False):
+                 num_sink=0, head_dim=HEAD_DIM, key_per_token=False, hadamard=False, outliers=False):
         assert bits in (2, 4) and residual % GROUP == 0 and residual > 0
         assert num_sink in (0, 1) and capacity >= 1
         self.S, self.H, self.D = num_seqs, num_kv_heads, head_dim
         self.bits, self.R, self.ns, self.capacity = bits, residual, num_sink, capacity
         self.kpt = bool(key_per_token)
         self.rot = bool(hadamard)
+        self.sparse = bool(outliers)
         stream_cap = max(capacity - num_sink, 0)
         self.max_groups = (stream_cap // residual) * residual // GROUP
-        self.bb = block_bytes(bits, head_dim, self.kpt)
+        self.bb = block_bytes(bits, head_dim, self.kpt, self.sparse)
         self.blocks = np.zeros((num_seqs, num_kv_heads, self.max_groups, self.bb), np.uint8)
         self.k_res = np.zeros((num_seqs, num_kv_heads, residual, head_dim), np.float16)
         self.v_res = np.zeros_like(self.k_res)
@@ -398,12 +473,17 @@ class OracleCache:
         vg = self.v_res[s].reshape(H, R // GROUP, GROUP, D)
         if self.rot:
             kg, vg = hadamard_rotate(kg), hadamard_rotate(vg)
-        if self.kpt:
-            kc, ks, km = quantize_keys_per_token(kg, self.bits)  # per token
+        if self.sparse:
+            kc, ks, km, ki, kv = quantize_dense_sparse(kg, -1 if self.kpt else -2, self.bits)
+            vc, vs, vm, vi, vv = quantize_dense_sparse(vg, -1, self.bits)
+            blk = pack_block(kc, ks, km, vc, vs, vm, self.bits, self.kpt, sparse=(ki, kv, vi, vv))
         else:
-            kc, ks, km = quantize_key_group(kg, self.bits)       # per channel
-        vc, vs, vm = quantize_value_tokens(vg, self.bits)        # per token
-        blk = pack_block(kc, ks, km, vc, vs, vm, self.bits, self.kpt)
+            if self.kpt:
+                kc, ks, km = quantize_keys_per_token(kg, self.bits)  # per token
+            else:
+                kc, ks, km = quantize_key_group(kg, self.bits)       # per channel
+            vc, vs, vm = quantize_value_tokens(vg, self.bits)        # per token
+            blk = pack_block(kc, ks, km, vc, vs, vm, self.bits, self.kpt)
         self.blocks[s, :, first_group:first_group + R // GROUP] = blk
 
     # -- reading the state back -------------------------------------------
@@ -424,12 +504,24 @@ class OracleCache:
         vs = [self.v_sink[s, h, :ns].astype(np.float64)]
         ng = Lq // GROUP
         if ng:
-            kc, ksc, kmn, vc, vsc, vmn = unpack_block(self.blocks[s, h, :ng], self.bits, self.D, self.kpt)
+            parts = unpack_block(self.blocks[s, h, :ng], self.bits, self.D, self.kpt, self.sparse)
+            kc, ksc, kmn, vc, vsc, vmn = parts[:6]
             if self.kpt:
-                ks.append(dequantize(kc, ksc[:, :, None], kmn[:, :, None]).reshape(-1, self.D))
+                kd = dequantize(kc, ksc[:, :, None], kmn[:, :, None])
             else:
-                ks.append(dequantize(kc, ksc[:, None, :], kmn[:, None, :]).reshape(-1, self.D))
-            vs.append(dequantize(vc, vsc[:, :, None], vmn[:, :, None]).reshape(-1, self.D))
+                kd = dequantize(kc, ksc[:, None, :], kmn[:, None, :])
+            vd = dequantize(vc, vsc[:, :, None], vmn[:, :, None])
+            if self.sparse:  # outliers exactly as stored: [group][token][channel]
+                ki, kv, vi, vv = parts[6:]
+                g = np.arange(ng)[:, None]
+                sl = np.arange(ki.shape[1])[None, :]
+                if self.kpt:
+                    kd[g, sl, ki] = kv
+                else:
+                    kd[g, ki, sl] = kv
+                vd[g, np.arange(GROUP)[None, :], vi] = vv
+            ks.append(kd.reshape(-1, self.D))
+            vs.append(vd.reshape(-1, self.D))
             if self.rot:
                 ks[-1], vs[-1] = hadamard_unrotate(ks[-1]), hadamard_unrotate(vs[-1])
         ks.append(self.k_res[s, h, :r].astype(np.float64))

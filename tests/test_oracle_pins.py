@@ -641,3 +641,173 @@ def test_hadamard_helps_per_token_keys_on_outlier_channels():
         c.append(k, v, [T])
         errs[rot] = float(np.abs(c.attention(q)[0].astype(np.float64) - exact).mean())
     assert errs[True] < 0.8 * errs[False], errs
+
+
+# --------------------------------------------------------- dense-and-sparse
+
+
+def _first_abs_max(vec):
+    """Brute force: the first position of the largest magnitude."""
+    best, arg = -1.0, -1
+    for i, x in enumerate(vec):
+        if abs(float(x)) > best:
+            best, arg = abs(float(x)), i
+    return arg
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("axis", [-1, -2])
+def test_dense_sparse_reduces_to_plain_quantization(bits, axis):
+    """The outlier is the first largest-magnitude element of its slice; the
+    other codes, the scale and the min are those of plain asymmetric
+    quantization of the slice with the outlier replaced by the min of the
+    rest (which leaves the rest's range unchanged); the outlier's code is 0
+    and its value is kept exactly."""
+    rng = np.random.default_rng(31 + bits)
+    x = rng.standard_normal((6, 32, 128)).astype(np.float32)
+    x[rng.random(x.shape) < 0.01] *= 40
+    x = x.astype(np.float16)
+    c, s, m, idx, val = oracle.quantize_dense_sparse(x, axis, bits)
+    xs = np.moveaxis(x, axis, -1)
+    cs = np.moveaxis(c, axis, -1)
+    for b in range(xs.shape[0]):
+        for r in range(xs.shape[1]):
+            vec = xs[b, r]
+            i = _first_abs_max(vec)
+            assert idx[b, r] == i and val[b, r] == vec[i]
+            rest = np.delete(vec, i)
+            rep = vec.copy()
+            rep[i] = rest.min()
+            pc, ps, pm = oracle.quantize_asymmetric(rep[None, :], -1, bits)
+            assert ps[0] == s[b, r] and pm[0] == m[b, r]
+            want = pc[0].copy()
+            want[i] = 0
+            np.testing.assert_array_equal(cs[b, r], want)
+
+
+def test_dense_sparse_error_bound_and_spike_isolation():
+    """Every non-outlier element comes back within half a scale of the
+    rest's range, the outlier exactly; a single spike per vector no longer
+    inflates the error of the others (plain quantization's error grows with
+    the spike, the split's does not)."""
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((200, 128)).astype(np.float32)
+    spike = rng.integers(0, 128, 200)
+    x[np.arange(200), spike] = 60 * np.sign(rng.standard_normal(200))
+    x = x.astype(np.float16)
+    c, s, m, idx, val = oracle.quantize_dense_sparse(x, -1, 2)
+    np.testing.assert_array_equal(idx, spike)
+    xh = oracle.dequantize(c, s[:, None], m[:, None])
+    xh[np.arange(200), idx] = val
+    err = np.abs(xh - x.astype(np.float64))
+    assert err[np.arange(200), idx].max() == 0
+    assert (err <= s[:, None].astype(np.float64) / 2 * (1 + 1e-6) + 1e-7).all()
+    pc, ps, pm = oracle.quantize_asymmetric(x, -1, 2)
+    plain = np.abs(oracle.dequantize(pc, ps[:, None], pm[:, None]) - x.astype(np.float64))
+    others = np.ones_like(err, bool)
+    others[np.arange(200), idx] = False
+    assert err[others].mean() < 0.25 * plain[others].mean()
+
+
+def test_dense_sparse_ties_and_degenerate_slices():
+    """Ties go to the first position (+a before -a and the reverse); a
+    constant slice keeps its first element as the outlier and the rest has
+    scale 0; a zero slice gives index 0, value 0, scale 0."""
+    x = np.zeros((4, 8), np.float16)
+    x[0] = [1, -3, 2, 3, 0, 0, 0, 0]
+    x[1] = [1, 3, 2, -3, 0, 0, 0, 0]
+    x[2] = 5
+    c, s, m, idx, val = oracle.quantize_dense_sparse(x, -1, 2)
+    assert list(idx) == [1, 1, 0, 0]
+    assert list(val.astype(np.float64)) == [-3, 3, 5, 0]
+    assert s[2] == 0 and m[2] == 5 and (c[2] == 0).all()
+    assert s[3] == 0 and m[3] == 0 and not np.signbit(m[3])
+    # row 0 without its outlier: rest in [0, 3] -> scale 1, min 0
+    assert s[0] == 1 and m[0] == 0 and list(c[0]) == [1, 0, 2, 3, 0, 0, 0, 0]
+
+
+def test_dense_sparse_block_layout_roundtrip():
+    """One 32-bit entry (fp16 bits, then the index at bit 16) per key slice
+    and per value token after the metadata: 3968 / 6016 B per block with
+    per-channel keys, 2816 / 4864 B with per-token keys; packing
+    round-trips."""
+    assert oracle.block_bytes(2, outliers=True) == 3328 + 4 * (128 + 32)
+    assert oracle.block_bytes(4, outliers=True) == 5376 + 4 * (128 + 32)
+    assert oracle.block_bytes(2, key_per_token=True, outliers=True) == 2560 + 4 * 64
+    assert oracle.block_bytes(4, key_per_token=True, outliers=True) == 4608 + 4 * 64
+    e = oracle.kivi.sparse_entries(np.array([5, 31], np.uint8), np.array([-2.5, 1.0], np.float16))
+    assert list(e) == [0xC100 | (5 << 16), 0x3C00 | (31 << 16)]  # -2.5 = 0xC100, 1.0 = 0x3C00
+    rng = np.random.default_rng(34)
+    for bits, kpt in ((2, False), (4, True)):
+        n = 32 if kpt else 128
+        kc = rng.integers(0, 1 << bits, (3, 32, 128)).astype(np.uint8)
+        vc = rng.integers(0, 1 << bits, (3, 32, 128)).astype(np.uint8)
+        ks, km = (rng.standard_normal((3, n)).astype(np.float32) for _ in range(2))
+        vs, vm = (rng.standard_normal((3, 32)).astype(np.float32) for _ in range(2))
+        ki = rng.integers(0, 32 if not kpt else 128, (3, n)).astype(np.uint8)
+        kv = rng.standard_normal((3, n)).astype(np.float16)
+        vi = rng.integers(0, 128, (3, 32)).astype(np.uint8)
+        vv = rng.standard_normal((3, 32)).astype(np.float16)
+        blk = oracle.kivi.pack_block(kc, ks, km, vc, vs, vm, bits, kpt, sparse=(ki, kv, vi, vv))
+        out = oracle.kivi.unpack_block(blk, bits, key_per_token=kpt, outliers=True)
+        for a, b in zip(out, (kc, ks, km, vc, vs, vm, ki, kv, vi, vv)):
+            np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("kpt", [False, True])
+def test_dense_sparse_cache_streaming_and_reconstruction(kpt):
+    """With the split: prefill equals token-by-token appends; every
+    dequantized slice holds its outlier exactly and the rest within half of
+    the rest's scale; sink and window exact."""
+    rng = np.random.default_rng(35)
+    S, H, T = 2, 2, 230
+    k = rng.standard_normal((S, H, T, 128)).astype(np.float32)
+    k[rng.random(k.shape) < 0.005] *= 50
+    k = k.astype(np.float16)
+    v = rng.standard_normal((S, H, T, 128)).astype(np.float16)
+    a = oracle.OracleCache(S, H, 256, 2, residual=64, num_sink=1, key_per_token=kpt, outliers=True)
+    a.append(k, v, [T, T - 11])
+    b = oracle.OracleCache(S, H, 256, 2, residual=64, num_sink=1, key_per_token=kpt, outliers=True)
+    for t in range(T):
+        b.append(k[:, :, t:t + 1], v[:, :, t:t + 1], [1, int(t < T - 11)])
+    np.testing.assert_array_equal(a.blocks, b.blocks)
+    ns, Lq, r = a.split(0)
+    kh, vh = a.keys_values(0, 1)
+    np.testing.assert_array_equal(kh[:ns], k[0, 1, :ns].astype(np.float64))
+    np.testing.assert_array_equal(kh[ns + Lq:], k[0, 1, ns + Lq:ns + Lq + r].astype(np.float64))
+    for got, src, axis, is_key in ((kh, k, -1 if kpt else -2, True), (vh, v, -1, False)):
+        x = src[0, 1, ns:ns + Lq].reshape(-1, 32, 128)
+        _, s, m, idx, val = oracle.quantize_dense_sparse(x, axis, 2)
+        g = got[ns:ns + Lq].reshape(-1, 32, 128)
+        err = np.abs(g - x.astype(np.float64))
+        if axis == -2:
+            assert (err <= s[:, None, :].astype(np.float64) / 2 * (1 + 1e-6) + 1e-7).all()
+            gi = np.arange(g.shape[0])[:, None]
+            np.testing.assert_array_equal(g[gi, idx, np.arange(128)[None, :]], val.astype(np.float64))
+        else:
+            assert (err <= s[:, :, None].astype(np.float64) / 2 * (1 + 1e-6) + 1e-7).all()
+            gi = np.arange(g.shape[0])[:, None]
+            np.testing.assert_array_equal(g[gi, np.arange(32)[None, :], idx], val.astype(np.float64))
+
+
+def test_dense_sparse_helps_on_per_token_spikes():
+    """Outliers at random positions (not fixed channels) skew per-channel key
+    groups and per-token value ranges; isolating one per vector lowers the
+    mean attention error."""
+    rng = np.random.default_rng(36)
+    T, Hq = 250, 64
+    k = rng.standard_normal((1, 1, T, 128)).astype(np.float32)
+    v = rng.standard_normal((1, 1, T, 128)).astype(np.float32)
+    for a in (k, v):
+        a[rng.random(a.shape) < 0.004] *= 30
+    k, v = k.astype(np.float16), v.astype(np.float16)
+    q = rng.standard_normal((1, Hq, 128)).astype(np.float16)
+    scale = 1 / np.sqrt(128)
+    exact = np.stack([oracle.dense_attention(q[0, j].astype(np.float64), k[0, 0].astype(np.float64),
+                                             v[0, 0].astype(np.float64), scale) for j in range(Hq)])
+    errs = {}
+    for sp in (False, True):
+        c = oracle.OracleCache(1, 1, 256, 2, residual=32, outliers=sp)
+        c.append(k, v, [T])
+        errs[sp] = float(np.abs(c.attention(q)[0].astype(np.float64) - exact).mean())
+    assert errs[True] < 0.8 * errs[False], errs
