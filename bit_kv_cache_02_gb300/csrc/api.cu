@@ -27,6 +27,8 @@ int check_geometry(const kvq_cache *c) {
   if (c->key_per_token && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
   if (c->hadamard != 0 && c->hadamard != 1) return KVQ_ERR_INVALID_ARG;
   if (c->hadamard && c->pre_rope) return KVQ_ERR_UNSUPPORTED;
+  if (c->outliers != 0 && c->outliers != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->outliers && (c->pre_rope || c->hadamard)) return KVQ_ERR_UNSUPPORTED;
   if (c->block_table && c->num_blocks < 0) return KVQ_ERR_INVALID_ARG;
   if (c->num_seqs > 65535 || c->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
@@ -65,6 +67,7 @@ kvq::Geo make_geo(const kvq_cache *c) {
   g.pre_rope = c->pre_rope;
   g.kpt = c->key_per_token;
   g.rot = c->hadamard;
+  g.sparse = c->outliers;
   g.theta = c->rope_theta;
   g.capacity = c->capacity;
   g.max_groups = max_groups_of(c);
@@ -89,9 +92,11 @@ int from_cuda(cudaError_t e, uint64_t launched) {
 
 extern "C" {
 
-int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token) {
-  if (head_dim != kvq::kD || (bits != 2 && bits != 4) || (key_per_token != 0 && key_per_token != 1)) return 0;
-  return kvq::block_bytes(bits, key_per_token != 0);
+int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token, int32_t outliers) {
+  if (head_dim != kvq::kD || (bits != 2 && bits != 4) || (key_per_token != 0 && key_per_token != 1) ||
+      (outliers != 0 && outliers != 1))
+    return 0;
+  return kvq::block_bytes(bits, key_per_token != 0, outliers != 0);
 }
 
 int32_t kvq_max_groups(const kvq_cache *cache) {
@@ -105,7 +110,7 @@ int64_t kvq_buffer_bytes(const kvq_cache *c, int32_t which) {
   switch (which) {
     case KVQ_BUF_BLOCKS:
       return (c->block_table ? static_cast<int64_t>(c->num_blocks) : sh * max_groups_of(c)) *
-             kvq::block_bytes(c->bits, c->key_per_token != 0);
+             kvq::block_bytes(c->bits, c->key_per_token != 0, c->outliers != 0);
     case KVQ_BUF_BLOCK_TABLE: return c->block_table ? sh * max_groups_of(c) * 4 : 0;
     case KVQ_BUF_K_RES:
     case KVQ_BUF_V_RES: return sh * c->residual * kvq::kD * 2;

@@ -1,7 +1,8 @@
 // Decode attention: the plan kernel, the RoPE tables, the workspace plan and
-// the launch of the contiguous-layout kernels (the paged-layout and the
-// rotating-cache kernels are instantiated in decode_paged.cu, decode_rot.cu
-// and decode_rot_paged.cu).  The kernel itself is in decode_kernel.cuh.
+// the launch of the contiguous-layout kernels (the paged-layout, the
+// rotating-cache and the dense-and-sparse kernels are instantiated in
+// decode_paged.cu, decode_rot*.cu and decode_sparse*.cu).  The kernel itself
+// is in decode_kernel.cuh.
 #include "decode_kernel.cuh"
 
 namespace kvq {
@@ -154,12 +155,14 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const int gq = Hq / geo.H;
-  if (geo.rot)
+  if (geo.sparse)
+    e = geo.table ? launch_sparse_paged(a, gq, stream) : launch_sparse(a, gq, stream);
+  else if (geo.rot)
     e = geo.table ? launch_rot_paged(a, gq, stream) : launch_rot(a, gq, stream);
   else if (geo.table)
     e = launch_paged(a, gq, stream);
   else
-    e = geo.bits == 2 ? launch_b<2, false, false>(a, gq, stream) : launch_b<4, false, false>(a, gq, stream);
+    e = geo.bits == 2 ? launch_b<2, false, false, false>(a, gq, stream) : launch_b<4, false, false, false>(a, gq, stream);
   *launches += inline_plan ? 1 : 2;
   return e;
 }

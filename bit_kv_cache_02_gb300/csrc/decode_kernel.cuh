@@ -69,8 +69,10 @@ struct DecodeArgs {
 
 // Shared memory of one warp: a ring of NS group blocks, one mbarrier per
 // slot, the query of the current pair (fp32, GQ heads), whose space the
-// score operand staging reuses once the query sits in registers, and (keys
-// stored pre-RoPE) the per-group channel-pair coefficients.
+// score operand staging reuses once the query sits in registers, (keys
+// stored pre-RoPE) the per-group channel-pair coefficients, and
+// (dense-and-sparse blocks) the outlier corrections: score corrections of
+// two groups [2][GQ][32] and value corrections [GQ][128], fp32.
 // Ring slots (group blocks in flight) per warp.
 #ifndef KVQ_DECODE_RING_2BIT
 #define KVQ_DECODE_RING_2BIT 4
@@ -79,14 +81,18 @@ struct DecodeArgs {
 #define KVQ_DECODE_RING_4BIT 2
 #endif
 
-template <int BITS, int GQ, bool ROPE, bool KPT>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool SP = false>
 struct WarpSmem {
-  static constexpr int BB = block_bytes(BITS, KPT);
-  static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2) : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
+  static constexpr int BB = block_bytes(BITS, KPT, SP);
+  static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2)
+                            : SP ? ((BITS == 2 && GQ != 2) ? 3 : 2)
+                                 : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
   static constexpr int BAR_OFF = NS * BB;
   static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
   static constexpr int COEF_OFF = Q_OFF + GQ * kD * 4;            // [GQ][64] float4, then [GQ][64] float2
-  static constexpr int BYTES = (COEF_OFF + (ROPE ? GQ * 64 * 24 : 0) + 127) / 128 * 128;
+  static constexpr int SP_OFF = COEF_OFF + (ROPE ? GQ * 64 * 24 : 0);
+  static constexpr int SP_FLOATS = SP ? GQ * (2 * kG + kD) : 0;
+  static constexpr int BYTES = (SP_OFF + SP_FLOATS * 4 + 127) / 128 * 128;
   static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
 };
 
@@ -392,6 +398,29 @@ static __device__ __forceinline__ void group_scores_kpt(const uint8_t *blk, cons
     }
 }
 
+// Dense-and-sparse blocks, per-channel keys: each lane adds, for its four
+// query channels (those of QkOperand), q_d (x_d - min_d) of every head to
+// the score correction of the channel's outlier token t_d (zc[h][t]; one
+// outlier per channel, several may share a token, hence the shared-memory
+// atomics).  The dense part already holds code 0 there, i.e. min_d.
+template <int BITS, int GQ>
+static __device__ __forceinline__ void key_outliers(const uint8_t *blk, const QkOperand<GQ> &qo, float *zc, int lane) {
+  const int c0 = QkOperand<GQ>::chan0(lane);
+  const uint32_t *ksp = reinterpret_cast<const uint32_t *>(blk + off_ksp(BITS));
+  const float *km = reinterpret_cast<const float *>(blk + off_km(BITS));
+  const uint2 e01 = *reinterpret_cast<const uint2 *>(ksp + c0), e89 = *reinterpret_cast<const uint2 *>(ksp + c0 + 8);
+  const float2 m01 = *reinterpret_cast<const float2 *>(km + c0), m89 = *reinterpret_cast<const float2 *>(km + c0 + 8);
+  const uint32_t e[4] = {e01.x, e01.y, e89.x, e89.y};
+  const float m[4] = {m01.x, m01.y, m89.x, m89.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float dx = __half2float(__ushort_as_half(static_cast<unsigned short>(e[i] & 0xFFFFu))) - m[i];
+    const int t = static_cast<int>(e[i] >> 16) & (kG - 1);
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) atomicAdd(zc + h * kG + t, qo.qv[h][i] * dx);
+  }
+}
+
 // o += values of one group weighted by ps (score layout: token 8*tau + g,
 // head q).  The value mma's B column h carries head h's p_t * scale_t as one
 // fp16 (its rounding error, at most 2^-11 relative per weight, enters the
@@ -481,10 +510,10 @@ static __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, f
 #define KVQ_DECODE_MIN_BLOCKS_GQ4 3
 #endif
 
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
     decode_kernel(DecodeArgs a) {
-  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT, SP>;
   constexpr int NS = WS::NS, BB = WS::BB;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -494,7 +523,12 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
   float *q_s = reinterpret_cast<float *>(ring + WS::Q_OFF);              // [GQ][D]
   uint32_t *stage = reinterpret_cast<uint32_t *>(q_s);                   // score operand staging
   float2 *roff_s = reinterpret_cast<float2 *>(smem + kWarps * WS::BYTES);  // [32][65]
+  float *zc_s = reinterpret_cast<float *>(ring + WS::SP_OFF);            // [2][GQ][32] score corrections
+  float *oc_s = zc_s + 2 * GQ * kG;                                      // [GQ][128] value corrections
   const Geo &geo = a.geo;
+  if (SP) {  // the corrections start at zero; their readers zero them again
+    for (int i = lane; i < WS::SP_FLOATS; i += 32) zc_s[i] = 0.f;
+  }
 
   if (ROPE) {
     for (int i = threadIdx.x; i < kG * 64; i += blockDim.x)
@@ -865,6 +899,41 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
             } else {
               zb[0] = zb[1] = zb[2] = zb[3] = -INFINITY;
             }
+            if (SP) {  // outliers: z_t += zscale q_d (x - min) of each slice's outlier
+              if (KPT) {  // one outlier per token: this lane's tokens, query from shared memory
+                const float *qh = q_s + min(q, GQ - 1) * kD;
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {
+                  if (gg == 1 && !two) break;
+                  const uint8_t *bk = gg ? bb : ba;
+                  const uint32_t *ksp = reinterpret_cast<const uint32_t *>(bk + off_ksp(BITS, true));
+                  const float *km = reinterpret_cast<const float *>(bk + off_km(BITS, true));
+#pragma unroll
+                  for (int tau = 0; tau < 4; ++tau) {
+                    const uint32_t e = ksp[8 * tau + g];
+                    const float dx = __half2float(__ushort_as_half(static_cast<unsigned short>(e & 0xFFFFu))) -
+                                     km[8 * tau + g];
+                    const float corr = a.zscale * qh[(e >> 16) & (kD - 1)] * dx;
+                    if (gg) zb[tau] += corr; else za[tau] += corr;
+                  }
+                }
+              } else {
+                key_outliers<BITS, GQ>(ba, qo, zc_s, lane);
+                if (two) key_outliers<BITS, GQ>(bb, qo, zc_s + GQ * kG, lane);
+                __syncwarp();
+                if (head_valid) {
+#pragma unroll
+                  for (int tau = 0; tau < 4; ++tau) {
+                    float *ca = zc_s + q * kG + 8 * tau + g, *cb = ca + GQ * kG;
+                    za[tau] = fmaf(*ca, qo.qscale, za[tau]);
+                    zb[tau] = fmaf(*cb, qo.qscale, zb[tau]);
+                    *ca = 0.f;
+                    *cb = 0.f;
+                  }
+                }
+                __syncwarp();
+              }
+            }
             float mx = fmaxf(fmaxf(fmaxf(za[0], za[1]), fmaxf(za[2], za[3])),
                              fmaxf(fmaxf(zb[0], zb[1]), fmaxf(zb[2], zb[3])));
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
@@ -877,12 +946,18 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
             const float *vsb = reinterpret_cast<const float *>(bb + off_vs(BITS, KPT));
             const float *vmb = reinterpret_cast<const float *>(bb + off_vm(BITS, KPT));
             float psa[4], psb[4], psum = 0.f, mus = 0.f;
+            float wsp[2][4];  // outliers: p_t (x - min_t) of each token's value outlier
 #pragma unroll
             for (int tau = 0; tau < 4; ++tau) {
               const float pa = fast_exp2(za[tau] - m_new);
               psum += pa;
               psa[tau] = pa * vsa[8 * tau + g];
               mus = fmaf(pa, vma[8 * tau + g], mus);
+              if (SP) {
+                const uint32_t e = reinterpret_cast<const uint32_t *>(ba + off_vsp(BITS, KPT))[8 * tau + g];
+                wsp[0][tau] = pa * (__half2float(__ushort_as_half(static_cast<unsigned short>(e & 0xFFFFu))) -
+                                    vma[8 * tau + g]);
+              }
             }
             if (two) {
 #pragma unroll
@@ -891,13 +966,41 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
                 psum += pb;
                 psb[tau] = pb * vsb[8 * tau + g];
                 mus = fmaf(pb, vmb[8 * tau + g], mus);
+                if (SP) {
+                  const uint32_t e = reinterpret_cast<const uint32_t *>(bb + off_vsp(BITS, KPT))[8 * tau + g];
+                  wsp[1][tau] = pb * (__half2float(__ushort_as_half(static_cast<unsigned short>(e & 0xFFFFu))) -
+                                      vmb[8 * tau + g]);
+                }
               }
             }
             l_run = fmaf(l_run, alpha, psum);
             mu_run = fmaf(mu_run, alpha, mus);
             m_run = m_new;
-            if (__any_sync(kFull, head_valid && alpha != 1.f))
+            const bool rescale = __any_sync(kFull, head_valid && alpha != 1.f);
+            if (rescale)
               rescale_o(o, __shfl_sync(kFull, alpha, (2 * q) & 31), __shfl_sync(kFull, alpha, (2 * q + 1) & 31));
+            if (SP) {  // value corrections: rescaled with o, then this step's outliers added
+              if (rescale) {
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                  const float ah = __shfl_sync(kFull, alpha, hh);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) oc_s[hh * kD + lane + 32 * j] *= ah;
+                }
+              }
+              __syncwarp();
+              if (head_valid) {
+#pragma unroll
+                for (int tau = 0; tau < 4; ++tau) {
+                  const uint32_t ea = reinterpret_cast<const uint32_t *>(ba + off_vsp(BITS, KPT))[8 * tau + g];
+                  atomicAdd(oc_s + q * kD + ((ea >> 16) & (kD - 1)), wsp[0][tau]);
+                  if (two) {
+                    const uint32_t eb = reinterpret_cast<const uint32_t *>(bb + off_vsp(BITS, KPT))[8 * tau + g];
+                    atomicAdd(oc_s + q * kD + ((eb >> 16) & (kD - 1)), wsp[1][tau]);
+                  }
+                }
+              }
+            }
             group_values<BITS, ROT>(ba, psa, lane, o);
             if (two) group_values<BITS, ROT>(bb, psb, lane, o);
             __syncwarp();
@@ -1064,6 +1167,7 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_down_sync(kFull, o[mt][i], 2);
       }
+      if (SP) __syncwarp();  // every value correction of the range is in
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (2 * q + c < GQ) {
@@ -1071,10 +1175,18 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-              po[16 * mt + 8 * rr + g] = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
+            for (int rr = 0; rr < 2; ++rr) {
+              float v = fmaf(o[mt][2 * rr + c], val_row_scale<BITS>(mt, rr), mu_c[c]);
+              if (SP) {
+                float *oc = oc_s + (2 * q + c) * kD + 16 * mt + 8 * rr + g;
+                v += *oc;
+                *oc = 0.f;
+              }
+              po[16 * mt + 8 * rr + g] = v;
+            }
         }
       }
+      if (SP) __syncwarp();
       if (head_valid && g == 0) a.part_ml[slot * GQ + q] = make_float2(m_run, l_run);
       ++npart;
     }
@@ -1153,14 +1265,17 @@ int decode_warps_override();
 cudaError_t launch_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
 cudaError_t launch_rot(const DecodeArgs &a, int gq, cudaStream_t stream);
 cudaError_t launch_rot_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
+// Defined in decode_sparse.cu and decode_sparse_paged.cu: dense-and-sparse blocks.
+cudaError_t launch_sparse(const DecodeArgs &a, int gq, cudaStream_t stream);
+cudaError_t launch_sparse_paged(const DecodeArgs &a, int gq, cudaStream_t stream);
 
 // Resident CTAs per SM of one instantiation on the current device, and the
 // device's SM count (cached per device ordinal).
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
-  using WS = WarpSmem<BITS, GQ, ROPE, KPT>;
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT, SP>;
   constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
-  auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT>;
+  auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT, SP>;
   static int resident[64] = {};
   static int sms[64] = {};
   bytes_out = bytes;
@@ -1187,10 +1302,10 @@ static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
 
 // Warps one launch spreads the work over: every resident warp of the device
 // (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
-template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT>
+template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   int per_sm = 0, n_sm = 0, bytes = 0;
-  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED, ROT>(per_sm, n_sm, bytes);
+  cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED, ROT, SP>(per_sm, n_sm, bytes);
   if (e != cudaSuccess) return e;
   const int over = decode_warps_override();
   int nw = over ? over : min(n_sm * per_sm * kWarps, kMaxDecodeWarps);
@@ -1199,27 +1314,27 @@ static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
   if (a.base != nullptr) {
     if ((e = launch_plan(a, stream)) != cudaSuccess) return e;
   }
-  decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
+  decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT, SP><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <int BITS, int GQ, bool PAGED, bool ROT>
+template <int BITS, int GQ, bool PAGED, bool ROT, bool SP>
 static cudaError_t launch_g(const DecodeArgs &a, cudaStream_t stream) {
-  // keys grouped per token, and rotating caches, are never stored pre-RoPE
-  // (rejected at the boundary)
-  if (a.geo.kpt) return launch_t<BITS, GQ, false, true, PAGED, ROT>(a, stream);
-  if constexpr (!ROT) {
-    if (a.geo.pre_rope) return launch_t<BITS, GQ, true, false, PAGED, false>(a, stream);
+  // keys grouped per token, rotating caches and dense-and-sparse blocks are
+  // never stored pre-RoPE (rejected at the boundary)
+  if (a.geo.kpt) return launch_t<BITS, GQ, false, true, PAGED, ROT, SP>(a, stream);
+  if constexpr (!ROT && !SP) {
+    if (a.geo.pre_rope) return launch_t<BITS, GQ, true, false, PAGED, false, false>(a, stream);
   }
-  return launch_t<BITS, GQ, false, false, PAGED, ROT>(a, stream);
+  return launch_t<BITS, GQ, false, false, PAGED, ROT, SP>(a, stream);
 }
 
-template <int BITS, bool PAGED, bool ROT>
+template <int BITS, bool PAGED, bool ROT, bool SP>
 static cudaError_t launch_b(const DecodeArgs &a, int gq, cudaStream_t stream) {
   switch (gq) {
-    case 1: return launch_g<BITS, 1, PAGED, ROT>(a, stream);
-    case 2: return launch_g<BITS, 2, PAGED, ROT>(a, stream);
-    default: return launch_g<BITS, 4, PAGED, ROT>(a, stream);
+    case 1: return launch_g<BITS, 1, PAGED, ROT, SP>(a, stream);
+    case 2: return launch_g<BITS, 2, PAGED, ROT, SP>(a, stream);
+    default: return launch_g<BITS, 4, PAGED, ROT, SP>(a, stream);
   }
 }
 

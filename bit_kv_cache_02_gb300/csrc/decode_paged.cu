@@ -7,7 +7,7 @@
 namespace kvq {
 
 cudaError_t launch_paged(const DecodeArgs &a, int gq, cudaStream_t stream) {
-  return a.geo.bits == 2 ? launch_b<2, true, false>(a, gq, stream) : launch_b<4, true, false>(a, gq, stream);
+  return a.geo.bits == 2 ? launch_b<2, true, false, false>(a, gq, stream) : launch_b<4, true, false, false>(a, gq, stream);
 }
 
 }  // namespace kvq

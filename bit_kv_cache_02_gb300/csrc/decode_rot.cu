@@ -8,7 +8,7 @@
 namespace kvq {
 
 cudaError_t launch_rot(const DecodeArgs &a, int gq, cudaStream_t stream) {
-  return a.geo.bits == 2 ? launch_b<2, false, true>(a, gq, stream) : launch_b<4, false, true>(a, gq, stream);
+  return a.geo.bits == 2 ? launch_b<2, false, true, false>(a, gq, stream) : launch_b<4, false, true, false>(a, gq, stream);
 }
 
 }  // namespace kvq

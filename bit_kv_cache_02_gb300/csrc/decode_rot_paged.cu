@@ -5,7 +5,7 @@
 namespace kvq {
 
 cudaError_t launch_rot_paged(const DecodeArgs &a, int gq, cudaStream_t stream) {
-  return a.geo.bits == 2 ? launch_b<2, true, true>(a, gq, stream) : launch_b<4, true, true>(a, gq, stream);
+  return a.geo.bits == 2 ? launch_b<2, true, true, false>(a, gq, stream) : launch_b<4, true, true, false>(a, gq, stream);
 }
 
 }  // namespace kvq

@@ -4,7 +4,8 @@
 // quantization", "What they report"); keys per channel / values per token
 // (KIVI page, second paragraph).  Keys are returned pre-RoPE.  When the
 // cache rotates its tokens (Walsh-Hadamard, include/kvq.h) the group rows
-// are rotated back, x_hat = H y_hat, in fp32.
+// are rotated back, x_hat = H y_hat, in fp32.  Dense-and-sparse blocks
+// return each slice's outlier as its stored fp16 value.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -37,7 +38,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
   float *vo = v_out + sh * geo.capacity * kD;
   if (gi < geo.max_groups) {
     if (gi >= sp.Lq / kG) return;
-    const uint8_t *blk = group_block(geo, s, h, gi, block_bytes(BITS, KPT));
+    const uint8_t *blk = group_block(geo, s, h, gi, block_bytes(BITS, KPT, geo.sparse != 0));
     if (!blk) {
       if (threadIdx.x == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
       return;
@@ -46,14 +47,21 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
     const float *km = reinterpret_cast<const float *>(blk + off_km(BITS, KPT));
     const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS, KPT));
     const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS, KPT));
+    const uint32_t *ksp = reinterpret_cast<const uint32_t *>(blk + off_ksp(BITS, KPT));
+    const uint32_t *vsp = reinterpret_cast<const uint32_t *>(blk + off_vsp(BITS, KPT));
     const int p0 = sp.nsink + gi * kG;
     __shared__ float rows[2 * kG][kD];  // rotated layout: key rows, then value rows
     for (int idx = threadIdx.x; idx < kG * kD; idx += blockDim.x) {
       const int t = idx / kD, d = idx % kD;
       const uint32_t ck = tile_code<BITS>(blk + off_kc(BITS), t, d, kD);
       const uint32_t cv = tile_code<BITS>(blk + off_vc(BITS), d, t, kG);
-      const float kx = fmaf(static_cast<float>(ck), ks[KPT ? t : d], km[KPT ? t : d]);
-      const float vx = fmaf(static_cast<float>(cv), vs[t], vm[t]);
+      float kx = fmaf(static_cast<float>(ck), ks[KPT ? t : d], km[KPT ? t : d]);
+      float vx = fmaf(static_cast<float>(cv), vs[t], vm[t]);
+      if (geo.sparse) {  // entry: fp16 bits, index within the slice at bit 16
+        const uint32_t ek = ksp[KPT ? t : d], ev = vsp[t];
+        if (static_cast<int>(ek >> 16) == (KPT ? d : t)) kx = __half2float(__ushort_as_half(ek & 0xFFFFu));
+        if (static_cast<int>(ev >> 16) == d) vx = __half2float(__ushort_as_half(ev & 0xFFFFu));
+      }
       if (geo.rot) {
         rows[t][d] = kx;
         rows[kG + t][d] = vx;

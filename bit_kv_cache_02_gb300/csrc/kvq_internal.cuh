@@ -29,8 +29,10 @@ constexpr int kG = 32;        // tokens per group
 // are grouped per token (kpt).
 __host__ __device__ constexpr int code_tile_bytes(int bits) { return kG * kD * bits / 8; }
 __host__ __device__ constexpr int kmeta_n(bool kpt) { return kpt ? kG : kD; }
-__host__ __device__ constexpr int block_bytes(int bits, bool kpt = false) {
-  return 2 * code_tile_bytes(bits) + 8 * kmeta_n(kpt) + 8 * kG;
+// sp: dense-and-sparse blocks add one 32-bit outlier entry per key slice and
+// per value token (fp16 value bits 0-15, index within the slice at bit 16).
+__host__ __device__ constexpr int block_bytes(int bits, bool kpt = false, bool sp = false) {
+  return 2 * code_tile_bytes(bits) + 8 * kmeta_n(kpt) + 8 * kG + (sp ? 4 * (kmeta_n(kpt) + kG) : 0);
 }
 __host__ __device__ constexpr int off_kc(int) { return 0; }
 __host__ __device__ constexpr int off_vc(int bits) { return code_tile_bytes(bits); }
@@ -38,12 +40,15 @@ __host__ __device__ constexpr int off_ks(int bits) { return 2 * code_tile_bytes(
 __host__ __device__ constexpr int off_km(int bits, bool kpt = false) { return off_ks(bits) + 4 * kmeta_n(kpt); }
 __host__ __device__ constexpr int off_vs(int bits, bool kpt = false) { return off_km(bits, kpt) + 4 * kmeta_n(kpt); }
 __host__ __device__ constexpr int off_vm(int bits, bool kpt = false) { return off_vs(bits, kpt) + 4 * kG; }
+__host__ __device__ constexpr int off_ksp(int bits, bool kpt = false) { return off_vm(bits, kpt) + 4 * kG; }
+__host__ __device__ constexpr int off_vsp(int bits, bool kpt = false) { return off_ksp(bits, kpt) + 4 * kmeta_n(kpt); }
 
 // Cache geometry and buffers as the kernels see them.
 struct Geo {
   int S, H, R, ns, bits, pre_rope;
   int kpt;  // keys grouped per token
   int rot;  // tokens Walsh-Hadamard rotated before quantization
+  int sparse;  // dense-and-sparse: each slice's largest-magnitude element kept apart
   float theta;
   int capacity;
   int max_groups;

@@ -103,7 +103,9 @@ struct __align__(128) QuantSmem {
   SliceQ vq[kG];             // value token constants
   uint32_t vstat[kG / 2][2]; // value (min, max) half2 of each token pair
   uint32_t kvst[kG / 2][2];  // key (min, max) half2 of each token pair (keys grouped per token)
-  __align__(128) uint8_t blk[block_bytes(4)];  // the packed block being built
+  uint32_t vout[kG];         // dense-and-sparse: outlier entry of each value token
+  uint32_t kout[kG];         // ... and of each key token (keys grouped per token)
+  __align__(128) uint8_t blk[block_bytes(4, false, true)];  // the packed block being built
 };
 
 // One group's rows in registers: thread (p, c8) holds the 16-byte chunk c8
@@ -248,6 +250,64 @@ __device__ __forceinline__ uint4 hadamard_row(uint4 x, int c8) {
   return y;
 }
 
+// Dense-and-sparse split of tokens 2p and 2p + 1, whose 128 channels the 16
+// threads c8 hold 8 each (channels 8 c8 .. 8 c8 + 7 of ra and rb): the
+// outlier is the first channel of largest magnitude; entry[t] holds its fp16
+// bits and, at bit 16, its channel; mn2 / mx2 are the (token 2p, token 2p + 1)
+// half2 min and max over the other 127 channels (fp16 values, so exact).
+// Every thread of the warp calls it.
+__device__ __forceinline__ void token_outliers(const uint4 &ra, const uint4 &rb, int c8, int lane,
+                                               uint32_t (&entry)[2], uint32_t &mn2, uint32_t &mx2) {
+  float lo[2], hi[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const __half *x = reinterpret_cast<const __half *>(t ? &rb : &ra);
+    const uint16_t *xb = reinterpret_cast<const uint16_t *>(t ? &rb : &ra);
+    float best = -1.f;
+    int bi = 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float a = fabsf(__half2float(x[c]));
+      if (a > best) {
+        best = a;
+        bi = 8 * c8 + c;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    float l = INFINITY, u = -INFINITY;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float v = __half2float(x[c]);
+      if (8 * c8 + c != bi) {
+        l = fminf(l, v);
+        u = fmaxf(u, v);
+      } else {
+        bits = xb[c];
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      l = fminf(l, __shfl_xor_sync(0xffffffffu, l, o));
+      u = fmaxf(u, __shfl_xor_sync(0xffffffffu, u, o));
+    }
+    bits = __shfl_sync(0xffffffffu, bits, (lane & 16) | (bi >> 3));  // from the thread holding channel bi
+    entry[t] = bits | (static_cast<uint32_t>(bi) << 16);
+    lo[t] = l;
+    hi[t] = u;
+  }
+  mn2 = h2_as_u32(__floats2half2_rn(lo[0], lo[1]));
+  mx2 = h2_as_u32(__floats2half2_rn(hi[0], hi[1]));
+}
+
 // Quantize and pack the group held in `rin` (tokens from stream index i0 of
 // (s, h)) and write its block with a bulk copy issued by thread 0.  Before
 // the call thread 0 must have waited (bulk_wait_read) for the previous
@@ -255,7 +315,11 @@ __device__ __forceinline__ uint4 hadamard_row(uint4 x, int c8) {
 // every read of the tiles.  KPT: keys grouped per token (scale and min over
 // each token's channels, like values) instead of per channel.  ROT: the
 // rows are Walsh-Hadamard rotated first (every thread of the CTA calls this).
-template <int BITS, bool KPT, bool ROT>
+// SP: dense-and-sparse ("KV cache quantization", "What they report",
+// KVQuant paragraph): each slice's first largest-magnitude element leaves
+// the statistics, its entry goes to the block, and its tile element is
+// replaced by the slice's min so that the packing codes it 0.
+template <int BITS, bool KPT, bool ROT, bool SP>
 __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &rin, const Geo &geo, int s, int h,
                                                int i0) {
   constexpr int NU = 8 / BITS;  // fields per byte
@@ -278,7 +342,7 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   {
     *reinterpret_cast<uint4 *>(&sm.k[(2 * p) * 64 + 4 * c8]) = r.k[0];
     *reinterpret_cast<uint4 *>(&sm.k[(2 * p + 1) * 64 + 4 * c8]) = r.k[1];
-    if (!KPT) {
+    if (!KPT && !SP) {
       const uint32_t ka[4] = {r.k[0].x, r.k[0].y, r.k[0].z, r.k[0].w};
       const uint32_t kb[4] = {r.k[1].x, r.k[1].y, r.k[1].z, r.k[1].w};
       uint32_t kmn[4], kmx[4];
@@ -294,7 +358,14 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
         ks[0] = make_uint4(kmn[0], kmx[0], kmn[1], kmx[1]);
         ks[1] = make_uint4(kmn[2], kmx[2], kmn[3], kmx[3]);
       }
-    } else {  // per-token keys: (token 2p, token 2p + 1) min/max over the 128 channels
+    } else if (KPT && SP) {
+      uint32_t e[2], mn2, mx2;
+      token_outliers(r.k[0], r.k[1], c8, lane, e, mn2, mx2);
+      if (c8 == 0) {
+        *reinterpret_cast<uint2 *>(sm.kvst[p]) = make_uint2(mn2, mx2);
+        *reinterpret_cast<uint2 *>(&sm.kout[2 * p]) = make_uint2(e[0], e[1]);
+      }
+    } else if (KPT) {  // per-token keys: (token 2p, token 2p + 1) min/max over the 128 channels
       const __half *ka = reinterpret_cast<const __half *>(&r.k[0]);
       const __half *kb = reinterpret_cast<const __half *>(&r.k[1]);
       __half2 kn2 = __halves2half2(ka[0], kb[0]), kx2 = kn2;
@@ -318,6 +389,13 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     const __half *va = reinterpret_cast<const __half *>(&r.v[0]);
     const __half *vb = reinterpret_cast<const __half *>(&r.v[1]);
     __half2 mn2 = __halves2half2(va[0], vb[0]), mx2 = mn2;
+    if (SP) {
+      uint32_t e[2], smn, smx;
+      token_outliers(r.v[0], r.v[1], c8, lane, e, smn, smx);
+      mn2 = *reinterpret_cast<const __half2 *>(&smn);
+      mx2 = *reinterpret_cast<const __half2 *>(&smx);
+      if (c8 == 0) *reinterpret_cast<uint2 *>(&sm.vout[2 * p]) = make_uint2(e[0], e[1]);
+    }
     // vword(8 c8 + c, p) = 128 c8 + 32 (c / 2) + ((p ^ 2 c8) ^ 16 (c % 2) ^ 4 (c / 2))
     uint32_t *vrow = sm.v + 128 * c8;
     const int vx = p ^ (2 * c8);
@@ -325,15 +403,19 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     for (int c = 0; c < 8; ++c) {
       const __half2 pr = __halves2half2(va[c], vb[c]);  // (token 2p, token 2p + 1) of channel 8 c8 + c
       vrow[32 * (c >> 1) + (vx ^ ((16 * (c & 1)) ^ (4 * (c >> 1))))] = *reinterpret_cast<const uint32_t *>(&pr);
-      mn2 = __hmin2(mn2, pr);
-      mx2 = __hmax2(mx2, pr);
+      if (!SP) {
+        mn2 = __hmin2(mn2, pr);
+        mx2 = __hmax2(mx2, pr);
+      }
     }
+    if (!SP) {
 #pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {  // over the 16 lanes holding the tokens' 128 channels
-      const uint32_t a = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mn2), o);
-      const uint32_t b = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mx2), o);
-      mn2 = __hmin2(mn2, *reinterpret_cast<const __half2 *>(&a));
-      mx2 = __hmax2(mx2, *reinterpret_cast<const __half2 *>(&b));
+      for (int o = 1; o < 16; o <<= 1) {  // over the 16 lanes holding the tokens' 128 channels
+        const uint32_t a = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mn2), o);
+        const uint32_t b = __shfl_xor_sync(0xffffffffu, *reinterpret_cast<uint32_t *>(&mx2), o);
+        mn2 = __hmin2(mn2, *reinterpret_cast<const __half2 *>(&a));
+        mx2 = __hmax2(mx2, *reinterpret_cast<const __half2 *>(&b));
+      }
     }
     if (c8 == 0)
       *reinterpret_cast<uint2 *>(sm.vstat[p]) =
@@ -349,16 +431,51 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     sm.kq[tid] = make_slice(lo, sc, levels);
     blkf[off_ks(BITS) / 4 + tid] = sc;
     blkf[off_km(BITS, KPT) / 4 + tid] = lo;
-  } else if (!KPT && tid < kD) {
-    const int cp = tid >> 1, e = tid & 1;
-    uint32_t mn = sm.kstat[0][cp][0], mx = sm.kstat[0][cp][1];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) {
-      mn = h2min(mn, sm.kstat[w][cp][0]);
-      mx = h2max(mx, sm.kstat[w][cp][1]);
+    if (SP) {  // the entry, and the outlier's tile element becomes the min (code 0)
+      const uint32_t e = sm.kout[tid];
+      blkw[off_ksp(BITS, KPT) / 4 + tid] = e;
+      reinterpret_cast<__half *>(sm.k)[kD * tid + (e >> 16)] = __float2half_rn(lo);
     }
-    const float2 mnf = h2_to_f2_pos0(mn), mxf = h2_to_f2_pos0(mx);
-    const float lo = e ? mnf.y : mnf.x, hi = e ? mxf.y : mxf.x;
+  } else if (!KPT && tid < kD) {
+    float lo, hi;
+    if (SP) {  // channel tid over the group's 32 tokens, from the tile
+      const __half *col = reinterpret_cast<const __half *>(sm.k) + tid;  // token t at col[kD * t]
+      float best = -1.f;
+      int bi = 0;
+      for (int t = 0; t < kG; ++t) {
+        const float a = fabsf(__half2float(col[kD * t]));
+        if (a > best) {
+          best = a;
+          bi = t;
+        }
+      }
+      lo = INFINITY;
+      hi = -INFINITY;
+      for (int t = 0; t < kG; ++t) {
+        if (t == bi) continue;
+        const float v = __half2float(col[kD * t]);
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+      }
+      lo = __fadd_rn(lo, 0.f);
+      hi = __fadd_rn(hi, 0.f);
+      const uint32_t bits = reinterpret_cast<const uint16_t *>(sm.k)[kD * bi + tid];
+      blkw[off_ksp(BITS, KPT) / 4 + tid] = bits | (static_cast<uint32_t>(bi) << 16);
+      // the outlier's tile element becomes the min (code 0); the neighbouring
+      // channel's thread only ever reads the other half of this word
+      reinterpret_cast<__half *>(sm.k)[kD * bi + tid] = __float2half_rn(lo);
+    } else {
+      const int cp = tid >> 1, e = tid & 1;
+      uint32_t mn = sm.kstat[0][cp][0], mx = sm.kstat[0][cp][1];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) {
+        mn = h2min(mn, sm.kstat[w][cp][0]);
+        mx = h2max(mx, sm.kstat[w][cp][1]);
+      }
+      const float2 mnf = h2_to_f2_pos0(mn), mxf = h2_to_f2_pos0(mx);
+      lo = e ? mnf.y : mnf.x;
+      hi = e ? mxf.y : mxf.x;
+    }
     const float sc = __fdiv_rn(__fsub_rn(hi, lo), levels);
     sm.kq[tid] = make_slice(lo, sc, levels);
     blkf[off_ks(BITS) / 4 + tid] = sc;
@@ -371,6 +488,11 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
     sm.vq[t] = make_slice(lo, sc, levels);
     blkf[off_vs(BITS, KPT) / 4 + t] = sc;
     blkf[off_vm(BITS, KPT) / 4 + t] = lo;
+    if (SP) {
+      const uint32_t e = sm.vout[t];
+      blkw[off_vsp(BITS, KPT) / 4 + t] = e;
+      reinterpret_cast<__half *>(&sm.v[vword(e >> 16, t >> 1)])[t & 1] = __float2half_rn(lo);
+    }
   }
   __syncthreads();
 
@@ -494,9 +616,9 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   fence_proxy_async();  // this thread's block writes, before the bulk copy reads them
   __syncthreads();
   if (tid == 0) {
-    uint8_t *dst = group_block(geo, s, h, i0 / kG, block_bytes(BITS, KPT));
+    uint8_t *dst = group_block(geo, s, h, i0 / kG, block_bytes(BITS, KPT, SP));
     if (dst)
-      bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT));
+      bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT, SP));
     else
       set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
   }
@@ -511,7 +633,7 @@ constexpr int kLenMask = (1 << kLenBits) - 1;
 // t % gmax of (sequence, KV head) t / gmax (fewer than 2^31 tasks); CTA b
 // takes tasks b, b + grid, ... and loads the next task's rows while it
 // quantizes the current one.
-template <int BITS, bool KPT, bool ROT>
+template <int BITS, bool KPT, bool ROT, bool SP>
 __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                        const __half *__restrict__ v_new,
                                                                        const int *__restrict__ new_len,
@@ -561,7 +683,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quant_flush_kernel(Geo geo, 
     const bool more = find(nxt);
     if (more) load_group(rn, geo, nxt, k_new, v_new, max_new);
     if (threadIdx.x == 0) bulk_wait_read();  // the previous block's copy has left sm.blk
-    quantize_group<BITS, KPT, ROT>(sm, rc, geo, cur.s, cur.h, cur.i0);
+    quantize_group<BITS, KPT, ROT, SP>(sm, rc, geo, cur.s, cur.h, cur.i0);
     if (!more) break;
     cur = nxt;
     rc = rn;
@@ -614,7 +736,7 @@ __device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1,
 // fills, the copy would overwrite window slots the sequence's other CTAs may
 // still be quantizing, so the CTAs arrive after quantizing and the last one
 // copies the new tokens of every head.
-template <int BITS, bool KPT, bool ROT>
+template <int BITS, bool KPT, bool ROT, bool SP>
 __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, const __half *__restrict__ k_new,
                                                                     const __half *__restrict__ v_new,
                                                                     const int *__restrict__ new_len, int max_new) {
@@ -691,7 +813,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, 
         load_group(rn, geo, g, k_new, v_new, max_new);
       }
       if (threadIdx.x == 0) bulk_wait_read();
-      quantize_group<BITS, KPT, ROT>(sm, rc, geo, s, h, i0);
+      quantize_group<BITS, KPT, ROT, SP>(sm, rc, geo, s, h, i0);
       rc = rn;
     }
     // quantize_group ends with a barrier: every read of the window is done
@@ -736,21 +858,24 @@ int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R /
 using FlushKernel = void (*)(Geo, const __half *, const __half *, const int *, int, int);
 using StepKernel = void (*)(Geo, const __half *, const __half *, const int *, int);
 
-// Instantiations by (bits, keys per token, rotation).
-static int variant(const Geo &geo) { return (geo.bits == 4 ? 4 : 0) + (geo.kpt ? 2 : 0) + (geo.rot ? 1 : 0); }
-static const FlushKernel kFlushKernels[8] = {
-    quant_flush_kernel<2, false, false>, quant_flush_kernel<2, false, true>, quant_flush_kernel<2, true, false>,
-    quant_flush_kernel<2, true, true>,   quant_flush_kernel<4, false, false>, quant_flush_kernel<4, false, true>,
-    quant_flush_kernel<4, true, false>,  quant_flush_kernel<4, true, true>};
-static const StepKernel kStepKernels[8] = {
-    step_append_kernel<2, false, false>, step_append_kernel<2, false, true>, step_append_kernel<2, true, false>,
-    step_append_kernel<2, true, true>,   step_append_kernel<4, false, false>, step_append_kernel<4, false, true>,
-    step_append_kernel<4, true, false>,  step_append_kernel<4, true, true>};
+// Instantiations by (bits, keys per token, plain / rotated / dense-and-sparse).
+static int variant(const Geo &geo) {
+  return ((geo.bits == 4 ? 2 : 0) + (geo.kpt ? 1 : 0)) * 3 + (geo.rot ? 1 : geo.sparse ? 2 : 0);
+}
+#define KVQ_QUANT_SET(K, B, P)                                                                  \
+  K<B, P, false, false>, K<B, P, true, false>, K<B, P, false, true>
+static const FlushKernel kFlushKernels[12] = {
+    KVQ_QUANT_SET(quant_flush_kernel, 2, false), KVQ_QUANT_SET(quant_flush_kernel, 2, true),
+    KVQ_QUANT_SET(quant_flush_kernel, 4, false), KVQ_QUANT_SET(quant_flush_kernel, 4, true)};
+static const StepKernel kStepKernels[12] = {
+    KVQ_QUANT_SET(step_append_kernel, 2, false), KVQ_QUANT_SET(step_append_kernel, 2, true),
+    KVQ_QUANT_SET(step_append_kernel, 4, false), KVQ_QUANT_SET(step_append_kernel, 4, true)};
+#undef KVQ_QUANT_SET
 
 // Persistent CTAs of flush kernel variant v on the current device: every
 // resident slot (cached per variant and device ordinal).
 static cudaError_t flush_grid(int v, int &ctas) {
-  static int cache[8][64] = {};
+  static int cache[12][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

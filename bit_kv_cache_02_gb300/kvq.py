@@ -39,6 +39,7 @@ class CacheStruct(ctypes.Structure):
         ("bits", c_int32), ("group", c_int32), ("residual", c_int32),
         ("num_sink", c_int32), ("pre_rope", c_int32), ("rope_theta", c_float),
         ("capacity", c_int32), ("key_per_token", c_int32), ("num_blocks", c_int32), ("hadamard", c_int32),
+        ("outliers", c_int32),
         ("blocks", c_void_p), ("k_res", c_void_p), ("v_res", c_void_p),
         ("k_sink", c_void_p), ("v_sink", c_void_p), ("seq_len", c_void_p),
         ("status", c_void_p), ("block_table", c_void_p),
@@ -51,7 +52,7 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(CacheStruct)
     sig = {
-        "kvq_block_bytes": (c_int32, [c_int32, c_int32, c_int32]),
+        "kvq_block_bytes": (c_int32, [c_int32, c_int32, c_int32, c_int32]),
         "kvq_max_groups": (c_int32, [P]),
         "kvq_buffer_bytes": (c_int64, [P, c_int32]),
         "kv_quant_append": (ctypes.c_int, [P, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
@@ -95,8 +96,8 @@ def _stream(stream):
     return c_void_p(stream.cuda_stream)
 
 
-def block_bytes(bits: int, head_dim: int = 128, key_per_token: bool = False) -> int:
-    return lib.kvq_block_bytes(bits, head_dim, int(key_per_token))
+def block_bytes(bits: int, head_dim: int = 128, key_per_token: bool = False, outliers: bool = False) -> int:
+    return lib.kvq_block_bytes(bits, head_dim, int(key_per_token), int(outliers))
 
 
 class KVCache:
@@ -108,24 +109,26 @@ class KVCache:
 
     def __init__(self, num_seqs, num_kv_heads, capacity, bits=2, residual=128, num_sink=0,
                  pre_rope=False, rope_theta=10000.0, head_dim=128, device="cuda", key_per_token=False,
-                 num_blocks=None, paged=False, hadamard=False):
+                 num_blocks=None, paged=False, hadamard=False, outliers=False):
         """num_blocks (or paged=True, for a pool of one block per logical
         group): a paged layout with a pool of that many blocks and a block
         table [S][Hkv][max_groups] (int32, filled with -1: the caller assigns
         pool blocks before the appends that need them).  hadamard: tokens are
-        Walsh-Hadamard rotated before quantization (include/kvq.h)."""
+        Walsh-Hadamard rotated before quantization; outliers: dense-and-sparse
+        blocks (include/kvq.h)."""
         st = CacheStruct(num_seqs, num_kv_heads, head_dim, bits, 32, residual, num_sink,
                          int(bool(pre_rope)), float(rope_theta), capacity, int(bool(key_per_token)),
-                         int(num_blocks or 0), int(bool(hadamard)))
+                         int(num_blocks or 0), int(bool(hadamard)), int(bool(outliers)))
         self.num_seqs, self.num_kv_heads, self.capacity = num_seqs, num_kv_heads, capacity
         self.bits, self.residual, self.num_sink, self.head_dim = bits, residual, num_sink, head_dim
         self.pre_rope, self.rope_theta = bool(pre_rope), rope_theta
         self.key_per_token = bool(key_per_token)
         self.hadamard = bool(hadamard)
+        self.outliers = bool(outliers)
         self.max_groups = lib.kvq_max_groups(ctypes.byref(st))
         if self.max_groups < 0:
             raise KvqError(-2, "kvq_max_groups")
-        self.block_bytes = block_bytes(bits, head_dim, key_per_token)
+        self.block_bytes = block_bytes(bits, head_dim, key_per_token, outliers)
         self.paged = paged or num_blocks is not None
         if self.paged and num_blocks is None:
             num_blocks = num_seqs * num_kv_heads * self.max_groups

@@ -39,6 +39,7 @@ class Workload:
     key_per_token: bool = False  # keys grouped per token (the ablation of per-channel keys)
     paged: bool = False      # group blocks in a shared pool behind a shuffled block table
     hadamard: bool = False   # tokens Walsh-Hadamard rotated before quantization
+    outliers: bool = False   # dense-and-sparse blocks (each slice's largest element kept in fp16)
     extra: dict = field(default_factory=dict)
 
 
@@ -59,6 +60,8 @@ WORKLOADS = {
     "llama2_7b_mha_hadamard": Workload("llama2_7b_mha_hadamard", 32, 16, 32, 32, 4096, 2, hadamard=True),
     "llama2_7b_mha_key_per_token_hadamard": Workload("llama2_7b_mha_key_per_token_hadamard", 32, 16, 32, 32,
                                                      4096, 2, key_per_token=True, hadamard=True),
+    # the Llama-2 shape with dense-and-sparse blocks
+    "llama2_7b_mha_outliers": Workload("llama2_7b_mha_outliers", 32, 16, 32, 32, 4096, 2, outliers=True),
 }
 
 

@@ -116,6 +116,17 @@ extern "C" {
  * the sink and the window keep tokens as given.  Decode scores the groups
  * with H q and rotates their weighted value sum back by H (H H = D I), so
  * its output is attention over x_hat = H y_hat; kv_dequant returns x_hat.
+ *
+ * outliers (per-vector dense-and-sparse, "KV cache quantization", "What
+ * they report", KVQuant paragraph): in every quantization slice (a key
+ * channel's 32 tokens of a group, or a token's D channels for per-token
+ * keys and for values) the element of largest magnitude (the first in slice
+ * order on ties) is the outlier.  The slice's min and scale come from the
+ * other elements, the outlier's code is 0, and the block gains, after V
+ * min, one 32-bit entry per key slice (D, or 32 with per-token keys) and
+ * then one per value token (32): the outlier's fp16 bits in bits 0-15 and
+ * its index within the slice (token, or channel) at bit 16.  The
+ * dequantized outlier is its fp16 value.
  */
 typedef struct kvq_cache {
   int32_t  num_seqs;       /* S, >= 1                                   */
@@ -136,6 +147,8 @@ typedef struct kvq_cache {
   int32_t  hadamard;       /* 1: every key and value token is rotated by
                               the Walsh-Hadamard transform before it is
                               quantized (see below; not with pre_rope)  */
+  int32_t  outliers;       /* 1: dense-and-sparse blocks (see below; not
+                              with pre_rope or hadamard)                */
   uint8_t  *blocks;
   uint16_t *k_res, *v_res;
   uint16_t *k_sink, *v_sink;
@@ -145,9 +158,10 @@ typedef struct kvq_cache {
 } kvq_cache;
 
 /* Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128 with
- * per-channel keys; 2560 / 4608 with per-token keys); 0 for an unsupported
- * (bits, head_dim). */
-int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token);
+ * per-channel keys; 2560 / 4608 with per-token keys; plus 4 * (D + 32), or
+ * 4 * 64 with per-token keys, for dense-and-sparse blocks); 0 for an
+ * unsupported (bits, head_dim) or a flag other than 0 / 1. */
+int32_t kvq_block_bytes(int32_t bits, int32_t head_dim, int32_t key_per_token, int32_t outliers);
 
 /* Quantized groups per (sequence, KV head) the cache can hold; -1 on bad
  * geometry. */

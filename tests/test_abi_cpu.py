@@ -45,9 +45,12 @@ def _struct(kvq, **kw):
 
 
 def test_sizes(kvq):
-    assert kvq.lib.kvq_block_bytes(2, 128, 0) == 3328 and kvq.lib.kvq_block_bytes(4, 128, 0) == 5376
-    assert kvq.lib.kvq_block_bytes(2, 128, 1) == 2560 and kvq.lib.kvq_block_bytes(4, 128, 1) == 4608
-    assert kvq.lib.kvq_block_bytes(3, 128, 0) == 0 and kvq.lib.kvq_block_bytes(2, 64, 0) == 0
+    bb = kvq.lib.kvq_block_bytes
+    assert bb(2, 128, 0, 0) == 3328 and bb(4, 128, 0, 0) == 5376
+    assert bb(2, 128, 1, 0) == 2560 and bb(4, 128, 1, 0) == 4608
+    assert bb(2, 128, 0, 1) == 3968 and bb(4, 128, 0, 1) == 6016     # + one entry per key channel and value token
+    assert bb(2, 128, 1, 1) == 2816 and bb(4, 128, 1, 1) == 4864
+    assert bb(3, 128, 0, 0) == 0 and bb(2, 64, 0, 0) == 0 and bb(2, 128, 0, 2) == 0
     st = _struct(kvq)
     # (1000 - 1) // 128 * 128 = 896 quantized tokens -> 28 groups
     assert kvq.lib.kvq_max_groups(ctypes.byref(st)) == 28
@@ -69,7 +72,7 @@ def test_sizes(kvq):
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 64, -2), ("bits", 3, -2), ("group", 16, -2), ("residual", 100, -2),
     ("residual", 256, -2), ("num_sink", 2, -2), ("num_seqs", 0, -1), ("capacity", 0, -1),
-    ("key_per_token", 2, -1), ("hadamard", 2, -1),
+    ("key_per_token", 2, -1), ("hadamard", 2, -1), ("outliers", 2, -1),
 ])
 def test_bad_geometry_rejected(kvq, field, value, code):
     st = _struct(kvq, **{field: value})
@@ -112,12 +115,24 @@ def test_hadamard_with_pre_rope_unsupported(kvq):
     assert kvq.lib.kvq_max_groups(ctypes.byref(_struct(kvq, hadamard=1, key_per_token=1))) == 28
 
 
+def test_outliers_combinations(kvq):
+    """Dense-and-sparse blocks work with both key groupings and with paging,
+    not with pre-RoPE keys or the rotation; the pool grows by the entries."""
+    fake = ctypes.c_void_p(1 << 20)
+    for kw in (dict(pre_rope=1), dict(hadamard=1)):
+        st = _struct(kvq, outliers=1, **kw)
+        assert kvq.lib.kv_quant_append(ctypes.byref(st), fake, fake, fake, 1, None) == -2
+    st = _struct(kvq, outliers=1, key_per_token=1)
+    assert kvq.lib.kvq_buffer_bytes(ctypes.byref(st), kvq.BUF_BLOCKS) == 2 * 3 * 28 * 2816
+
+
 def test_struct_layout_matches_header(kvq):
-    """The ctypes mirror has the header's field order and offsets: 13 int32
+    """The ctypes mirror has the header's field order and offsets: 14 int32
     or float fields, then eight pointers from byte 56."""
     names = [f[0] for f in kvq.CacheStruct._fields_]
-    assert names[:13] == ["num_seqs", "num_kv_heads", "head_dim", "bits", "group", "residual", "num_sink",
-                          "pre_rope", "rope_theta", "capacity", "key_per_token", "num_blocks", "hadamard"]
+    assert names[:14] == ["num_seqs", "num_kv_heads", "head_dim", "bits", "group", "residual", "num_sink",
+                          "pre_rope", "rope_theta", "capacity", "key_per_token", "num_blocks", "hadamard",
+                          "outliers"]
     assert kvq.CacheStruct.blocks.offset == 56 and ctypes.sizeof(kvq.CacheStruct) == 56 + 8 * 8
 
 

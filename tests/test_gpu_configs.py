@@ -37,7 +37,7 @@ def _run(kvq, name, pairs):
     cap = T + 8
     cache = kvq.KVCache(w.seqs, w.kv_heads, cap, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
                         pre_rope=w.pre_rope, device=dev, key_per_token=w.key_per_token, paged=w.paged,
-                        hadamard=w.hadamard)
+                        hadamard=w.hadamard, outliers=w.outliers)
     if w.paged:
         tbl = synth.block_table(w, 0, w.seqs, w.kv_heads, cache.max_groups)
         cache.block_table.copy_(torch.from_numpy(tbl).to(dev))
@@ -60,7 +60,8 @@ def _run(kvq, name, pairs):
     for s, h in pairs:
         L = int(lens[s])
         orc = oracle.OracleCache(1, 1, cap, w.bits, residual=w.residual, num_sink=w.num_sink,
-                                 key_per_token=w.key_per_token, hadamard=w.hadamard)
+                                 key_per_token=w.key_per_token, hadamard=w.hadamard,
+                                 outliers=w.outliers)
         ks = k[s:s + 1, h:h + 1, :L].cpu().numpy()
         vs = v[s:s + 1, h:h + 1, :L].cpu().numpy()
         orc.append(ks, vs, [L])
@@ -110,9 +111,10 @@ def test_long_context_1m(kvq):
 
 
 @pytest.mark.parametrize("name", ["llama2_7b_mha_key_per_token", "llama2_7b_mha_paged", "llama2_7b_mha_hadamard",
-                                  "llama2_7b_mha_key_per_token_hadamard"])
+                                  "llama2_7b_mha_key_per_token_hadamard", "llama2_7b_mha_outliers"])
 def test_llama2_7b_mha_variants(kvq, name):
     """The Llama-2 shape with keys grouped per token, with its group blocks
     paged through a shuffled block table, and with Walsh-Hadamard rotated
-    tokens (per-channel and per-token keys)."""
+    tokens (per-channel and per-token keys), and with dense-and-sparse
+    blocks."""
     _run(kvq, name, [(0, 0), (15, 31), (9, 12)])

@@ -70,10 +70,11 @@ def _attn_close(got, want):
     return float(err.max())
 
 
-def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False, num_blocks=None, rot=False):
+def _build(kvq, S, H, cap, bits, ns=0, pre_rope=False, R=128, kpt=False, num_blocks=None, rot=False, sp=False):
     cache = kvq.KVCache(S, H, cap, bits=bits, residual=R, num_sink=ns, pre_rope=pre_rope, key_per_token=kpt,
-                        num_blocks=num_blocks, hadamard=rot)
-    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt, hadamard=rot)
+                        num_blocks=num_blocks, hadamard=rot, outliers=sp)
+    orc = oracle.OracleCache(S, H, cap, bits, residual=R, num_sink=ns, key_per_token=kpt, hadamard=rot,
+                             outliers=sp)
     return cache, orc
 
 
@@ -283,6 +284,62 @@ def test_hadamard_rotation(kvq, bits, gq, ns, kpt, paged):
             ns_s, Lq, r = orc.split(s)
             np.testing.assert_array_equal(g[:, :ns_s], w[:, :ns_s])
             np.testing.assert_array_equal(g[:, ns_s + Lq:], w[:, ns_s + Lq:])
+
+
+def _spiky_kv(S, H, T, seed):
+    """Keys with fixed outlier channels plus, in keys and values, random x30
+    spikes, planted equal-magnitude ties (a token row with +8 and -8, a key
+    channel with +9 and -9 in one group) and constant rows."""
+    k, v = _rand_kv(S, H, T, seed)
+    rng = np.random.default_rng(seed + 1000)
+    k, v = k.astype(np.float32), v.astype(np.float32)
+    for a in (k, v):
+        a[rng.random(a.shape) < 0.004] *= 30
+        a[:, :, 5, :] = 0.5
+        a[:, :, 5, 3] = 8.0       # ties inside token rows: the earlier channel wins
+        a[:, :, 5, 70] = -8.0
+        a[:, :, 40, :] = -1.25    # a constant row
+    k[:, :, 64 + 3, 20] = -9.0    # a tie inside a key channel of one group: the earlier token wins
+    k[:, :, 64 + 17, 20] = 9.0
+    return k.astype(np.float16), v.astype(np.float16)
+
+
+@pytest.mark.parametrize("bits,gq,ns,kpt,paged", [(2, 1, 0, False, False), (4, 4, 1, False, False),
+                                                  (2, 2, 1, True, False), (4, 1, 0, True, True),
+                                                  (2, 4, 0, False, True), (4, 2, 1, False, False)])
+def test_dense_and_sparse(kvq, bits, gq, ns, kpt, paged):
+    """Dense-and-sparse blocks: the quantize kernels leave the oracle's bytes
+    (outlier entries, codes with the outlier at 0, statistics of the rest)
+    after a prefill and per-token and chunked appends; attention matches;
+    dequantization returns the outliers exactly and the rest within one fp32
+    ulp."""
+    S, H, T = 3, 2, 450
+    k, v = _spiky_kv(S, H, T, seed=130 + bits + gq + 2 * ns)
+    nb = S * H * 16 + 3 if paged else None
+    cache, orc = _build(kvq, S, H, T + 8, bits, ns=ns, kpt=kpt, num_blocks=nb, sp=True)
+    assert cache.block_bytes == oracle.block_bytes(bits, key_per_token=kpt, outliers=True)
+    if paged:
+        rng = np.random.default_rng(bits + 5)
+        perm = rng.permutation(cache.num_blocks)[:S * H * cache.max_groups].astype(np.int32)
+        cache.block_table.copy_(torch.from_numpy(perm.reshape(S, H, cache.max_groups)).cuda())
+    lens = np.array([T, T - 53, 170])
+    _append(kvq, cache, orc, k[:, :, :230], v[:, :, :230], np.minimum(lens, 230))
+    pos = 230
+    for step in [1] * 60 + [128, 32]:
+        sl = np.clip(lens - pos, 0, step).astype(np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+    assert pos == T
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=gq + 11)
+    _attn_close(_attend(kvq, cache, q, T), orc.attention(q))
+    K = torch.full((S, H, T + 8, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    for s, L in enumerate(lens):
+        np.testing.assert_array_max_ulp(K.cpu().numpy()[s, :, :L], Ko[s, :, :L].astype(np.float32), maxulp=1)
+        np.testing.assert_array_max_ulp(V.cpu().numpy()[s, :, :L], Vo[s, :, :L].astype(np.float32), maxulp=1)
 
 
 @pytest.mark.parametrize("bits,gq,ns,kpt", [(2, 1, 0, False), (4, 4, 1, False), (2, 2, 1, True)])
