@@ -11,7 +11,9 @@ every layer's read comes from HBM.
 Metric: decode-attention context tokens/s/layer = sum over sequences of the
 tokens attended, divided by the time of one layer (step time / layers).  The
 JSON line also carries the roofline of the decode-attention call (algorithmic
-bytes / CUDA-event time against the measured HBM copy bandwidth), the CPU
+bytes / CUDA-event time against the measured HBM copy bandwidth), timed
+before the steps on the workload's own state (context + 1 tokens per
+sequence), the prefill's quantize kernel, the CPU
 oracle's throughput on a bounded sample, and an end-to-end number through the
 same C ABI with host buffers copied in and out every step.
 
@@ -229,13 +231,14 @@ def _num(s):
 
 # ---------------------------------------------------------- our arm (GPU)
 
-def prefill_lengths(w, steps, warmup):
-    """Prefilled tokens per sequence: the workload's context lengths, less
-    half the timed steps and the untimed steps before them, so that the
-    context averaged over the timed steps equals the workload's."""
+def prefill_lengths(w, untimed):
+    """Prefilled tokens per sequence: the workload's context lengths plus its
+    new token, less the untimed steps appended before the timed regions, so
+    that decode attention is timed on the workload's own state (L = context
+    + 1 per sequence: 4096 quantized tokens and a one-token window for the
+    Llama-2 shape); the timed steps continue from there."""
     base = synth.context_lengths(w)
-    shift = warmup + steps // 2
-    return np.maximum(base - shift, 1).astype(np.int64)
+    return np.maximum(base + 1 - untimed, 1).astype(np.int64)
 
 
 def prefill_bytes(lengths, w):
@@ -296,7 +299,7 @@ def run_ours(args, w, layers, rank, world, local):
         kvq.set_decode_warps(args.warps)
     K, W = args.steps, args.warmup
     pool = max(1, min(4, K))
-    pre = prefill_lengths(w, K, max(W, 1) + pool)
+    pre = prefill_lengths(w, max(W, 1) + pool)
     capacity = int(pre.max()) + max(W, 1) + pool + K + 32   # room for the end-to-end steps too
     caches, prefill_s = build_caches(kvq, w, layers, pre, capacity, device)
     prefill = {"seconds_per_layer": statistics.median(prefill_s), "bytes_per_layer": prefill_bytes(pre, w)}
@@ -338,12 +341,27 @@ def run_ours(args, w, layers, rank, world, local):
         graphs[p].replay()
     torch.cuda.synchronize()
     done = max(W, 1) + pool                # steps appended so far
-    lens_at = [pre + 1 + done + i for i in range(K)]   # lengths attended in timed step i
+    attn_lens = pre + done                 # the workload's state: context + 1 per sequence
+    lens_at = [attn_lens + 1 + i for i in range(K)]   # lengths attended in timed step i
     stream = torch.cuda.current_stream(device)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
+    wall_d0 = time.time()
+    # decode attention alone, on the workload's state: the same calls
+    # without the appends, replayed (the state does not change)
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    dgraph.replay()
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for _ in range(K):
+        dgraph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    attn_avg_s = d0.elapsed_time(d1) / 1e3 / (K * layers)
+
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -355,23 +373,11 @@ def run_ours(args, w, layers, rank, world, local):
     t1.record(stream)
     torch.cuda.synchronize()
     if sampler:
-        sampler.mark(wall0, time.time())
+        sampler.mark(wall_d0, time.time())   # both timed regions
     barrier(world)
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t0.elapsed_time(t1)
-
-    # decode attention alone: the same calls without the appends, replayed
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    dgraph.replay()
-    torch.cuda.synchronize()
-    d0.record(stream)
-    for _ in range(K):
-        dgraph.replay()
-    d1.record(stream)
-    torch.cuda.synchronize()
-    attn_avg_s = d0.elapsed_time(d1) / 1e3 / (K * layers)
-    final_lens = pre + done + K
+    final_lens = attn_lens + K
     for c in caches:
         if int(c.status.item()) != 0:
             raise RuntimeError(f"device status {int(c.status.item())} after the timed steps")
@@ -382,8 +388,8 @@ def run_ours(args, w, layers, rank, world, local):
     total_tokens = sum_over_ranks(local_tokens, world, device)
     # tokens/s/layer = (tokens one layer attends) / (step time / layers)
     value = total_tokens / (elapsed_ms / 1e3)
-    bytes_avg = decode_bytes(final_lens, w)
-    attn_tokens_per_s = float(final_lens.sum()) / attn_avg_s
+    bytes_avg = decode_bytes(attn_lens, w)
+    attn_tokens_per_s = float(attn_lens.sum()) / attn_avg_s
 
     e2e = None
     if not args.no_e2e:
@@ -391,7 +397,8 @@ def run_ours(args, w, layers, rank, world, local):
 
     return dict(value=value, elapsed_ms=elapsed_ms, attn_avg_s=attn_avg_s, bytes_avg=bytes_avg,
                 attn_tokens_per_s=attn_tokens_per_s, clocks=clocks, launches=launches_per_step * K,
-                mean_ctx=float(np.mean([l.mean() for l in lens_at])), e2e=e2e, prefill=prefill,
+                mean_ctx=float(np.mean([l.mean() for l in lens_at])), attn_ctx=float(attn_lens.mean()),
+                e2e=e2e, prefill=prefill,
                 cache_bytes=sum(c.blocks.numel() + 4 * c.k_res.numel() for c in caches))
 
 
@@ -566,7 +573,7 @@ def main():
         "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["elapsed_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": f"u{w.bits}-codes/f32-accum",
-        "data": "synthetic", "config": dict(config, mean_ctx_timed=r["mean_ctx"]),
+        "data": "synthetic", "config": dict(config, mean_ctx_timed=r["mean_ctx"], attn_ctx=r["attn_ctx"]),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_nominal_8tbs": achieved / 8000.0, "traffic": traffic,
                      "kernel": "decode_kernel (one per kv_decode_attn call)", "peak_source": which,
