@@ -41,7 +41,6 @@
 
 namespace kvq {
 
-constexpr int kWarps = 4;              // independent warps per CTA
 constexpr int kRopeOffStride = 65;     // padded row of the in-group rotation table
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -315,7 +314,9 @@ static __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, in
 //
 // The decode work of a (sequence, KV head) pair is a run of units: first
 // kPassUnits units per 32-token pass over its fp16 sink + window tokens, then
-// one unit per packed group.  Pairs are laid out sequence-major: sequence s
+// one unit per packed group.  (A pass costs about kPassUnits groups' time
+// however few tokens it holds: its query, key and value loads are
+// dependent global round trips.)  Pairs are laid out sequence-major: sequence s
 // starts at unit base[s] = Hkv * (units per head of the sequences before
 // it), the line holds W units in all.  Each warp derives base[] and W from
 // seq_len itself (warp scans), or, for large batches, reads them from a plan
@@ -326,6 +327,19 @@ static __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, in
 #ifndef KVQ_PASS_UNITS
 #define KVQ_PASS_UNITS 4
 #endif
+#ifndef KVQ_DECODE_PREFETCH
+#define KVQ_DECODE_PREFETCH 1
+#endif
+// Ring slots a warp fills before its first group arrives; one more per group
+// consumed, up to the ring size (0: the whole ring at once).  Every warp
+// starts at the same moment, so filling whole rings at once asks HBM for all
+// of them together and a warp's first group waits behind the others' later
+// ones; a shallow start lets every warp's first groups arrive first.  At
+// least 2: the group loop waits on two slots at a time.
+#ifndef KVQ_RING_RAMP
+#define KVQ_RING_RAMP 2
+#endif
+static_assert(KVQ_RING_RAMP == 0 || KVQ_RING_RAMP >= 2, "the group loop consumes two slots at a time");
 constexpr int kPassUnits = KVQ_PASS_UNITS;
 constexpr int kInlinePlanSeqs = 256;  // larger batches use the plan kernel
 
@@ -343,6 +357,11 @@ static __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Spli
   ng = spl.Lq / kG;
   tp = (spl.nsink + spl.r + 31) / 32;
   return kPassUnits * tp + ng;
+}
+
+// L2 prefetch of one line (no register, no wait).
+static __device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // The warp whose unit range holds unit x.
@@ -509,12 +528,35 @@ static __device__ __forceinline__ void rescale_o(float (&o)[8][4], float a_lo, f
 #ifndef KVQ_DECODE_MIN_BLOCKS_GQ4
 #define KVQ_DECODE_MIN_BLOCKS_GQ4 3
 #endif
+// One CTA per SM holding every resident warp, rather than several CTAs of
+// four warps.  Warps of CTAs launched later on an SM are scheduled behind
+// the older ones and finish up to 12 us later; warps of one CTA start as
+// equals (their spread fell to about 3 us).  It helped the million-token
+// context (-4%) but not the 4096-token batch, whose tail comes from the
+// warps that cross pairs, run window passes or merge, so it is off.
+#ifndef KVQ_DECODE_ONE_CTA
+#define KVQ_DECODE_ONE_CTA 0
+#endif
+
+// Launch shape of one instantiation: warps per CTA and CTAs per SM the
+// register budget allows (groups of four warps), warps per CTA capped by
+// the shared memory a CTA may hold.
+template <int BITS, int GQ, bool ROPE, bool KPT, bool SP>
+struct CtaShape {
+  using WS = WarpSmem<BITS, GQ, ROPE, KPT, SP>;
+  static constexpr int kQuads = ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS);
+  static constexpr int kExtra = ROPE ? kG * kRopeOffStride * 8 : 0;  // the in-group rotation table
+  static constexpr int kFit = (232448 - kExtra) / WS::BYTES;         // largest opt-in shared memory
+  static constexpr int W = KVQ_DECODE_ONE_CTA ? (4 * kQuads < kFit ? 4 * kQuads : kFit) : 4;
+  static constexpr int MIN_BLOCKS = KVQ_DECODE_ONE_CTA ? 1 : kQuads;
+  static constexpr int BYTES = W * WS::BYTES + kExtra;
+};
 
 template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
-__global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS))
+__global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, CtaShape<BITS, GQ, ROPE, KPT, SP>::MIN_BLOCKS)
     decode_kernel(DecodeArgs a) {
   using WS = WarpSmem<BITS, GQ, ROPE, KPT, SP>;
-  constexpr int NS = WS::NS, BB = WS::BB;
+  constexpr int NS = WS::NS, BB = WS::BB, kWarps = CtaShape<BITS, GQ, ROPE, KPT, SP>::W;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
@@ -632,6 +674,24 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
     const long long gb = P0 + kPassUnits * tp;
     fg = static_cast<int>(min(max(ua - gb, 0LL), static_cast<long long>(ng)));
     fg_end = static_cast<int>(min(max(ub - gb, 0LL), static_cast<long long>(ng)));
+#if KVQ_DECODE_PREFETCH
+    // warm L2 with the rows the consumer reads directly when it reaches this
+    // pair (several groups from now): the query rows, and the sink and
+    // window rows of the passes whose first unit is in this warp's range
+    if (u > 0 && P0 < ub) {
+      const char *qp = reinterpret_cast<const char *>(a.q + (static_cast<size_t>(fs) * a.Hq + static_cast<size_t>(fh) * GQ) * kD);
+      if (lane < 2 * GQ) prefetch_l2(qp + 128 * lane);
+      const int T = spl.nsink + spl.r;
+      const size_t sh = static_cast<size_t>(fs) * H + fh;
+      for (int i = lane; i < 4 * T; i += 32) {  // token i / 4: K or V row, first or second 128 bytes
+        const int t = i >> 2;
+        if (P0 + kPassUnits * (t >> 5) < ua) continue;
+        const __half *row = t < spl.nsink ? ((i & 2) ? geo.v_sink : geo.k_sink) + (sh * geo.ns + t) * kD
+                                          : ((i & 2) ? geo.v_res : geo.k_res) + (sh * geo.R + (t - spl.nsink)) * kD;
+        prefetch_l2(reinterpret_cast<const char *>(row) + 128 * (i & 1));
+      }
+    }
+#endif
     if (PAGED && fg < fg_end) {  // check this range's table entries once
       const int *te = geo.table + (static_cast<size_t>(fs) * H + fh) * geo.max_groups;
       bool bad = false;
@@ -663,7 +723,9 @@ __global__ void __launch_bounds__(kWarps * 32, ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_
   if (!fetch_pair()) fdone = true;
   if (!fdone && fg >= fg_end) fetch_next_pair();
   auto top_up = [&]() {
-    while (!fdone && fseq - cseq < static_cast<uint32_t>(NS)) {
+    const uint32_t depth = KVQ_RING_RAMP ? min(static_cast<uint32_t>(NS), cseq + KVQ_RING_RAMP)
+                                         : static_cast<uint32_t>(NS);
+    while (!fdone && fseq - cseq < depth) {
       if (lane == 0) {
         const uint32_t slot = fseq % NS;
         // paged: an entry outside the pool reads pool block 0 (reported when
@@ -1273,8 +1335,7 @@ cudaError_t launch_sparse_paged(const DecodeArgs &a, int gq, cudaStream_t stream
 // device's SM count (cached per device ordinal).
 template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
-  using WS = WarpSmem<BITS, GQ, ROPE, KPT, SP>;
-  constexpr int bytes = kWarps * WS::BYTES + (ROPE ? kG * kRopeOffStride * 8 : 0);
+  constexpr int bytes = CtaShape<BITS, GQ, ROPE, KPT, SP>::BYTES, kWarps = CtaShape<BITS, GQ, ROPE, KPT, SP>::W;
   auto kern = decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT, SP>;
   static int resident[64] = {};
   static int sms[64] = {};
@@ -1304,6 +1365,7 @@ static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
 // (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
 template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
+  constexpr int kWarps = CtaShape<BITS, GQ, ROPE, KPT, SP>::W;
   int per_sm = 0, n_sm = 0, bytes = 0;
   cudaError_t e = kernel_slots<BITS, GQ, ROPE, KPT, PAGED, ROT, SP>(per_sm, n_sm, bytes);
   if (e != cudaSuccess) return e;
