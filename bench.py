@@ -406,31 +406,34 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, max_len, lens0, w
     """The same steps through the same C ABI, with every step's inputs (new K/V
     token and query of every layer) copied from pinned host memory and every
     output copied back to pinned host memory inside the timed region, and the
-    host waiting for each step's outputs before the next.  As a serving loop
-    would, the step's calls are captured once in a CUDA graph and replayed:
-    the graph holds the host-to-device copies, every layer's kv_quant_append
-    and kv_decode_attn and the device-to-host copies, so every replay moves
-    that step's bytes.  The same steps issued eagerly from Python are timed
-    too (eager_value).  The caches continue from their current state (one
-    more token per step)."""
+    host waiting for each step's outputs before the next.  A step's inputs
+    arrive together: they are staged in one pinned host buffer per kind and
+    copied in one transfer each; the per-layer calls take views of the
+    device copies, and all layers' outputs go back in one transfer.  As a
+    serving loop would, the step's calls are captured once in a CUDA graph
+    and replayed: the graph holds the copies in, every layer's
+    kv_quant_append and kv_decode_attn and the copy out, so every replay
+    moves that step's bytes.  The same steps issued eagerly from Python are
+    timed too (eager_value).  The caches continue from their current state
+    (one more token per step)."""
     pool = len(k_new)
-    h_k = [[(k.cpu().pin_memory(), v.cpu().pin_memory()) for (k, v) in row] for row in k_new]
-    h_q = [[q.cpu().pin_memory() for q in row] for row in qs]
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    d_k = [torch.empty_like(k_new[0][0][0]) for _ in range(layers)]
-    d_v = [torch.empty_like(k_new[0][0][1]) for _ in range(layers)]
-    d_q = [torch.empty_like(qs[0][0]) for _ in range(layers)]
-    h2d = sum(2 * d_k[l].numel() * 2 + d_q[l].numel() * 2 for l in range(layers))
-    d2h = sum(outs[l].numel() * 2 for l in range(layers))
+    h_kv = [torch.stack([torch.stack([k_new[p][l][j] for l in range(layers)]) for j in range(2)]).cpu().pin_memory()
+            for p in range(pool)]                                   # [2][layers][S][Hkv][1][D]
+    h_q = [torch.stack([qs[p][l] for l in range(layers)]).cpu().pin_memory() for p in range(pool)]
+    d_kv = torch.empty(h_kv[0].shape, dtype=h_kv[0].dtype, device=device)
+    d_q = torch.empty(h_q[0].shape, dtype=h_q[0].dtype, device=device)
+    d_out = torch.empty((layers,) + tuple(outs[0].shape), dtype=outs[0].dtype, device=device)
+    h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
+    h2d = (d_kv.numel() + d_q.numel()) * 2
+    d2h = d_out.numel() * 2
 
     def step_calls(p):
+        d_kv.copy_(h_kv[p], non_blocking=True)
+        d_q.copy_(h_q[p], non_blocking=True)
         for l in range(layers):
-            d_k[l].copy_(h_k[p][l][0], non_blocking=True)
-            d_v[l].copy_(h_k[p][l][1], non_blocking=True)
-            d_q[l].copy_(h_q[p][l], non_blocking=True)
-            kvq.kv_quant_append(caches[l], d_k[l], d_v[l], ones, 1)
-            kvq.kv_decode_attn(caches[l], d_q[l], outs[l], ws, max_len)
-            h_out[l].copy_(outs[l], non_blocking=True)
+            kvq.kv_quant_append(caches[l], d_kv[0, l], d_kv[1, l], ones, 1)
+            kvq.kv_decode_attn(caches[l], d_q[l], d_out[l], ws, max_len)
+        h_out.copy_(d_out, non_blocking=True)
 
     def timed(run_step, n, state):
         barrier(world)
