@@ -478,6 +478,42 @@ def test_split_sizes_agree(kvq, warps):
         kvq.set_decode_warps(0)
 
 
+@pytest.mark.parametrize("variant", ["rotation", "outliers", "outliers_kpt", "paged_rotation", "paged_outliers"])
+@pytest.mark.parametrize("warps", [1, 7, 64, 2560])
+def test_split_sizes_agree_variants(kvq, variant, warps):
+    """The kernels for rotated tokens, dense-and-sparse blocks and paged
+    caches carry per-warp state across pairs (the query rotated in place,
+    outlier corrections zeroed by their readers, the table check): their
+    answers must not depend on the warp ranges either, with one warp
+    crossing every pair, ranges ending inside passes and groups, and empty
+    ranges."""
+    S, H, T = 3, 2, 700
+    k, v = _spiky_kv(S, H, T, seed=150)
+    rot = "rotation" in variant
+    sp = "outliers" in variant
+    kpt = variant.endswith("kpt")
+    nb = S * H * 24 + 7 if variant.startswith("paged") else None
+    cache, orc = _build(kvq, S, H, T + 8, 2, ns=1, kpt=kpt, num_blocks=nb, rot=rot, sp=sp)
+    if nb:
+        perm = np.random.default_rng(3).permutation(nb)[:S * H * cache.max_groups].astype(np.int32)
+        cache.block_table.copy_(torch.from_numpy(perm.reshape(S, H, cache.max_groups)).cuda())
+    _append(kvq, cache, orc, k, v, [T, T - 211, 333])
+    q = _rand_q(S, 4 * H, seed=9)
+    want = orc.attention(q)
+    dq = torch.from_numpy(q).cuda()
+    ws = kvq.alloc_workspace(cache, q.shape[1], T)
+    try:
+        kvq.set_decode_warps(warps)
+        for _ in range(2):  # the second call reuses the workspace's self-cleaning counters
+            out = torch.empty_like(dq)
+            kvq.kv_decode_attn(cache, dq, out, ws, T)
+            torch.cuda.synchronize()
+            _attn_close(out.cpu().numpy(), want)
+    finally:
+        kvq.set_decode_warps(0)
+    assert int(cache.status.item()) == 0
+
+
 @pytest.mark.parametrize("S", [200, 300])
 def test_many_sequences_with_empty_and_overlong(kvq, S):
     """Batches planned inside the decode kernel (S <= 256) and by the plan
