@@ -16,7 +16,11 @@
  *   - optionally keys stored before RoPE with RoPE applied after
  *     dequantization, and the first token kept in fp16 as an attention sink
  *     ("KV cache quantization", "Keys are harder than values" and "What they
- *     report").
+ *     report");
+ *   - options of the cache descriptor below: keys grouped per token (the
+ *     baseline KIVI compares against), per-vector dense-and-sparse outlier
+ *     entries (KVQuant), a Walsh-Hadamard rotation of every token before it
+ *     is quantized, and a block-paged layout of the group blocks.
  *
  * Conventions shared by every entry point:
  *   - All buffer pointers are DEVICE pointers owned by the caller.  The
@@ -245,9 +249,12 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  * window, then packed groups -- is cut into equal contiguous ranges, one per
  * warp; the kernel dequantizes in registers, forms scores, runs an online
  * softmax over each range, and the last range of a pair to finish merges its
- * partials (log-sum-exp).  Enqueues the decode kernel, plus a plan kernel
- * (work prefix over the sequences) when S > 256 and a RoPE table kernel when
- * pre_rope.
+ * partials (log-sum-exp).  Every option of the descriptor is honoured:
+ * per-token key scales, outlier entries (each adds q . (x - min) to its
+ * token's score, or p (x - min) to its channel's output), the rotation
+ * (groups scored with H q, their value sum rotated back), and the block
+ * table.  Enqueues the decode kernel, plus a plan kernel (work prefix over
+ * the sequences) when S > 256 and a RoPE table kernel when pre_rope.
  */
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    const uint16_t *q, float softmax_scale, uint16_t *out,
@@ -291,8 +298,12 @@ int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_heads,
  *   k_out, v_out  [S][Hkv][capacity][D] fp32.  For every stored position p <
  *                 seq_len[s]: sink and window tokens are converted exactly,
  *                 quantized tokens are code * scale + min (one fused
- *                 multiply-add in fp32); keys are pre-RoPE.  Positions at or
- *                 past seq_len are not written.
+ *                 multiply-add in fp32), an outlier entry's position its fp16
+ *                 value, and with the rotation the group rows are rotated
+ *                 back (H y_hat in fp32); keys are pre-RoPE.  Positions at or
+ *                 past seq_len are not written.  Through a block table, a
+ *                 group whose entry lies outside the pool is not written and
+ *                 sets KVQ_STATUS_BAD_BLOCK.
  */
 int kv_dequant(const kvq_cache *cache, float *k_out, float *v_out, void *stream);
 
