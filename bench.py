@@ -548,14 +548,30 @@ def host_cores():
 
 
 def host_cpu_model():
+    """The host CPU's model name: lscpu's, else /proc/cpuinfo's (Arm cores
+    report an implementer and a part number there instead of a name)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    arm_parts = {"0xd0c": "Neoverse N1", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2", "0xd4f": "Neoverse V2",
+                 "0xd8e": "Neoverse N3", "0xd84": "Neoverse V3"}
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware"):
-                    return line.split(":", 1)[1].strip()
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
     except OSError:
         pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        return arm_parts.get(fields["cpu part"], f"Arm core, part {fields['cpu part']}")
     import platform
     return platform.processor() or platform.machine()
 
