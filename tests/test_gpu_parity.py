@@ -146,6 +146,46 @@ def test_boundary_sweep(kvq, bits, ns, pre_rope):
         assert np.isnan(Kg[s, :, L:]).all()
 
 
+@pytest.mark.parametrize("option", ["key_per_token", "rotation", "outliers", "rotation_kpt", "outliers_kpt"])
+@pytest.mark.parametrize("ns", [0, 1])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_boundary_sweep_options(kvq, bits, ns, option):
+    """The same lengths around every group and window boundary with each
+    option of the descriptor: blocks byte for byte, attention, and the
+    dequantized rows (within one fp32 ulp, outliers exact; with the rotation
+    within the back-rotation's 2^-20 ||x_hat|| per row).  Values get the
+    x30 spikes only with the options built for them (outlier entries, the
+    rotation's two-part value weights): otherwise a value token whose range
+    a spike stretches far beyond its other entries loses about 2^-12 of
+    code * scale in the fp16 value weight, more than the tolerance once the
+    min cancels most of it."""
+    S, H, gq = len(LENS), 2, 2
+    T = max(LENS)
+    kpt = option == "key_per_token" or option.endswith("kpt")
+    rot, sp = option.startswith("rotation"), option.startswith("outliers")
+    k, v = _spiky_kv(S, H, T, seed=170 + bits + 10 * ns)
+    if not (rot or sp):
+        v = _rand_kv(S, H, T, seed=170 + bits + 10 * ns)[1]
+    cache, orc = _build(kvq, S, H, 300, bits, ns=ns, kpt=kpt, rot=rot, sp=sp)
+    _append(kvq, cache, orc, k, v, LENS)
+    _compare_state(cache, orc)
+    q = _rand_q(S, H * gq, seed=8)
+    _attn_close(_attend(kvq, cache, q, T), orc.attention(q))
+    K = torch.full((S, H, 300, 128), float("nan"), device="cuda")
+    V = torch.full_like(K, float("nan"))
+    kvq.kv_dequant(cache, K, V)
+    Ko, Vo = orc.dequant_all()
+    Kg, Vg = K.cpu().numpy().astype(np.float64), V.cpu().numpy().astype(np.float64)
+    for s, L in enumerate(LENS):
+        for got, want in ((Kg[s, :, :L], Ko[s, :, :L]), (Vg[s, :, :L], Vo[s, :, :L])):
+            if rot:
+                tol = 2.0 ** -20 * np.linalg.norm(want, axis=-1, keepdims=True)
+                assert (np.abs(got - want) <= tol).all()
+            else:
+                np.testing.assert_array_max_ulp(got.astype(np.float32), want.astype(np.float32), maxulp=1)
+        assert np.isnan(Kg[s, :, L:]).all()
+
+
 @pytest.mark.parametrize("gq", [1, 2, 4])
 @pytest.mark.parametrize("bits", [2, 4])
 def test_gqa_group_sizes(kvq, gq, bits):
