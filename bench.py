@@ -115,7 +115,7 @@ def decode_bytes(lengths, w):
     group block (K/V codes + fp32 metadata) once, every fp16 sink/window
     token (K and V) once, the query and the output."""
     from bit_kv_cache_02_gb300.kvq import block_bytes
-    bb = block_bytes(w.bits, key_per_token=w.key_per_token, outliers=w.outliers)
+    bb = block_bytes(w.bits, key_per_token=w.key_per_token, outliers=w.dense_sparse)
     total = 0
     for L in lengths:
         ns = min(L, w.num_sink)
@@ -246,7 +246,7 @@ def prefill_bytes(lengths, w):
     write their share of the packed blocks; window and sink tokens are read
     and written as fp16."""
     from bit_kv_cache_02_gb300.kvq import block_bytes
-    bb = block_bytes(w.bits, key_per_token=w.key_per_token, outliers=w.outliers)
+    bb = block_bytes(w.bits, key_per_token=w.key_per_token, outliers=w.dense_sparse)
     total = 0
     for L in lengths:
         L = int(L)
@@ -265,7 +265,7 @@ def build_caches(kvq, w, layers, pre, capacity, device):
     for layer in range(layers):
         c = kvq.KVCache(w.seqs, w.kv_heads, capacity, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
                         pre_rope=w.pre_rope, device=device, key_per_token=w.key_per_token,
-                        paged=w.paged, hadamard=w.hadamard, outliers=w.outliers)
+                        paged=w.paged, hadamard=w.hadamard, outliers=w.dense_sparse)
         if w.paged:
             tbl = synth.block_table(w, layer, w.seqs, w.kv_heads, c.max_groups)
             c.block_table.copy_(torch.from_numpy(tbl).to(device))
@@ -499,7 +499,7 @@ class OracleSample:
         k, v = k.numpy(), v.numpy()
         c = oracle.OracleCache(n, 1, self.ctx + extra, self.w.bits, residual=self.w.residual,
                                num_sink=self.w.num_sink, key_per_token=self.w.key_per_token,
-                               hadamard=self.w.hadamard, outliers=self.w.outliers)
+                               hadamard=self.w.hadamard, outliers=self.w.dense_sparse)
         c.append(k[:, :, :self.ctx], v[:, :, :self.ctx], [self.ctx] * n)
         return ws, k, v, c
 
@@ -643,7 +643,7 @@ def main():
               "key_per_token": w.key_per_token,
               "paged": w.paged,
               "hadamard": w.hadamard,
-              "outliers": w.outliers,
+              "outliers": w.dense_sparse,
               "ragged": bool(w.ragged_min), "parallelism": f"replicas{world}",
               "l2": "inputs larger than L2: each layer's packed cache is streamed once per step"}
 

@@ -82,8 +82,15 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 }
 
 static int g_warps_override = 0;
+static long long g_wait_limit = 0;
 
 int decode_warps_override() { return g_warps_override; }
+
+int set_wait_limit(long long cycles) {
+  if (cycles < 0 || cycles > kWaitLimitCycles) return -1;
+  g_wait_limit = cycles;
+  return 0;
+}
 
 cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t stream) {
   decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
@@ -140,6 +147,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.pass_slot0 = p.pass_slot0;
   a.tail_passes = p.tail_passes;
   a.max_len = max_len;
+  a.wait_limit = g_wait_limit ? g_wait_limit : kWaitLimitCycles;
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
   cudaError_t e = cudaSuccess;

@@ -62,6 +62,7 @@ struct DecodeArgs {
   size_t pass_slot0;        // first partial slot of the window passes
   int tail_passes;          // window/sink passes per (sequence, KV head) at most, 32 tokens each
   int max_len;              // host bound on seq_len the plan was sized for
+  long long wait_limit;     // SM cycles a ring wait may last before it gives up
   const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
   const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
 };
@@ -441,19 +442,22 @@ static __device__ __forceinline__ void key_outliers(const uint8_t *blk, const Qk
 }
 
 // o += values of one group weighted by ps (score layout: token 8*tau + g,
-// head q).  The value mma's B column h carries head h's p_t * scale_t as one
-// fp16 (its rounding error, at most 2^-11 relative per weight, enters the
-// output linearly); o columns 2q and 2q+1 of this lane are heads 2q, 2q+1.
-// LO (rotating caches, at most four query heads): columns 4 + h carry the
-// fp16 rounding remainder of head h's weights, so the weights enter to
-// about 22 bits.  The Walsh-Hadamard transform that turns the rotated value
-// sums back concentrates every token's code part sum_d code * scale into
-// channel 0 (about D times a typical entry), where a single fp16 weight's
-// 2^-12 relative error would otherwise exceed the output tolerance.
-template <int BITS, bool LO>
+// head q).  The value mma's B column h (h < 4) carries head h's weights
+// p_t * scale_t rounded to fp16 and column 4 + h the fp16 rounding
+// remainder, so each weight enters to about 22 bits (the two parts of o are
+// summed when the partial is written; o columns 2q and 2q+1 of this lane
+// are those of B).  One fp16 weight would carry a 2^-12 relative error into
+// code * scale, whose size the min can nearly cancel: a value token whose
+// range one large entry stretches (|min| >> |x|), or the rotated value sums
+// that the Walsh-Hadamard back-transform concentrates into channel 0, would
+// then miss the output tolerance.  Values carry the attention output as a
+// weighted sum in which the few heavily weighted tokens decide the result
+// ("KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache", second
+// paragraph), so their weights must not lose precision.
+template <int BITS>
 static __device__ __forceinline__ void group_values(const uint8_t *blk, const float (&ps)[4], int lane, float (&o)[8][4]) {
   const int q = lane & 3, gcol = lane >> 2;
-  const int src = LO ? (gcol & 3) : gcol;
+  const int src = gcol & 3;
   uint32_t bp[2][2];
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt)
@@ -461,7 +465,7 @@ static __device__ __forceinline__ void group_values(const uint8_t *blk, const fl
     for (int j = 0; j < 2; ++j) {
       const float v0 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q) + src) & 31);
       const float v1 = __shfl_sync(kFull, ps[2 * kt + j], (4 * (2 * q + 1) + src) & 31);
-      bp[kt][j] = LO ? split_part(v0, v1, gcol >= 4 ? 1.f : 0.f) : h2_as_u32(__floats2half2_rn(v0, v1));
+      bp[kt][j] = split_part(v0, v1, gcol >= 4 ? 1.f : 0.f);
     }
   pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
 }
@@ -942,8 +946,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           for (int gi = g_lo; gi < g_hi; gi += 2) {
             const bool two = gi + 1 < g_hi;
             const uint32_t sa = cseq % NS, sb = (cseq + 1) % NS;
-            if (!mbar_wait_bounded(&full[sa], (cseq / NS) & 1) ||
-                (two && !mbar_wait_bounded(&full[sb], ((cseq + 1) / NS) & 1))) {
+            if (!mbar_wait_bounded(&full[sa], (cseq / NS) & 1, a.wait_limit) ||
+                (two && !mbar_wait_bounded(&full[sb], ((cseq + 1) / NS) & 1, a.wait_limit))) {
               ok = false;
               break;
             }
@@ -1063,8 +1067,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
                 }
               }
             }
-            group_values<BITS, ROT>(ba, psa, lane, o);
-            if (two) group_values<BITS, ROT>(bb, psb, lane, o);
+            group_values<BITS>(ba, psa, lane, o);
+            if (two) group_values<BITS>(bb, psb, lane, o);
             __syncwarp();
             cseq += two ? 2 : 1;
             top_up();
@@ -1085,7 +1089,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           for (int hh = 0; hh < GQ; ++hh) m_all[hh] = -INFINITY;
           for (int gi = g_lo; gi < g_hi; ++gi) {
             const uint32_t slot = cseq % NS;
-            if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1)) {
+            if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1, a.wait_limit)) {
               ok = false;
               break;
             }
@@ -1187,6 +1191,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
             mu_run = fmaf(mu_run, alpha_q, g == 0 ? mus_q : 0.f);
             m_run = m_q;
             rescale_o(o, a_lo, a_hi);
+            // B column g: head g & 3's weights, fp16 high parts in columns
+            // 0..3 and rounding remainders in 4..7 (as group_values)
             uint32_t bp[2][2];
 #pragma unroll
             for (int kt = 0; kt < 2; ++kt)
@@ -1197,12 +1203,12 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
                 for (int hh = 0; hh < GQ; ++hh) {
                   const float a0 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q);
                   const float a1 = __shfl_sync(kFull, ps[hh], 16 * kt + 8 * j + 2 * q + 1);
-                  if (hh == g) {
+                  if (hh == (g & 3)) {
                     v0 = a0;
                     v1 = a1;
                   }
                 }
-                bp[kt][j] = h2_as_u32(__floats2half2_rn(v0, v1));
+                bp[kt][j] = split_part(v0, v1, g >= 4 ? 1.f : 0.f);
               }
             pv_mma<BITS>(blk + off_vc(BITS), lane, bp, o);
             __syncwarp();
@@ -1220,15 +1226,13 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
       }
       const size_t slot = static_cast<size_t>(gw) + pair;
       const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
-      // (a rotating cache leaves this partial in the rotated value domain;
-      // the merge rotates the groups' sum back.  Its weights' low parts
-      // sit in columns 4 .. 7, two lanes up: fold them in.)
-      if (ROT) {
+      // the value weights' low parts sit in columns 4 .. 7, two lanes up:
+      // fold them in.  (A rotating cache leaves this partial in the rotated
+      // value domain; the merge rotates the groups' sum back.)
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
+      for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_down_sync(kFull, o[mt][i], 2);
-      }
+        for (int i = 0; i < 4; ++i) o[mt][i] += __shfl_down_sync(kFull, o[mt][i], 2);
       if (SP) __syncwarp();  // every value correction of the range is in
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -1309,7 +1313,9 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
   }
   if (!ok) {
     set_status(geo.status, KVQ_STATUS_TIMEOUT);
-    // let this warp's copies still in flight land before it exits
+    // let this warp's copies still in flight land before it exits: they read
+    // valid cache blocks, so they complete; the wait keeps its own default
+    // bound (about two seconds) whatever limit gave up above
     for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
   }
 }

@@ -146,13 +146,24 @@ __device__ inline bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`, giving up after about two seconds of SM
-// clock; returns false (and the caller records KVQ_STATUS_TIMEOUT) on timeout.
-__device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// SM clock cycles a pipeline wait may last before it gives up (about two
+// seconds), and the longest suspension one poll of it may ask for.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+#ifndef KVQ_WAIT_HINT_NS
+#define KVQ_WAIT_HINT_NS 100000u
+#endif
+
+// Wait for phase `parity` of `bar`, giving up once `limit` SM clock cycles
+// have passed since the first poll failed; returns false (and the caller
+// records KVQ_STATUS_TIMEOUT) on timeout.  Polls suspend the warp for up to
+// KVQ_WAIT_HINT_NS while the phase is incomplete; with a limit shorter than
+// the default they do not suspend, so the limit holds to within a poll.
+__device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  while (!mbar_try_wait_hint(bar, parity, 100000u)) {
-    if (clock64() - start > 4000000000LL) return false;
+  const uint32_t hint = limit >= kWaitLimitCycles ? KVQ_WAIT_HINT_NS : 0u;
+  while (!mbar_try_wait_hint(bar, parity, hint)) {
+    if (clock64() - start > limit) return false;
   }
   return true;
 }
@@ -227,5 +238,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
 int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
                          uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream);
 int set_decode_warps(int warps);
+// Cycle limit of the decode kernel's pipeline waits (0: the default).
+int set_wait_limit(long long cycles);
 
 }  // namespace kvq

@@ -28,7 +28,7 @@ BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN, BUF_BLOCK
 EXPORTED = (
     "kvq_block_bytes", "kvq_max_groups", "kvq_buffer_bytes", "kv_quant_append",
     "kv_decode_workspace_bytes", "kv_decode_attn", "kv_dequant", "kvq_strerror",
-    "kvq_launch_count", "kvq_set_decode_warps", "kv_decode_attn_noalloc",
+    "kvq_launch_count", "kvq_set_decode_warps", "kv_decode_attn_noalloc", "kvq_set_wait_limit_cycles",
 )
 
 
@@ -63,6 +63,7 @@ def _load():
         "kvq_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvq_launch_count": (c_uint64, []),
         "kvq_set_decode_warps": (ctypes.c_int, [c_int32]),
+        "kvq_set_wait_limit_cycles": (ctypes.c_int, [c_int64]),
         "kv_decode_attn_noalloc": (ctypes.c_int, [P, c_int32, c_void_p, c_float, c_void_p, c_int32, c_void_p]),
     }
     for name, (res, args) in sig.items():
@@ -230,3 +231,9 @@ def launch_count() -> int:
 def set_decode_warps(warps: int):
     """Warps a decode launch cuts its work into (0: every resident warp)."""
     _check(lib.kvq_set_decode_warps(warps), "kvq_set_decode_warps")
+
+
+def set_wait_limit_cycles(cycles: int):
+    """Cycle limit of the decode kernel's pipeline waits (0: the default of
+    about two seconds); a test aid for the timeout path."""
+    _check(lib.kvq_set_wait_limit_cycles(int(cycles)), "kvq_set_wait_limit_cycles")

@@ -31,20 +31,21 @@ class Workload:
     num_sink: int = 0
     pre_rope: bool = False
     residual: int = 128
-    outliers: tuple = ()     # fixed channels (same for every head) ...
-    n_outliers: int = 4      # ... or this many drawn per (layer, KV head)
+    outlier_channels_fixed: tuple = ()  # key channels scaled up, the same for every head ...
+    n_outliers: int = 4      # ... or, when empty, this many drawn per (layer, KV head)
     outlier_mult: float = 15.0
     seed: int = 0
     decode_tokens: int = 1   # tokens appended before attending
     key_per_token: bool = False  # keys grouped per token (the ablation of per-channel keys)
     paged: bool = False      # group blocks in a shared pool behind a shuffled block table
     hadamard: bool = False   # tokens Walsh-Hadamard rotated before quantization
-    outliers: bool = False   # dense-and-sparse blocks (each slice's largest element kept in fp16)
+    dense_sparse: bool = False  # dense-and-sparse blocks (each slice's largest element kept in fp16)
     extra: dict = field(default_factory=dict)
 
 
 WORKLOADS = {
-    "tiny": Workload("tiny", 1, 1, 1, 1, 256, 2, outliers=(3, 17, 64, 101), outlier_mult=20.0,
+    "tiny": Workload("tiny", 1, 1, 1, 1, 256, 2, outlier_channels_fixed=(3, 17, 64, 101),
+                     outlier_mult=20.0,
                      decode_tokens=0),
     "llama2_7b_mha": Workload("llama2_7b_mha", 32, 16, 32, 32, 4096, 2),
     "llama3_8b_gqa_2bit": Workload("llama3_8b_gqa_2bit", 32, 64, 32, 8, 8192, 2, ragged_min=1024),
@@ -61,7 +62,8 @@ WORKLOADS = {
     "llama2_7b_mha_key_per_token_hadamard": Workload("llama2_7b_mha_key_per_token_hadamard", 32, 16, 32, 32,
                                                      4096, 2, key_per_token=True, hadamard=True),
     # the Llama-2 shape with dense-and-sparse blocks
-    "llama2_7b_mha_outliers": Workload("llama2_7b_mha_outliers", 32, 16, 32, 32, 4096, 2, outliers=True),
+    "llama2_7b_mha_outliers": Workload("llama2_7b_mha_outliers", 32, 16, 32, 32, 4096, 2,
+                                       dense_sparse=True),
 }
 
 
@@ -83,8 +85,8 @@ def block_table(w: Workload, layer: int, seqs: int, heads: int, max_groups: int)
 
 def outlier_channels(w: Workload, layer: int) -> np.ndarray:
     """[kv_heads][n] key channels scaled by outlier_mult in this layer."""
-    if w.outliers:
-        return np.tile(np.array(w.outliers, np.int64), (w.kv_heads, 1))
+    if w.outlier_channels_fixed:
+        return np.tile(np.array(w.outlier_channels_fixed, np.int64), (w.kv_heads, 1))
     rng = np.random.default_rng([w.seed, 11, layer])
     return np.stack([rng.choice(HEAD_DIM, w.n_outliers, replace=False) for _ in range(w.kv_heads)])
 

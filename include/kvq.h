@@ -161,7 +161,9 @@ typedef struct kvq_cache {
   int32_t  *block_table;   /* NULL: contiguous blocks                    */
 } kvq_cache;
 
-/* Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128 with
+/* Sizing helpers (plumbing of this library; the pages define no interface).
+ *
+ * Bytes of one group block (3328 at 2-bit, 5376 at 4-bit for D = 128 with
  * per-channel keys; 2560 / 4608 with per-token keys; plus 4 * (D + 32), or
  * 4 * 64 with per-token keys, for dense-and-sparse blocks); 0 for an
  * unsupported (bits, head_dim) or a flag other than 0 / 1. */
@@ -208,7 +210,8 @@ int kv_quant_append(const kvq_cache *cache, const uint16_t *k_new,
                     int32_t max_new, void *stream);
 
 /*
- * kv_decode_workspace_bytes -- scratch size for kv_decode_attn.
+ * kv_decode_workspace_bytes -- scratch size for kv_decode_attn (plumbing of
+ * this library's split-K schedule; not on the pages).
  *
  *   num_q_heads  query heads (a multiple of num_kv_heads, ratio 1, 2 or 4).
  *   max_len      host bound on every seq_len at the time of the call
@@ -272,16 +275,19 @@ int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
  * memory budget), and paths where a cudaMalloc is not allowed because it can
  * synchronize the device.
  *
- * Same arguments and results as kv_decode_attn, minus the workspace.  The
- * scratch is a 16 MiB array compiled into this library (every GPU that loads
- * the library keeps it until the process exits).  A call whose
+ * Same arguments and results as kv_decode_attn, minus the workspace: the
+ * arguments are checked first and give the same error codes.  The scratch
+ * is a 16 MiB array compiled into this library (every GPU that loads the
+ * library keeps it until the process exits).  A valid call whose
  * kv_decode_workspace_bytes(cache, num_q_heads, max_len) exceeds 16 MiB
  * returns KVQ_ERR_WORKSPACE and enqueues nothing.  Nothing is allocated: no
  * cudaMalloc, no cudaFree, no allocating library call.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any
- * stream capture.  All calls on a device share the one array and it keeps
+ * Every call looks up the array's device address in the current device's
+ * context (nothing is cached, so a cudaDeviceReset in between is harmless).
+ * The first lookup on a device loads the array's module there: make the
+ * first call on each device before any stream capture.  All calls on a
+ * device share the one array and it keeps
  * the previous call's contents (each call clears the part that must start
  * at zero, on its own stream, before using it): calls
  * whose work overlaps on the GPU (different streams, or different host
@@ -295,6 +301,11 @@ int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_heads,
 /*
  * kv_dequant -- test aid: write the dequantized cache.
  *
+ * Source: "KV cache quantization", "What they report" (asymmetric
+ * quantization: a value is rebuilt as code * scale + min from its slice's
+ * scale and minimum); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for
+ * KV Cache", second paragraph (which slice a key or value code belongs to).
+ *
  *   k_out, v_out  [S][Hkv][capacity][D] fp32.  For every stored position p <
  *                 seq_len[s]: sink and window tokens are converted exactly,
  *                 quantized tokens are code * scale + min (one fused
@@ -307,7 +318,8 @@ int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_heads,
  */
 int kv_dequant(const kvq_cache *cache, float *k_out, float *v_out, void *stream);
 
-/* Message for a KVQ_ERR_* code (static storage). */
+/* Message for a KVQ_ERR_* code (static storage).  Plumbing; not on the
+ * pages, like the two calls below. */
 const char *kvq_strerror(int err);
 
 /* Number of kernels this library has launched in this process (for
@@ -320,6 +332,16 @@ uint64_t kvq_launch_count(void);
  * workspace size does not depend on it.  Returns KVQ_OK or
  * KVQ_ERR_INVALID_ARG. */
 int kvq_set_decode_warps(int32_t warps);
+
+/* Test aid (not on the pages): SM clock cycles a pipeline wait of the decode
+ * kernel may last before it gives up, records KVQ_STATUS_TIMEOUT, lets its
+ * own copies in flight land (those waits keep the default bound) and ends its
+ * work; 0 restores the default of about two seconds (4e9 cycles).  A small
+ * limit makes the waits give up whenever data is not there yet, which is how
+ * tests exercise the timeout path without a fault.  Affects kv_decode_attn
+ * calls made afterwards in this process.  Returns KVQ_OK, or
+ * KVQ_ERR_INVALID_ARG for a negative value or one above the default. */
+int kvq_set_wait_limit_cycles(int64_t cycles);
 
 #ifdef __cplusplus
 }

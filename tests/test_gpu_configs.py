@@ -37,7 +37,7 @@ def _run(kvq, name, pairs):
     cap = T + 8
     cache = kvq.KVCache(w.seqs, w.kv_heads, cap, bits=w.bits, residual=w.residual, num_sink=w.num_sink,
                         pre_rope=w.pre_rope, device=dev, key_per_token=w.key_per_token, paged=w.paged,
-                        hadamard=w.hadamard, outliers=w.outliers)
+                        hadamard=w.hadamard, outliers=w.dense_sparse)
     if w.paged:
         tbl = synth.block_table(w, 0, w.seqs, w.kv_heads, cache.max_groups)
         cache.block_table.copy_(torch.from_numpy(tbl).to(dev))
@@ -61,7 +61,7 @@ def _run(kvq, name, pairs):
         L = int(lens[s])
         orc = oracle.OracleCache(1, 1, cap, w.bits, residual=w.residual, num_sink=w.num_sink,
                                  key_per_token=w.key_per_token, hadamard=w.hadamard,
-                                 outliers=w.outliers)
+                                 outliers=w.dense_sparse)
         ks = k[s:s + 1, h:h + 1, :L].cpu().numpy()
         vs = v[s:s + 1, h:h + 1, :L].cpu().numpy()
         orc.append(ks, vs, [L])
@@ -106,8 +106,10 @@ def test_kvquant_prerope_sink(kvq):
 
 
 def test_long_context_1m(kvq):
-    """One sequence x 32 heads, 2^20 context tokens (+1), split-K decode."""
-    _run(kvq, "long_1m", [(0, 13)])
+    """One sequence x 32 heads, 2^20 context tokens (+1), split-K decode: the
+    first and last pairs on the work line (whose range and merge edges
+    differ) and one between."""
+    _run(kvq, "long_1m", [(0, 0), (0, 13), (0, 31)])
 
 
 @pytest.mark.parametrize("name", ["llama2_7b_mha_key_per_token", "llama2_7b_mha_paged", "llama2_7b_mha_hadamard",

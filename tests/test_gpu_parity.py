@@ -122,13 +122,21 @@ def test_tiny_full(kvq):
 LENS = [1, 2, 31, 32, 33, 127, 128, 129, 255, 256, 257]
 
 
+@pytest.mark.parametrize("spiky", [False, True])
 @pytest.mark.parametrize("pre_rope", [False, True])
 @pytest.mark.parametrize("ns", [0, 1])
 @pytest.mark.parametrize("bits", [2, 4])
-def test_boundary_sweep(kvq, bits, ns, pre_rope):
+def test_boundary_sweep(kvq, bits, ns, pre_rope, spiky):
+    """Lengths around every group and window boundary, plain caches (keys
+    per channel, post- or pre-RoPE): blocks byte for byte, attention,
+    dequantized rows within one fp32 ulp.  The spiky inputs add random x30
+    entries, ties and constant rows to keys and values: a value token whose
+    range a spike stretches has |min| >> |x|, where code * scale and the min
+    nearly cancel, so its attention weight must keep its precision."""
     S, H, gq = len(LENS), 2, 2
     T = max(LENS)
-    k, v = _rand_kv(S, H, T, seed=100 + bits + 10 * ns)
+    seed = 100 + bits + 10 * ns
+    k, v = _spiky_kv(S, H, T, seed) if spiky else _rand_kv(S, H, T, seed)
     cache, orc = _build(kvq, S, H, 300, bits, ns=ns, pre_rope=pre_rope)
     _append(kvq, cache, orc, k, v, LENS)
     _compare_state(cache, orc)
@@ -153,19 +161,13 @@ def test_boundary_sweep_options(kvq, bits, ns, option):
     """The same lengths around every group and window boundary with each
     option of the descriptor: blocks byte for byte, attention, and the
     dequantized rows (within one fp32 ulp, outliers exact; with the rotation
-    within the back-rotation's 2^-20 ||x_hat|| per row).  Values get the
-    x30 spikes only with the options built for them (outlier entries, the
-    rotation's two-part value weights): otherwise a value token whose range
-    a spike stretches far beyond its other entries loses about 2^-12 of
-    code * scale in the fp16 value weight, more than the tolerance once the
-    min cancels most of it."""
+    within the back-rotation's 2^-20 ||x_hat|| per row).  Keys and values
+    carry random x30 spikes, ties and constant rows with every option."""
     S, H, gq = len(LENS), 2, 2
     T = max(LENS)
     kpt = option == "key_per_token" or option.endswith("kpt")
     rot, sp = option.startswith("rotation"), option.startswith("outliers")
     k, v = _spiky_kv(S, H, T, seed=170 + bits + 10 * ns)
-    if not (rot or sp):
-        v = _rand_kv(S, H, T, seed=170 + bits + 10 * ns)[1]
     cache, orc = _build(kvq, S, H, 300, bits, ns=ns, kpt=kpt, rot=rot, sp=sp)
     _append(kvq, cache, orc, k, v, LENS)
     _compare_state(cache, orc)
@@ -498,6 +500,46 @@ def test_workspace_too_small_raises(kvq):
     with pytest.raises(kvq.KvqError) as e:
         kvq.kv_decode_attn(cache, q, torch.empty_like(q), ws, 64)
     assert e.value.code == -4
+
+
+@pytest.mark.parametrize("pre_rope", [False, True])
+def test_wait_timeout_sets_status_and_recovers(kvq, pre_rope):
+    """The decode kernel's ring waits are bounded: with the limit cut to one
+    SM cycle a wait gives up whenever its group has not landed yet, records
+    KVQ_STATUS_TIMEOUT, lets its warp's copies in flight land and ends that
+    warp's work; the call returns and the device stays usable.  After the
+    workspace is zeroed again (a timed-out call leaves merge counters
+    non-zero) and the limit restored, the same call matches the oracle.
+    Nothing faults and nothing hangs: the waits are on copies of valid
+    blocks, which complete."""
+    S, H, T = 8, 4, 3000
+    k, v = _rand_kv(S, H, T, seed=41)
+    cache, orc = _build(kvq, S, H, T + 8, 2, ns=int(pre_rope), pre_rope=pre_rope)
+    _append(kvq, cache, orc, k, v, [T - 97 * s for s in range(S)])
+    q = _rand_q(S, 2 * H, seed=42)
+    dq = torch.from_numpy(q).cuda()
+    out = torch.empty_like(dq)
+    ws = kvq.alloc_workspace(cache, 2 * H, T)
+    seen = 0
+    try:
+        kvq.set_wait_limit_cycles(1)
+        for _ in range(5):          # a call gives up unless every first poll finds its data
+            kvq.kv_decode_attn(cache, dq, out, ws, T)
+            torch.cuda.synchronize()
+            seen = int(cache.status.item())
+            if seen & kvq.KVQ_STATUS_TIMEOUT:
+                break
+            ws.zero_()
+    finally:
+        kvq.set_wait_limit_cycles(0)
+    assert seen & kvq.KVQ_STATUS_TIMEOUT, f"no wait gave up (status {seen})"
+    assert seen == kvq.KVQ_STATUS_TIMEOUT
+    cache.status.zero_()
+    ws.zero_()
+    kvq.kv_decode_attn(cache, dq, out, ws, T)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    _attn_close(out.cpu().numpy(), orc.attention(q, pre_rope=pre_rope))
 
 
 @pytest.mark.parametrize("warps", [1, 3, 7, 50, 333, 2560])

@@ -493,15 +493,23 @@ def test_ablation_ordering_on_outlier_keys():
 # ---------------------------------------------------------------- Hadamard
 
 
-def test_hadamard_matrix_is_sylvester_and_orthogonal():
-    """The matrix from its definition equals scipy's Sylvester construction,
-    is symmetric, and H H = D I."""
-    linalg = pytest.importorskip("scipy.linalg")
+def test_hadamard_matrix_is_symmetric_orthogonal_and_recursive():
+    """Without any library: H is symmetric, H H = D I, its entries are +-1,
+    and it follows the Sylvester doubling [[H, H], [H, -H]] from H_1 = [1]."""
     for D in (2, 8, 128):
         H = oracle.hadamard_matrix(D)
-        np.testing.assert_array_equal(H, linalg.hadamard(D).astype(np.float64))
+        assert set(np.unique(H).tolist()) == {-1.0, 1.0}
         np.testing.assert_array_equal(H, H.T)
         np.testing.assert_array_equal(H @ H, D * np.eye(D))
+        h = oracle.hadamard_matrix(D // 2) if D > 2 else np.ones((1, 1))
+        np.testing.assert_array_equal(H, np.block([[h, h], [h, -h]]))
+
+
+def test_hadamard_matrix_is_sylvester():
+    """The matrix from its definition equals scipy's Sylvester construction."""
+    linalg = pytest.importorskip("scipy.linalg")
+    for D in (2, 8, 128):
+        np.testing.assert_array_equal(oracle.hadamard_matrix(D), linalg.hadamard(D).astype(np.float64))
 
 
 def test_hadamard_rotate_exact_on_small_integers():
