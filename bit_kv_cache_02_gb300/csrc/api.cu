@@ -207,7 +207,9 @@ uint64_t kvq_launch_count(void) { return g_launches.load(); }
 
 int kvq_set_decode_warps(int32_t warps) { return kvq::set_decode_warps(warps) ? KVQ_ERR_INVALID_ARG : KVQ_OK; }
 
-int kvq_set_wait_limit_cycles(int64_t cycles) { return kvq::set_wait_limit(cycles) ? KVQ_ERR_INVALID_ARG : KVQ_OK; }
+int kvq_set_wait_test(int64_t limit_cycles, int32_t wait_before_fetch) {
+  return kvq::set_wait_test(limit_cycles, wait_before_fetch) ? KVQ_ERR_INVALID_ARG : KVQ_OK;
+}
 
 }  // extern "C"
 

@@ -83,12 +83,15 @@ __global__ void rope_table_kernel(float2 *base, int n_base, float2 *off, int ns,
 
 static int g_warps_override = 0;
 static long long g_wait_limit = 0;
+static int g_wait_before_fetch = 0;
 
 int decode_warps_override() { return g_warps_override; }
 
-int set_wait_limit(long long cycles) {
-  if (cycles < 0 || cycles > kWaitLimitCycles) return -1;
+int set_wait_test(long long cycles, int wait_before_fetch) {
+  if (cycles < 0 || cycles > kWaitLimitCycles || (wait_before_fetch != 0 && wait_before_fetch != 1)) return -1;
+  if (wait_before_fetch && cycles == 0) return -1;  // a wait that nothing completes needs a short limit
   g_wait_limit = cycles;
+  g_wait_before_fetch = wait_before_fetch;
   return 0;
 }
 
@@ -148,6 +151,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.tail_passes = p.tail_passes;
   a.max_len = max_len;
   a.wait_limit = g_wait_limit ? g_wait_limit : kWaitLimitCycles;
+  a.wait_before_fetch = g_wait_before_fetch;
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
   cudaError_t e = cudaSuccess;

@@ -63,6 +63,7 @@ struct DecodeArgs {
   int tail_passes;          // window/sink passes per (sequence, KV head) at most, 32 tokens each
   int max_len;              // host bound on seq_len the plan was sized for
   long long wait_limit;     // SM cycles a ring wait may last before it gives up
+  int wait_before_fetch;    // test aid: first ring wait before any copy is issued
   const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
   const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
 };
@@ -370,13 +371,33 @@ static __device__ __forceinline__ int owner_warp(long long x, long long W, int N
   return static_cast<int>(((x + 1) * NW - 1) / W);
 }
 
-// Warps with a non-empty unit range that intersect [P0, P1).
-static __device__ __forceinline__ int touching_warps(long long P0, long long P1, long long W, int NW) {
-  const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
-  if (W >= NW) return w1 - w0 + 1;
-  int n = 0;
-  for (int w = w0; w <= w1; ++w) n += (w * W / NW) < ((w + 1) * W / NW);
-  return n;
+// The warps with a non-empty unit range that intersect [P0, P1): n of them,
+// the i-th given by at().  When every range is non-empty (W >= NW) they are
+// the owners of the two ends and every warp between.  Otherwise each range
+// holds at most one unit, so they are the owners of the units of [P0, P1),
+// all distinct; then W < NW <= kMaxDecodeWarps and the owner of a unit takes
+// one 32-bit division (scanning the warp ids between the end owners instead
+// would cost a division per warp of the launch).
+struct Touching {
+  int w0, n, p0, W, NW;
+  bool by_unit;
+  __device__ __forceinline__ int at(int i) const { return by_unit ? ((p0 + i + 1) * NW - 1) / W : w0 + i; }
+};
+static __device__ __forceinline__ Touching touching_warps(long long P0, long long P1, long long W, int NW) {
+  Touching t;
+  t.by_unit = W < NW;
+  t.NW = NW;
+  if (t.by_unit) {
+    t.W = static_cast<int>(W);
+    t.p0 = static_cast<int>(P0);
+    t.w0 = 0;
+    t.n = static_cast<int>(P1 - P0);
+  } else {
+    t.W = t.p0 = 0;
+    t.w0 = owner_warp(P0, W, NW);
+    t.n = owner_warp(P1 - 1, W, NW) - t.w0 + 1;
+  }
+  return t;
 }
 
 // Scores of one packed group for this lane: z[tau] = log2-domain logit of
@@ -724,6 +745,14 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
       if (fg < fg_end) break;
     }
   };
+  if (a.wait_before_fetch) {
+    // test aid: wait on the first ring slot before anything is copied into
+    // it, so that the bounded wait runs out (nothing is in flight to drain)
+    if (!mbar_wait_bounded(&full[0], 0, a.wait_limit)) {
+      if (lane == 0) set_status(geo.status, KVQ_STATUS_TIMEOUT);
+      return;
+    }
+  }
   if (!fetch_pair()) fdone = true;
   if (!fdone && fg >= fg_end) fetch_next_pair();
   auto top_up = [&]() {
@@ -1261,20 +1290,19 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     // 0's acq_rel add publishes this warp's partials (ordered before it by
     // the warp barrier) and observes every other warp's
     __syncwarp();
-    const int expect = tp + touching_warps(P0, P1, W, NW);
+    const Touching tw = touching_warps(P0, P1, W, NW);
+    const int expect = tp + tw.n;
     int last = 0;
     if (lane == 0) last = atom_add_acq_rel(&a.counters[pair], npart) + npart == expect;
     if (__shfl_sync(kFull, last, 0)) {
       __threadfence();
       if (lane == 0) a.counters[pair] = 0;  // ready for the next call
-      const int w0 = owner_warp(P0, W, NW), w1 = owner_warp(P1 - 1, W, NW);
       for (int hh = 0; hh < GQ; ++hh) {
         float M = -INFINITY;
         for (int k = lane; k < tp; k += 32)
           M = fmaxf(M, __ldcg(&a.part_ml[(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k) * GQ + hh]).x);
-        for (int w = w0 + lane; w <= w1; w += 32)
-          if (w * W / NW < (w + 1) * W / NW)
-            M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(w) + pair) * GQ + hh]).x);
+        for (int i = lane; i < tw.n; i += 32)
+          M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(tw.at(i)) + pair) * GQ + hh]).x);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
         float Ls = 0.f;
@@ -1292,8 +1320,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
         if (M != -INFINITY) {
           for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k, acc);
 #pragma unroll 4
-          for (int w = w0; w <= w1; ++w)
-            if (w * W / NW < (w + 1) * W / NW) add(static_cast<size_t>(w) + pair, accg);
+          for (int i = 0; i < tw.n; ++i) add(static_cast<size_t>(tw.at(i)) + pair, accg);
         }
         if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
         acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);

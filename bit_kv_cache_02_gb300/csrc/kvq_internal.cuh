@@ -146,23 +146,40 @@ __device__ inline bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar`.
+__device__ inline bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // SM clock cycles a pipeline wait may last before it gives up (about two
-// seconds), and the longest suspension one poll of it may ask for.
+// seconds).
 constexpr long long kWaitLimitCycles = 4000000000LL;
-#ifndef KVQ_WAIT_HINT_NS
-#define KVQ_WAIT_HINT_NS 100000u
-#endif
 
 // Wait for phase `parity` of `bar`, giving up once `limit` SM clock cycles
-// have passed since the first poll failed; returns false (and the caller
-// records KVQ_STATUS_TIMEOUT) on timeout.  Polls suspend the warp for up to
-// KVQ_WAIT_HINT_NS while the phase is incomplete; with a limit shorter than
-// the default they do not suspend, so the limit holds to within a poll.
+// have passed; returns false (and the caller records KVQ_STATUS_TIMEOUT) on
+// timeout.  At the default limit the polls are try_waits, which suspend the
+// warp while the phase is incomplete (up to a system-dependent time, then up
+// to 100 us per poll); a shorter limit polls without suspending, so it holds
+// to within one poll.
 __device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit = kWaitLimitCycles) {
+  if (limit < kWaitLimitCycles) {
+    const long long start = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+      if (clock64() - start > limit) return false;
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
-  const uint32_t hint = limit >= kWaitLimitCycles ? KVQ_WAIT_HINT_NS : 0u;
-  while (!mbar_try_wait_hint(bar, parity, hint)) {
+  while (!mbar_try_wait_hint(bar, parity, 100000u)) {
     if (clock64() - start > limit) return false;
   }
   return true;
@@ -228,6 +245,14 @@ struct DecodePlan {
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                 int max_new, cudaStream_t stream, uint64_t *launches);
+// The flush of appends longer than the window by warps that each quantize
+// whole key or value tiles (quant_tiles.cu): caches with per-channel keys,
+// no rotation and no outlier entries, of at most kTileFlushMaxSeqs sequences
+// (each warp plans its range from the lengths of all of them).
+constexpr int kTileFlushMaxSeqs = 2048;
+bool flush_tiles_serves(const Geo &geo);
+cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
+                               int max_new, cudaStream_t stream);
 cudaError_t launch_dequant(const Geo &geo, float *k_out, float *v_out, cudaStream_t stream, uint64_t *launches);
 DecodePlan plan_decode(const Geo &geo, int Hq, int max_len);
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
@@ -238,7 +263,8 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
 int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
                          uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream);
 int set_decode_warps(int warps);
-// Cycle limit of the decode kernel's pipeline waits (0: the default).
-int set_wait_limit(long long cycles);
+// Test aid: cycle limit of the decode kernel's pipeline waits (0: the
+// default) and whether each warp's first wait comes before its first copy.
+int set_wait_test(long long cycles, int wait_before_fetch);
 
 }  // namespace kvq

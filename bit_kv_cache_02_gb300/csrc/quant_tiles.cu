@@ -1,0 +1,538 @@
+// Quantize-and-pack of the groups that an append flushes, one tile per warp.
+//
+// Source: "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
+// second paragraph (keys quantized per channel over groups of 32 tokens,
+// values per token, asymmetric min/scale codes) and third paragraph (the
+// window of newest tokens is quantized in blocks when it fills).
+//
+// Each group block is made of two independent halves: the key tile (32
+// tokens x 128 channels, one (scale, min) per channel) and the value tile
+// (one (scale, min) per token).  A warp quantizes one tile at a time, with
+// no synchronization beyond its own lanes: the line of tiles (key tile,
+// value tile, next group, ...) of every (sequence, KV head) is cut into one
+// contiguous range per warp.  The 32 token rows of a tile reach shared memory
+// through one 256-byte bulk copy per lane (rows from the fp16 window or the
+// new tokens alike), into a ring of slots whose rows are padded to 272 bytes
+// so that both read patterns below are free of bank conflicts; the next tiles
+// are in flight while the current one is quantized.
+//
+//   key tile:   lane L owns channels 4L .. 4L+3 of all 32 tokens: their
+//               min/max are lane-local, and the lane packs the codes of its
+//               channels into half-words of the mma-fragment layout.
+//   value tile: lane L owns tokens 2p, 2p+1 (p = L % 16) over channels
+//               64 (L / 16) .. +63: the token statistics take one exchange
+//               with lane L ^ 16, and byte permutes pair the two tokens of a
+//               channel, which the layout places in the two halves of a word.
+//
+// A packed word takes codes from two lanes (the two channel octets j of a
+// 16-channel tile for keys, the two token octets for values); each lane
+// builds its half-words for 16 words (2-bit; 32 at 4-bit), keeps half of
+// them and trades the other half with its partner lane in one shuffle each.
+// Codes use the reciprocal filter with the exact IEEE fallback of
+// quant_common.cuh, so they equal the oracle's bit for bit.  The finished
+// tile (codes, then its scales and mins) is staged in shared memory and
+// written by two bulk copies.
+#include "quant_common.cuh"
+
+namespace kvq {
+
+constexpr int kRowPad = 272;                // bytes per token row in a ring slot (256 + 16)
+constexpr int kSlotBytes = kG * kRowPad;    // 8704
+#ifndef KVQ_TILE_RING
+#define KVQ_TILE_RING 2
+#endif
+
+template <int BITS>
+struct TileSmem {  // one warp's shared memory
+  static constexpr int CT = code_tile_bytes(BITS);  // packed codes of one tile
+  static constexpr int NS = KVQ_TILE_RING;          // ring slots
+  static constexpr int STAGE = NS * kSlotBytes;     // codes, then scales and mins
+  static constexpr int BAR = STAGE + CT + 4 * 2 * kD;
+  static constexpr int BYTES = (BAR + 8 * NS + 127) / 128 * 128;
+  static constexpr int WARPS = 232448 / BYTES < 16 ? 232448 / BYTES : 16;  // warps per CTA (one CTA per SM)
+  static_assert(kSlotBytes % 16 == 0 && STAGE % 16 == 0 && (STAGE + CT) % 16 == 0, "bulk copies need 16 B");
+};
+
+// The flush of sequence s in this append: groups ng starting at stream
+// index Lq0 (0 when the sequence is skipped: its lengths are reported by the
+// tail kernel), the window's first stream index n0 - (n0 % R) = Lq0 and the
+// length L0 before the append.
+struct SeqFlush {
+  int ng, Lq0, n0, L0;
+};
+
+__device__ __forceinline__ SeqFlush seq_flush(const Geo &geo, const int *new_len, int max_new, int s) {
+  SeqFlush f;
+  f.L0 = geo.seq_len[s];
+  const int nn = new_len[s];
+  f.ng = f.Lq0 = f.n0 = 0;
+  if (nn < 0 || nn > max_new || f.L0 < 0 || f.L0 + nn > geo.capacity) return f;
+  f.n0 = max(f.L0 - geo.ns, 0);
+  const int n1 = max(f.L0 + nn - geo.ns, 0);
+  f.Lq0 = f.n0 - f.n0 % geo.R;
+  f.ng = (n1 - n1 % geo.R - f.Lq0) / kG;
+  return f;
+}
+
+// A position on the tile line: sequence s (its flush f), KV head h, group g
+// of the flush, kind 0 (keys) or 1 (values).
+struct TilePos {
+  int s, h, g, kind;
+  SeqFlush f;
+};
+
+// Next tile of the line (skipping sequences with nothing to flush); false
+// past the last sequence.
+__device__ __forceinline__ bool next_tile(TilePos &p, const Geo &geo, const int *new_len, int max_new) {
+  if (p.kind == 0) {
+    p.kind = 1;
+    return true;
+  }
+  p.kind = 0;
+  if (++p.g < p.f.ng) return true;
+  p.g = 0;
+  if (++p.h < geo.H) return true;
+  p.h = 0;
+  while (++p.s < geo.S) {
+    p.f = seq_flush(geo, new_len, max_new, p.s);
+    if (p.f.ng > 0) return true;
+  }
+  return false;
+}
+
+// Codes of NF fp16 pairs into one word: pair f holds the fields e = 0 (low
+// half) and e = 1 (high half) of one slice pair whose reciprocal filter
+// constants are (rcp, c); its codes land at bits pos_f and 16 + pos_f, with
+// sc[f] = 2^pos_f.  Each half accumulates 2^23 + sum code * 2^pos exactly in
+// fp32 and the low 16 bits of both are joined by one byte permute.  Sets
+// `near` when some estimate lies within the filter's tolerance of a rounding
+// boundary (thr = 1/2 - tol): the word is then redone exactly.
+template <int NF>
+__device__ __forceinline__ uint32_t pack_pairs(const uint32_t (&x)[NF], f2x rcp, f2x c, const float (&sc)[NF],
+                                               float thr, bool &near) {
+  const f2x magic = f2_pack(kMagic, kMagic);
+  f2x acc = f2_pack(kPackBase, kPackBase);
+  float emax = 0.f;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x[f]));
+    const f2x y = f2_fma(f2_pack(xf.x, xf.y), rcp, c);
+    const f2x r = f2_sub(f2_add(y, magic), magic);  // rne(y), exact
+    const float2 e = f2_unpack(f2_sub(y, r));
+    emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
+    acc = f2_fma(r, f2_pack(sc[f], sc[f]), acc);
+  }
+  near = emax > thr;
+  const float2 a = f2_unpack(acc);
+  return __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x5410);
+}
+
+// The same word by the IEEE subtract and divide of every code (when the
+// filter cannot decide one of them; rare, out of line).
+template <int BITS, int NF>
+__device__ __noinline__ uint32_t pack_pairs_exact(const uint32_t (&x)[NF], float lo0, float sc0, float lo1, float sc1,
+                                                  const int (&pos)[NF]) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x[f]));
+    w |= exact_code<BITS>(xf.x, lo0, sc0) << pos[f];
+    w |= exact_code<BITS>(xf.y, lo1, sc1) << (16 + pos[f]);
+  }
+  return w;
+}
+
+// Byte offset of packed word w of lane l in a code tile.
+__device__ __forceinline__ int word_offset(int w, int l) { return ((w >> 2) * 32 + l) * 16 + (w & 3) * 4; }
+
+// Slice constants of a pair of slices (lo, hi in fp32): scales, the filter
+// constants as pairs, and the filter threshold.
+struct PairQ {
+  float lo0, lo1, sc0, sc1, thr;
+  f2x rcp, c;
+};
+
+__device__ __forceinline__ PairQ pair_q(float lo0, float hi0, float lo1, float hi1, float levels) {
+  PairQ p;
+  p.lo0 = lo0;
+  p.lo1 = lo1;
+  p.sc0 = __fdiv_rn(__fsub_rn(hi0, lo0), levels);
+  p.sc1 = __fdiv_rn(__fsub_rn(hi1, lo1), levels);
+  const SliceQ a = make_slice(lo0, p.sc0, levels), b = make_slice(lo1, p.sc1, levels);
+  p.rcp = f2_pack(a.rcp, b.rcp);
+  p.c = f2_pack(a.c, b.c);
+  p.thr = 0.5f - fmaxf(a.tol, b.tol);
+  return p;
+}
+
+// Reduce eight fp16 pairs to their elementwise min and max.
+__device__ __forceinline__ void minmax8(const uint32_t (&v)[8], uint32_t &mn, uint32_t &mx) {
+  uint32_t a0 = h2min(v[0], v[1]), a1 = h2min(v[2], v[3]), a2 = h2min(v[4], v[5]), a3 = h2min(v[6], v[7]);
+  uint32_t b0 = h2max(v[0], v[1]), b1 = h2max(v[2], v[3]), b2 = h2max(v[4], v[5]), b3 = h2max(v[6], v[7]);
+  mn = h2min(h2min(a0, a1), h2min(a2, a3));
+  mx = h2max(h2max(b0, b1), h2max(b2, b3));
+}
+
+// ---------------------------------------------------------------- key tile
+//
+// Lane L: channels 4L .. 4L+3, i.e. k-tile kt = L / 4, channel octet j =
+// (L / 2) % 2 and lane columns qA = 2 (L % 2) (channels 4L, 4L+1) and qB = qA
+// + 1 (4L+2, 4L+3); fp16 pair A of token t holds channels 4L, 4L+1 (fields
+// e = 0, 1), pair B channels 4L+2, 4L+3.  Word (kt, hw) of lane 4g + q holds
+// tokens 8 (hw NU + u) + g at bits 16e + 8j + b u.
+template <int BITS>
+__device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
+  constexpr int NU = 8 / BITS, WH = 4 / NU;
+  const float levels = float((1 << BITS) - 1);
+  const int kt = lane >> 2, j = (lane >> 1) & 1, q0 = 2 * (lane & 1);
+  uint32_t xa[kG], xb[kG];
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(tile + t * kRowPad + 8 * lane);
+    xa[t] = w.x;
+    xb[t] = w.y;
+  }
+  uint32_t mnA, mxA, mnB, mxB;
+  {
+    uint32_t m[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t va[8] = {xa[8 * i], xa[8 * i + 1], xa[8 * i + 2], xa[8 * i + 3],
+                              xa[8 * i + 4], xa[8 * i + 5], xa[8 * i + 6], xa[8 * i + 7]};
+      minmax8(va, m[i][0], m[i][1]);
+    }
+    mnA = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
+    mxA = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t vb[8] = {xb[8 * i], xb[8 * i + 1], xb[8 * i + 2], xb[8 * i + 3],
+                              xb[8 * i + 4], xb[8 * i + 5], xb[8 * i + 6], xb[8 * i + 7]};
+      minmax8(vb, m[i][0], m[i][1]);
+    }
+    mnB = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
+    mxB = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
+  }
+  PairQ qa, qb;
+  {
+    const float2 la = h2_to_f2_pos0(mnA), ha = h2_to_f2_pos0(mxA), lb = h2_to_f2_pos0(mnB), hb = h2_to_f2_pos0(mxB);
+    qa = pair_q(la.x, ha.x, la.y, ha.y, levels);
+    qb = pair_q(lb.x, hb.x, lb.y, hb.y, levels);
+  }
+  reinterpret_cast<float4 *>(meta)[lane] = make_float4(qa.sc0, qa.sc1, qb.sc0, qb.sc1);
+  reinterpret_cast<float4 *>(meta + kD)[lane] = make_float4(qa.lo0, qa.lo1, qb.lo0, qb.lo1);
+  float sc[NU];
+  int pos[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    pos[u] = 8 * j + BITS * u;
+    sc[u] = __int_as_float((127 + pos[u]) << 23);
+  }
+  // half-words (A / B, hw, g)
+  uint32_t part[2][WH][8];
+#pragma unroll
+  for (int hw = 0; hw < WH; ++hw)
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      uint32_t va[NU], vb[NU];
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        va[u] = xa[8 * (hw * NU + u) + g];
+        vb[u] = xb[8 * (hw * NU + u) + g];
+      }
+      bool na, nb;
+      part[0][hw][g] = pack_pairs<NU>(va, qa.rcp, qa.c, sc, qa.thr, na);
+      part[1][hw][g] = pack_pairs<NU>(vb, qb.rcp, qb.c, sc, qb.thr, nb);
+      if (__any_sync(0xffffffffu, na || nb)) {
+        if (na) part[0][hw][g] = pack_pairs_exact<BITS, NU>(va, qa.lo0, qa.sc0, qa.lo1, qa.sc1, pos);
+        if (nb) part[1][hw][g] = pack_pairs_exact<BITS, NU>(vb, qb.lo0, qb.sc0, qb.lo1, qb.sc1, pos);
+      }
+    }
+  // lane L ^ 2 holds the other octet j of the same words: this lane keeps
+  // rows g = 4j .. 4j+3 and hands over the others
+#pragma unroll
+  for (int X = 0; X < 2; ++X)
+#pragma unroll
+    for (int hw = 0; hw < WH; ++hw)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t mine = j ? part[X][hw][4 + k] : part[X][hw][k];
+        const uint32_t send = j ? part[X][hw][k] : part[X][hw][4 + k];
+        const uint32_t w = mine | __shfl_xor_sync(0xffffffffu, send, 2);
+        const int l = 4 * (4 * j + k) + q0 + X;
+        *reinterpret_cast<uint32_t *>(codes + word_offset(kt * WH + hw, l)) = w;
+      }
+}
+
+// -------------------------------------------------------------- value tile
+//
+// Lane L: tokens 2p, 2p+1 (p = L % 16) over channels 64 hf .. 64 hf + 63
+// (hf = L / 16).  Token octet j = (p / 4) % 2, lane column q = p % 4 and
+// k-tile kt = p / 8 of the layout; word (2P + kt) WH + hw of lane 4g + q
+// holds channels 32P + 8 (hw NU + u) + g at bits 16e + 8j + b u, e the token
+// parity.  The two rows are read in the order (2p + j, 2p + 1 - j), which
+// spreads each quarter warp's 16-byte reads over the eight bank groups; the
+// byte permutes that pair a channel's two tokens undo the order.
+template <int BITS>
+__device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
+  constexpr int NU = 8 / BITS, WH = 4 / NU;
+  const float levels = float((1 << BITS) - 1);
+  const int p = lane & 15, hf = lane >> 4;
+  const int j = (p >> 2) & 1, q = p & 3, kt = p >> 3;
+  const int ra = 2 * p + j, rb = 2 * p + 1 - j;
+  uint32_t xa[32], xb[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(tile + ra * kRowPad + 128 * hf + 16 * i);
+    const uint4 b = *reinterpret_cast<const uint4 *>(tile + rb * kRowPad + 128 * hf + 16 * i);
+    xa[4 * i] = a.x;
+    xa[4 * i + 1] = a.y;
+    xa[4 * i + 2] = a.z;
+    xa[4 * i + 3] = a.w;
+    xb[4 * i] = b.x;
+    xb[4 * i + 1] = b.y;
+    xb[4 * i + 2] = b.z;
+    xb[4 * i + 3] = b.w;
+  }
+  // (token 2p, token 2p+1) min and max over the 128 channels
+  uint32_t mn2, mx2;
+  {
+    uint32_t m[4][2], n[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t va[8] = {xa[8 * i], xa[8 * i + 1], xa[8 * i + 2], xa[8 * i + 3],
+                              xa[8 * i + 4], xa[8 * i + 5], xa[8 * i + 6], xa[8 * i + 7]};
+      const uint32_t vb[8] = {xb[8 * i], xb[8 * i + 1], xb[8 * i + 2], xb[8 * i + 3],
+                              xb[8 * i + 4], xb[8 * i + 5], xb[8 * i + 6], xb[8 * i + 7]};
+      minmax8(va, m[i][0], m[i][1]);
+      minmax8(vb, n[i][0], n[i][1]);
+    }
+    const uint32_t an = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
+    const uint32_t ax = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
+    const uint32_t bn = h2min(h2min(n[0][0], n[1][0]), h2min(n[2][0], n[3][0]));
+    const uint32_t bx = h2max(h2max(n[0][1], n[1][1]), h2max(n[2][1], n[3][1]));
+    // (row a, row b) of the low halves and of the high halves, then their
+    // min: one pair per token; j = 1 swaps the rows back to (2p, 2p + 1)
+    const uint32_t lo_sel = j ? 0x1054u : 0x5410u, hi_sel = j ? 0x3276u : 0x7632u;
+    mn2 = h2min(__byte_perm(an, bn, lo_sel), __byte_perm(an, bn, hi_sel));
+    mx2 = h2max(__byte_perm(ax, bx, lo_sel), __byte_perm(ax, bx, hi_sel));
+    mn2 = h2min(mn2, __shfl_xor_sync(0xffffffffu, mn2, 16));  // the other channel half
+    mx2 = h2max(mx2, __shfl_xor_sync(0xffffffffu, mx2, 16));
+  }
+  PairQ pq;
+  {
+    const float2 lo = h2_to_f2_pos0(mn2), hi = h2_to_f2_pos0(mx2);
+    pq = pair_q(lo.x, hi.x, lo.y, hi.y, levels);
+  }
+  if (hf == 0) {
+    reinterpret_cast<float2 *>(meta)[p] = make_float2(pq.sc0, pq.sc1);
+    reinterpret_cast<float2 *>(meta + kG)[p] = make_float2(pq.lo0, pq.lo1);
+  }
+  float sc[NU];
+  int pos[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    pos[u] = 8 * j + BITS * u;
+    sc[u] = __int_as_float((127 + pos[u]) << 23);
+  }
+  const uint32_t lo_sel = j ? 0x1054u : 0x5410u, hi_sel = j ? 0x3276u : 0x7632u;
+  // half-words (Pl, hw, g): channel 64 hf + 32 Pl + 8 (hw NU + u) + g sits
+  // in pair m = g / 2 of chunk i = 4 Pl + hw NU + u, low half for even g
+  uint32_t part[2][WH][8];
+#pragma unroll
+  for (int Pl = 0; Pl < 2; ++Pl)
+#pragma unroll
+    for (int hw = 0; hw < WH; ++hw)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t ve[NU], vo[NU];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          const int w = 4 * (4 * Pl + hw * NU + u) + m;
+          ve[u] = __byte_perm(xa[w], xb[w], lo_sel);  // channel 2m (+ base): (token 2p, token 2p + 1)
+          vo[u] = __byte_perm(xa[w], xb[w], hi_sel);  // channel 2m + 1
+        }
+        bool ne, no;
+        part[Pl][hw][2 * m] = pack_pairs<NU>(ve, pq.rcp, pq.c, sc, pq.thr, ne);
+        part[Pl][hw][2 * m + 1] = pack_pairs<NU>(vo, pq.rcp, pq.c, sc, pq.thr, no);
+        if (__any_sync(0xffffffffu, ne || no)) {
+          if (ne) part[Pl][hw][2 * m] = pack_pairs_exact<BITS, NU>(ve, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
+          if (no) part[Pl][hw][2 * m + 1] = pack_pairs_exact<BITS, NU>(vo, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
+        }
+      }
+  // lane L ^ 4 holds the other token octet of the same words: keep rows
+  // g = 4j .. 4j+3, hand over the others
+#pragma unroll
+  for (int Pl = 0; Pl < 2; ++Pl)
+#pragma unroll
+    for (int hw = 0; hw < WH; ++hw)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t mine = j ? part[Pl][hw][4 + k] : part[Pl][hw][k];
+        const uint32_t send = j ? part[Pl][hw][k] : part[Pl][hw][4 + k];
+        const uint32_t w = mine | __shfl_xor_sync(0xffffffffu, send, 4);
+        const int P = 2 * hf + Pl;
+        *reinterpret_cast<uint32_t *>(codes + word_offset((2 * P + kt) * WH + hw, 4 * (4 * j + k) + q)) = w;
+      }
+}
+
+// ------------------------------------------------------------------ kernel
+
+// Persistent CTAs of WARPS independent warps (one CTA per SM).  Warp gw of
+// NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
+// flushed) tiles, ordered (sequence, KV head, group, keys / values).
+template <int BITS>
+__global__ void __launch_bounds__(TileSmem<BITS>::WARPS * 32, 1)
+    quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
+                       const int *__restrict__ new_len, int max_new) {
+  using TS = TileSmem<BITS>;
+  constexpr int NS = TS::NS, CT = TS::CT, BB = block_bytes(BITS);
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *base = smem + warp * TS::BYTES;
+  uint8_t *stage = base + TS::STAGE;                          // codes [CT], then scales and mins
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + TS::BAR);
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int NW = gridDim.x * TS::WARPS, gw = blockIdx.x * TS::WARPS + warp;
+  const int S = geo.S, H = geo.H;
+
+  // ---- the line: U tiles in all; the first tile of this warp's range
+  long long tot = 0;
+  for (int s = lane; s < S; s += 32) tot += seq_flush(geo, new_len, max_new, s).ng;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+  const long long U = 2 * tot * H;
+  const long long ua = gw * U / NW, ub = (gw + 1) * U / NW;
+  if (ua >= ub) return;
+  TilePos cp;
+  {
+    long long run = 0;  // tiles of the sequences before chunk c
+    cp.s = S;
+    for (int c = 0; c < S; c += 32) {
+      const long long v = c + lane < S ? 2LL * H * seq_flush(geo, new_len, max_new, c + lane).ng : 0;
+      long long incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, c + lane < S && run + incl > ua);
+      if (m) {
+        const int idx = __ffs(m) - 1;
+        cp.s = c + idx;
+        const long long local = ua - (run + __shfl_sync(0xffffffffu, incl - v, idx));
+        cp.f = seq_flush(geo, new_len, max_new, cp.s);
+        const long long per_head = 2LL * cp.f.ng;
+        cp.h = static_cast<int>(local / per_head);
+        const int rem = static_cast<int>(local - cp.h * per_head);
+        cp.g = rem >> 1;
+        cp.kind = rem & 1;
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+
+  // ---- fetch: lane r copies token row r of the tile into the ring slot
+  TilePos fp = cp;
+  long long fu = ua;  // next tile to fetch
+  uint32_t fseq = 0, cseq = 0;
+  auto top_up = [&]() {
+    while (fu < ub && fseq - cseq < static_cast<uint32_t>(NS)) {
+      const uint32_t slot = fseq % NS;
+      const size_t sh = static_cast<size_t>(fp.s) * H + fp.h;
+      const int i = fp.f.Lq0 + kG * fp.g + lane;  // stream index of row `lane`
+      const __half *src = i < fp.f.n0
+                              ? (fp.kind ? geo.v_res : geo.k_res) + (sh * geo.R + (i - fp.f.Lq0)) * kD
+                              : (fp.kind ? v_new : k_new) + (sh * max_new + (i + geo.ns - fp.f.L0)) * kD;
+      fence_proxy_async();  // this lane's reads of the slot, before the copy that overwrites it
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], kG * kD * 2);
+      __syncwarp();
+      bulk_g2s(base + slot * kSlotBytes + lane * kRowPad, src, kD * 2, &full[slot]);
+      ++fseq;
+      ++fu;
+      if (fu < ub) next_tile(fp, geo, new_len, max_new);
+    }
+  };
+  top_up();
+
+  // ---- consume
+  bool ok = true;
+  for (long long u = ua; u < ub; ++u) {
+    const uint32_t slot = cseq % NS;
+    if (!mbar_wait_bounded(&full[slot], (cseq / NS) & 1)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) bulk_wait_read();  // the previous tile's bulk stores have left the stage
+    __syncwarp();
+    const uint8_t *tile = base + slot * kSlotBytes;
+    float *meta = reinterpret_cast<float *>(stage + CT);
+    if (cp.kind == 0)
+      key_tile<BITS>(tile, stage, meta, lane);
+    else
+      value_tile<BITS>(tile, stage, meta, lane);
+    fence_proxy_async();  // this lane's stage writes, before the bulk copies read them
+    __syncwarp();
+    if (lane == 0) {
+      uint8_t *blk = group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB);
+      if (blk) {
+        if (cp.kind == 0) {
+          bulk_s2g(blk + off_kc(BITS), stage, CT);
+          bulk_s2g(blk + off_ks(BITS), meta, 4 * 2 * kD);
+        } else {
+          bulk_s2g(blk + off_vc(BITS), stage, CT);
+          bulk_s2g(blk + off_vs(BITS), meta, 4 * 2 * kG);
+        }
+      } else if (cp.kind == 0) {
+        set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
+      }
+    }
+    ++cseq;
+    top_up();
+    if (u + 1 < ub) next_tile(cp, geo, new_len, max_new);
+  }
+  if (!ok) {
+    if (lane == 0) set_status(geo.status, KVQ_STATUS_TIMEOUT);
+    for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+// One CTA per SM; false when this geometry is not served here (the caller
+// then uses the general flush kernel).
+template <int BITS>
+static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
+                                  int max_new, cudaStream_t stream) {
+  using TS = TileSmem<BITS>;
+  static int sms[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int n_sm = dev < 64 ? sms[dev] : 0;
+  if (n_sm == 0) {
+    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  TS::WARPS * TS::BYTES)) != cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (dev < 64) sms[dev] = n_sm;
+  }
+  quant_tiles_kernel<BITS><<<n_sm, TS::WARPS * 32, TS::WARPS * TS::BYTES, stream>>>(geo, k_new, v_new, new_len,
+                                                                                   max_new);
+  return cudaGetLastError();
+}
+
+bool flush_tiles_serves(const Geo &geo) {
+  return !geo.kpt && !geo.rot && !geo.sparse && geo.S <= kTileFlushMaxSeqs;
+}
+
+cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
+                               int max_new, cudaStream_t stream) {
+  return geo.bits == 2 ? launch_tiles_t<2>(geo, k_new, v_new, new_len, max_new, stream)
+                       : launch_tiles_t<4>(geo, k_new, v_new, new_len, max_new, stream);
+}
+
+}  // namespace kvq

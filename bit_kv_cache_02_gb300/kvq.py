@@ -28,7 +28,7 @@ BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN, BUF_BLOCK
 EXPORTED = (
     "kvq_block_bytes", "kvq_max_groups", "kvq_buffer_bytes", "kv_quant_append",
     "kv_decode_workspace_bytes", "kv_decode_attn", "kv_dequant", "kvq_strerror",
-    "kvq_launch_count", "kvq_set_decode_warps", "kv_decode_attn_noalloc", "kvq_set_wait_limit_cycles",
+    "kvq_launch_count", "kvq_set_decode_warps", "kv_decode_attn_noalloc", "kvq_set_wait_test",
 )
 
 
@@ -63,7 +63,7 @@ def _load():
         "kvq_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvq_launch_count": (c_uint64, []),
         "kvq_set_decode_warps": (ctypes.c_int, [c_int32]),
-        "kvq_set_wait_limit_cycles": (ctypes.c_int, [c_int64]),
+        "kvq_set_wait_test": (ctypes.c_int, [c_int64, c_int32]),
         "kv_decode_attn_noalloc": (ctypes.c_int, [P, c_int32, c_void_p, c_float, c_void_p, c_int32, c_void_p]),
     }
     for name, (res, args) in sig.items():
@@ -233,7 +233,8 @@ def set_decode_warps(warps: int):
     _check(lib.kvq_set_decode_warps(warps), "kvq_set_decode_warps")
 
 
-def set_wait_limit_cycles(cycles: int):
-    """Cycle limit of the decode kernel's pipeline waits (0: the default of
-    about two seconds); a test aid for the timeout path."""
-    _check(lib.kvq_set_wait_limit_cycles(int(cycles)), "kvq_set_wait_limit_cycles")
+def set_wait_test(limit_cycles: int, wait_before_fetch: bool = False):
+    """Test aid for the decode kernel's bounded waits: their cycle limit (0:
+    the default of about two seconds) and whether each warp's first wait
+    comes before its first copy (so that it runs out)."""
+    _check(lib.kvq_set_wait_test(int(limit_cycles), int(bool(wait_before_fetch))), "kvq_set_wait_test")

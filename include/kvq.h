@@ -333,15 +333,18 @@ uint64_t kvq_launch_count(void);
  * KVQ_ERR_INVALID_ARG. */
 int kvq_set_decode_warps(int32_t warps);
 
-/* Test aid (not on the pages): SM clock cycles a pipeline wait of the decode
- * kernel may last before it gives up, records KVQ_STATUS_TIMEOUT, lets its
- * own copies in flight land (those waits keep the default bound) and ends its
- * work; 0 restores the default of about two seconds (4e9 cycles).  A small
- * limit makes the waits give up whenever data is not there yet, which is how
- * tests exercise the timeout path without a fault.  Affects kv_decode_attn
- * calls made afterwards in this process.  Returns KVQ_OK, or
- * KVQ_ERR_INVALID_ARG for a negative value or one above the default. */
-int kvq_set_wait_limit_cycles(int64_t cycles);
+/* Test aid (not on the pages) for the bounded waits of the decode kernel.
+ * limit_cycles: SM clock cycles a pipeline wait may last before it gives up,
+ * records KVQ_STATUS_TIMEOUT, lets its own copies in flight land (those
+ * waits keep the default bound) and ends its warp's work; 0 restores the
+ * default of about two seconds (4e9 cycles).  wait_before_fetch = 1 makes
+ * each warp's first wait come before its first copy is issued, on a barrier
+ * that nothing completes, so that it runs out: this is how tests exercise the
+ * timeout path without a fault (in normal operation every copy of a valid
+ * block lands).  It needs limit_cycles > 0.  Affects kv_decode_attn calls made
+ * afterwards in this process.  Returns KVQ_OK, or KVQ_ERR_INVALID_ARG for a
+ * limit that is negative or above the default, or a bad flag. */
+int kvq_set_wait_test(int64_t limit_cycles, int32_t wait_before_fetch);
 
 #ifdef __cplusplus
 }

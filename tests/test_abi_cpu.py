@@ -175,7 +175,7 @@ def test_null_and_misaligned_buffers_rejected_before_launch(kvq):
     assert kvq.lib.kv_dequant(p, None, q, None) == -1
     assert kvq.lib.kvq_set_decode_warps(-1) == -1 and kvq.lib.kvq_set_decode_warps(2561) == -1
     assert kvq.lib.kvq_set_decode_warps(7) == 0 and kvq.lib.kvq_set_decode_warps(0) == 0
-    assert kvq.lib.kvq_set_wait_limit_cycles(-1) == -1
-    assert kvq.lib.kvq_set_wait_limit_cycles(4000000001) == -1
-    assert kvq.lib.kvq_set_wait_limit_cycles(1) == 0 and kvq.lib.kvq_set_wait_limit_cycles(0) == 0
+    assert kvq.lib.kvq_set_wait_test(-1, 0) == -1 and kvq.lib.kvq_set_wait_test(4000000001, 0) == -1
+    assert kvq.lib.kvq_set_wait_test(0, 1) == -1 and kvq.lib.kvq_set_wait_test(100, 2) == -1
+    assert kvq.lib.kvq_set_wait_test(100, 1) == 0 and kvq.lib.kvq_set_wait_test(0, 0) == 0
     assert kvq.lib.kvq_strerror(-4) == b"workspace missing or too small"

@@ -504,14 +504,13 @@ def test_workspace_too_small_raises(kvq):
 
 @pytest.mark.parametrize("pre_rope", [False, True])
 def test_wait_timeout_sets_status_and_recovers(kvq, pre_rope):
-    """The decode kernel's ring waits are bounded: with the limit cut to one
-    SM cycle a wait gives up whenever its group has not landed yet, records
-    KVQ_STATUS_TIMEOUT, lets its warp's copies in flight land and ends that
-    warp's work; the call returns and the device stays usable.  After the
-    workspace is zeroed again (a timed-out call leaves merge counters
-    non-zero) and the limit restored, the same call matches the oracle.
-    Nothing faults and nothing hangs: the waits are on copies of valid
-    blocks, which complete."""
+    """The decode kernel's ring waits are bounded.  In normal operation every
+    copy lands before its first poll, so the test makes each warp's first
+    wait come before its first copy is issued, on a barrier that nothing
+    completes, with a limit of 20000 SM cycles: the wait runs out, the
+    kernel records KVQ_STATUS_TIMEOUT and returns, and the device stays
+    usable.  With the defaults restored and the workspace zeroed again, the
+    same call matches the oracle.  Nothing faults and nothing hangs."""
     S, H, T = 8, 4, 3000
     k, v = _rand_kv(S, H, T, seed=41)
     cache, orc = _build(kvq, S, H, T + 8, 2, ns=int(pre_rope), pre_rope=pre_rope)
@@ -520,20 +519,13 @@ def test_wait_timeout_sets_status_and_recovers(kvq, pre_rope):
     dq = torch.from_numpy(q).cuda()
     out = torch.empty_like(dq)
     ws = kvq.alloc_workspace(cache, 2 * H, T)
-    seen = 0
     try:
-        kvq.set_wait_limit_cycles(1)
-        for _ in range(5):          # a call gives up unless every first poll finds its data
-            kvq.kv_decode_attn(cache, dq, out, ws, T)
-            torch.cuda.synchronize()
-            seen = int(cache.status.item())
-            if seen & kvq.KVQ_STATUS_TIMEOUT:
-                break
-            ws.zero_()
+        kvq.set_wait_test(20000, True)
+        kvq.kv_decode_attn(cache, dq, out, ws, T)
+        torch.cuda.synchronize()
     finally:
-        kvq.set_wait_limit_cycles(0)
-    assert seen & kvq.KVQ_STATUS_TIMEOUT, f"no wait gave up (status {seen})"
-    assert seen == kvq.KVQ_STATUS_TIMEOUT
+        kvq.set_wait_test(0, False)
+    assert int(cache.status.item()) == kvq.KVQ_STATUS_TIMEOUT
     cache.status.zero_()
     ws.zero_()
     kvq.kv_decode_attn(cache, dq, out, ws, T)
