@@ -732,6 +732,77 @@ __global__ void __launch_bounds__(256) append_tail_kernel(Geo geo, const __half 
   if (threadIdx.x == 0) geo.seq_len[s] = L0 + nn;
 }
 
+// The same as append_tail_kernel with one CTA per (KV head, sequence), for
+// long appends whose tails (up to R - 1 window tokens per head) a single CTA
+// per sequence copies too slowly.  Every CTA reads seq_len[s], then adds
+// 1 << kLenBits to it; the CTA completing the count (Hkv arrivals) stores
+// the new length (or the old one for a bad length, reported by head 0's
+// CTA), so no CTA reads seq_len[s] after it changes.  A negative length
+// makes every CTA leave the sequence untouched.  Each thread moves up to four
+// 16-byte chunks of K and of V per round, loads before stores.
+__global__ void __launch_bounds__(256) append_tail_split_kernel(Geo geo, const __half *__restrict__ k_new,
+                                                                const __half *__restrict__ v_new,
+                                                                const int *__restrict__ new_len, int max_new) {
+  const int s = blockIdx.y, h = blockIdx.x;
+  __shared__ int s_last, s_old;
+  const int raw = geo.seq_len[s];
+  const int nn = new_len[s];
+  if (raw < 0) {
+    if (threadIdx.x == 0 && h == 0) set_status(geo.status, KVQ_STATUS_BAD_LEN);
+    return;
+  }
+  __syncthreads();  // every thread has read seq_len[s]
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&geo.seq_len[s], 1 << kLenBits);
+    s_old = old - (geo.H - 1) * (1 << kLenBits);  // seq_len[s] before this kernel (valid for the last)
+    s_last = (old >> kLenBits) == geo.H - 1;
+  }
+  const int L0 = raw & kLenMask;
+  const bool bad_len = nn < 0 || nn > max_new;
+  const bool over = !bad_len && L0 + nn > geo.capacity;
+  if (!bad_len && !over) {
+    const int n1 = max(L0 + nn - geo.ns, 0);
+    const int Lq1 = n1 - n1 % geo.R;
+    const int j_sink_end = min(max(geo.ns - L0, 0), nn);  // new tokens [0, j_sink_end) -> sink
+    const int j_win = max(Lq1 + geo.ns - L0, j_sink_end);  // new tokens [j_win, nn) -> window
+    const int n_copy = j_sink_end + max(nn - j_win, 0);
+    constexpr int C16 = kD / 8;  // 16-byte chunks per token row
+    const int total = n_copy * C16;
+    const size_t sh = static_cast<size_t>(s) * geo.H + h;
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+      uint4 kr[4], vr[4];
+      uint4 *dk[4], *dv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = base + u * blockDim.x;
+        dk[u] = dv[u] = nullptr;
+        if (idx >= total) continue;
+        const int k = idx / C16, c8 = idx % C16;
+        const int j = k < j_sink_end ? k : j_win + (k - j_sink_end);
+        const int pos = L0 + j;
+        const size_t row = pos < geo.ns ? sh * geo.ns + pos : sh * geo.R + (pos - geo.ns - Lq1);
+        dk[u] = reinterpret_cast<uint4 *>((pos < geo.ns ? geo.k_sink : geo.k_res) + row * kD) + c8;
+        dv[u] = reinterpret_cast<uint4 *>((pos < geo.ns ? geo.v_sink : geo.v_res) + row * kD) + c8;
+        const size_t src = (sh * max_new + j) * kD + c8 * 8;
+        kr[u] = *reinterpret_cast<const uint4 *>(k_new + src);
+        vr[u] = *reinterpret_cast<const uint4 *>(v_new + src);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (dk[u]) {
+          *dk[u] = kr[u];
+          *dv[u] = vr[u];
+        }
+    }
+  }
+  __syncthreads();  // s_last / s_old
+  if (s_last && threadIdx.x == 0) {
+    if (bad_len) set_status(geo.status, KVQ_STATUS_BAD_LEN);
+    if (over) set_status(geo.status, KVQ_STATUS_CAPACITY);
+    geo.seq_len[s] = bad_len || over ? s_old : L0 + nn;
+  }
+}
+
 // Upper bound on groups quantized per (sequence, head) by one append of at
 // most max_new tokens: a window holding R-1 tokens plus max_new new ones.
 int max_flush_groups(int R, int max_new) { return ((R - 1 + max_new) / R) * (R / kG); }
@@ -800,7 +871,10 @@ cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __hal
     ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  append_tail_kernel<<<geo.S, 256, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+  if (geo.capacity <= kLenMask && geo.H < (1 << (31 - kLenBits)))
+    append_tail_split_kernel<<<dim3(geo.H, geo.S), 256, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
+  else
+    append_tail_kernel<<<geo.S, 256, 0, stream>>>(geo, k_new, v_new, new_len, max_new);
   ++*launches;
   return cudaGetLastError();
 }

@@ -25,13 +25,12 @@
 //               channel, which the layout places in the two halves of a word.
 //
 // A packed word takes codes from two lanes (the two channel octets j of a
-// 16-channel tile for keys, the two token octets for values); each lane
-// builds its half-words for 16 words (2-bit; 32 at 4-bit), keeps half of
-// them and trades the other half with its partner lane in one shuffle each.
-// Codes use the reciprocal filter with the exact IEEE fallback of
-// quant_common.cuh, so they equal the oracle's bit for bit.  The finished
-// tile (codes, then its scales and mins) is staged in shared memory and
-// written by two bulk copies.
+// 16-channel tile for keys, the two token octets for values): each lane
+// builds its half, one shuffle ORs in the partner's, and one of the two
+// stores the word.  Codes use the reciprocal filter with the exact IEEE
+// fallback of quant_common.cuh, so they equal the oracle's bit for bit.  The
+// finished tile (codes, then its scales and mins) is staged in shared memory
+// and written by two bulk copies.
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -165,52 +164,47 @@ __device__ __forceinline__ PairQ pair_q(float lo0, float hi0, float lo1, float h
   return p;
 }
 
-// Reduce eight fp16 pairs to their elementwise min and max.
-__device__ __forceinline__ void minmax8(const uint32_t (&v)[8], uint32_t &mn, uint32_t &mx) {
-  uint32_t a0 = h2min(v[0], v[1]), a1 = h2min(v[2], v[3]), a2 = h2min(v[4], v[5]), a3 = h2min(v[6], v[7]);
-  uint32_t b0 = h2max(v[0], v[1]), b1 = h2max(v[2], v[3]), b2 = h2max(v[4], v[5]), b3 = h2max(v[6], v[7]);
-  mn = h2min(h2min(a0, a1), h2min(a2, a3));
-  mx = h2max(h2max(b0, b1), h2max(b2, b3));
-}
-
 // ---------------------------------------------------------------- key tile
 //
 // Lane L: channels 4L .. 4L+3, i.e. k-tile kt = L / 4, channel octet j =
 // (L / 2) % 2 and lane columns qA = 2 (L % 2) (channels 4L, 4L+1) and qB = qA
 // + 1 (4L+2, 4L+3); fp16 pair A of token t holds channels 4L, 4L+1 (fields
 // e = 0, 1), pair B channels 4L+2, 4L+3.  Word (kt, hw) of lane 4g + q holds
-// tokens 8 (hw NU + u) + g at bits 16e + 8j + b u.
+// tokens 8 (hw NU + u) + g at bits 16e + 8j + b u: this lane's half of it,
+// OR-ed with lane L ^ 2's (the other octet), is stored by the lane whose
+// octet j = g / 4.  The loops stay rolled and re-read the tile from shared
+// memory: fully unrolled, the key and value code no longer fit the
+// instruction cache.
 template <int BITS>
 __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int kt = lane >> 2, j = (lane >> 1) & 1, q0 = 2 * (lane & 1);
-  uint32_t xa[kG], xb[kG];
-#pragma unroll
-  for (int t = 0; t < kG; ++t) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(tile + t * kRowPad + 8 * lane);
-    xa[t] = w.x;
-    xb[t] = w.y;
-  }
+  const uint8_t *col = tile + 8 * lane;  // this lane's 8 bytes of token row t at col + t * kRowPad
   uint32_t mnA, mxA, mnB, mxB;
   {
-    uint32_t m[4][2];
+    uint32_t an[4], ax[4], bn[4], bx[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t va[8] = {xa[8 * i], xa[8 * i + 1], xa[8 * i + 2], xa[8 * i + 3],
-                              xa[8 * i + 4], xa[8 * i + 5], xa[8 * i + 6], xa[8 * i + 7]};
-      minmax8(va, m[i][0], m[i][1]);
+      const uint2 w = *reinterpret_cast<const uint2 *>(col + i * kRowPad);
+      an[i] = ax[i] = w.x;
+      bn[i] = bx[i] = w.y;
     }
-    mnA = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
-    mxA = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
+#pragma unroll 2
+    for (int t = 4; t < kG; t += 4) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t vb[8] = {xb[8 * i], xb[8 * i + 1], xb[8 * i + 2], xb[8 * i + 3],
-                              xb[8 * i + 4], xb[8 * i + 5], xb[8 * i + 6], xb[8 * i + 7]};
-      minmax8(vb, m[i][0], m[i][1]);
+      for (int i = 0; i < 4; ++i) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(col + (t + i) * kRowPad);
+        an[i] = h2min(an[i], w.x);
+        ax[i] = h2max(ax[i], w.x);
+        bn[i] = h2min(bn[i], w.y);
+        bx[i] = h2max(bx[i], w.y);
+      }
     }
-    mnB = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
-    mxB = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
+    mnA = h2min(h2min(an[0], an[1]), h2min(an[2], an[3]));
+    mxA = h2max(h2max(ax[0], ax[1]), h2max(ax[2], ax[3]));
+    mnB = h2min(h2min(bn[0], bn[1]), h2min(bn[2], bn[3]));
+    mxB = h2max(h2max(bx[0], bx[1]), h2max(bx[2], bx[3]));
   }
   PairQ qa, qb;
   {
@@ -227,40 +221,31 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
     pos[u] = 8 * j + BITS * u;
     sc[u] = __int_as_float((127 + pos[u]) << 23);
   }
-  // half-words (A / B, hw, g)
-  uint32_t part[2][WH][8];
+#pragma unroll 1
+  for (int wg = 0; wg < 8 * WH; ++wg) {  // (hw, g)
+    const int hw = wg >> 3, g = wg & 7;
+    uint32_t va[NU], vb[NU];
 #pragma unroll
-  for (int hw = 0; hw < WH; ++hw)
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      uint32_t va[NU], vb[NU];
-#pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        va[u] = xa[8 * (hw * NU + u) + g];
-        vb[u] = xb[8 * (hw * NU + u) + g];
-      }
-      bool na, nb;
-      part[0][hw][g] = pack_pairs<NU>(va, qa.rcp, qa.c, sc, qa.thr, na);
-      part[1][hw][g] = pack_pairs<NU>(vb, qb.rcp, qb.c, sc, qb.thr, nb);
-      if (__any_sync(0xffffffffu, na || nb)) {
-        if (na) part[0][hw][g] = pack_pairs_exact<BITS, NU>(va, qa.lo0, qa.sc0, qa.lo1, qa.sc1, pos);
-        if (nb) part[1][hw][g] = pack_pairs_exact<BITS, NU>(vb, qb.lo0, qb.sc0, qb.lo1, qb.sc1, pos);
-      }
+    for (int u = 0; u < NU; ++u) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(col + (8 * (hw * NU + u) + g) * kRowPad);
+      va[u] = w.x;
+      vb[u] = w.y;
     }
-  // lane L ^ 2 holds the other octet j of the same words: this lane keeps
-  // rows g = 4j .. 4j+3 and hands over the others
-#pragma unroll
-  for (int X = 0; X < 2; ++X)
-#pragma unroll
-    for (int hw = 0; hw < WH; ++hw)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t mine = j ? part[X][hw][4 + k] : part[X][hw][k];
-        const uint32_t send = j ? part[X][hw][k] : part[X][hw][4 + k];
-        const uint32_t w = mine | __shfl_xor_sync(0xffffffffu, send, 2);
-        const int l = 4 * (4 * j + k) + q0 + X;
-        *reinterpret_cast<uint32_t *>(codes + word_offset(kt * WH + hw, l)) = w;
-      }
+    bool na, nb;
+    uint32_t pa = pack_pairs<NU>(va, qa.rcp, qa.c, sc, qa.thr, na);
+    uint32_t pb = pack_pairs<NU>(vb, qb.rcp, qb.c, sc, qb.thr, nb);
+    if (__any_sync(0xffffffffu, na || nb)) {
+      if (na) pa = pack_pairs_exact<BITS, NU>(va, qa.lo0, qa.sc0, qa.lo1, qa.sc1, pos);
+      if (nb) pb = pack_pairs_exact<BITS, NU>(vb, qb.lo0, qb.sc0, qb.lo1, qb.sc1, pos);
+    }
+    pa |= __shfl_xor_sync(0xffffffffu, pa, 2);
+    pb |= __shfl_xor_sync(0xffffffffu, pb, 2);
+    if ((g >> 2) == j) {
+      const int w = kt * WH + hw;
+      *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0)) = pa;
+      *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0 + 1)) = pb;
+    }
+  }
 }
 
 // -------------------------------------------------------------- value tile
@@ -269,52 +254,49 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
 // (hf = L / 16).  Token octet j = (p / 4) % 2, lane column q = p % 4 and
 // k-tile kt = p / 8 of the layout; word (2P + kt) WH + hw of lane 4g + q
 // holds channels 32P + 8 (hw NU + u) + g at bits 16e + 8j + b u, e the token
-// parity.  The two rows are read in the order (2p + j, 2p + 1 - j), which
-// spreads each quarter warp's 16-byte reads over the eight bank groups; the
-// byte permutes that pair a channel's two tokens undo the order.
+// parity; lane L ^ 4 holds the other token octet.  The two rows are read in
+// the order (2p + j, 2p + 1 - j), which spreads each quarter warp's 16-byte
+// reads over the eight bank groups; the byte permutes that pair a channel's
+// two tokens undo the order.
 template <int BITS>
 __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int p = lane & 15, hf = lane >> 4;
   const int j = (p >> 2) & 1, q = p & 3, kt = p >> 3;
-  const int ra = 2 * p + j, rb = 2 * p + 1 - j;
-  uint32_t xa[32], xb[32];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 a = *reinterpret_cast<const uint4 *>(tile + ra * kRowPad + 128 * hf + 16 * i);
-    const uint4 b = *reinterpret_cast<const uint4 *>(tile + rb * kRowPad + 128 * hf + 16 * i);
-    xa[4 * i] = a.x;
-    xa[4 * i + 1] = a.y;
-    xa[4 * i + 2] = a.z;
-    xa[4 * i + 3] = a.w;
-    xb[4 * i] = b.x;
-    xb[4 * i + 1] = b.y;
-    xb[4 * i + 2] = b.z;
-    xb[4 * i + 3] = b.w;
-  }
+  const uint8_t *rowa = tile + (2 * p + j) * kRowPad + 128 * hf;
+  const uint8_t *rowb = tile + (2 * p + 1 - j) * kRowPad + 128 * hf;
+  const uint32_t lo_sel = j ? 0x1054u : 0x5410u, hi_sel = j ? 0x3276u : 0x7632u;
   // (token 2p, token 2p+1) min and max over the 128 channels
   uint32_t mn2, mx2;
   {
-    uint32_t m[4][2], n[4][2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t va[8] = {xa[8 * i], xa[8 * i + 1], xa[8 * i + 2], xa[8 * i + 3],
-                              xa[8 * i + 4], xa[8 * i + 5], xa[8 * i + 6], xa[8 * i + 7]};
-      const uint32_t vb[8] = {xb[8 * i], xb[8 * i + 1], xb[8 * i + 2], xb[8 * i + 3],
-                              xb[8 * i + 4], xb[8 * i + 5], xb[8 * i + 6], xb[8 * i + 7]};
-      minmax8(va, m[i][0], m[i][1]);
-      minmax8(vb, n[i][0], n[i][1]);
+    uint32_t an[4], ax[4], bn[4], bx[4];
+    {
+      const uint4 a = *reinterpret_cast<const uint4 *>(rowa), b = *reinterpret_cast<const uint4 *>(rowb);
+      an[0] = ax[0] = a.x; an[1] = ax[1] = a.y; an[2] = ax[2] = a.z; an[3] = ax[3] = a.w;
+      bn[0] = bx[0] = b.x; bn[1] = bx[1] = b.y; bn[2] = bx[2] = b.z; bn[3] = bx[3] = b.w;
     }
-    const uint32_t an = h2min(h2min(m[0][0], m[1][0]), h2min(m[2][0], m[3][0]));
-    const uint32_t ax = h2max(h2max(m[0][1], m[1][1]), h2max(m[2][1], m[3][1]));
-    const uint32_t bn = h2min(h2min(n[0][0], n[1][0]), h2min(n[2][0], n[3][0]));
-    const uint32_t bx = h2max(h2max(n[0][1], n[1][1]), h2max(n[2][1], n[3][1]));
+#pragma unroll 7
+    for (int i = 1; i < 8; ++i) {
+      const uint4 a = *reinterpret_cast<const uint4 *>(rowa + 16 * i);
+      const uint4 b = *reinterpret_cast<const uint4 *>(rowb + 16 * i);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        an[k] = h2min(an[k], av[k]);
+        ax[k] = h2max(ax[k], av[k]);
+        bn[k] = h2min(bn[k], bv[k]);
+        bx[k] = h2max(bx[k], bv[k]);
+      }
+    }
+    const uint32_t amn = h2min(h2min(an[0], an[1]), h2min(an[2], an[3]));
+    const uint32_t amx = h2max(h2max(ax[0], ax[1]), h2max(ax[2], ax[3]));
+    const uint32_t bmn = h2min(h2min(bn[0], bn[1]), h2min(bn[2], bn[3]));
+    const uint32_t bmx = h2max(h2max(bx[0], bx[1]), h2max(bx[2], bx[3]));
     // (row a, row b) of the low halves and of the high halves, then their
     // min: one pair per token; j = 1 swaps the rows back to (2p, 2p + 1)
-    const uint32_t lo_sel = j ? 0x1054u : 0x5410u, hi_sel = j ? 0x3276u : 0x7632u;
-    mn2 = h2min(__byte_perm(an, bn, lo_sel), __byte_perm(an, bn, hi_sel));
-    mx2 = h2max(__byte_perm(ax, bx, lo_sel), __byte_perm(ax, bx, hi_sel));
+    mn2 = h2min(__byte_perm(amn, bmn, lo_sel), __byte_perm(amn, bmn, hi_sel));
+    mx2 = h2max(__byte_perm(amx, bmx, lo_sel), __byte_perm(amx, bmx, hi_sel));
     mn2 = h2min(mn2, __shfl_xor_sync(0xffffffffu, mn2, 16));  // the other channel half
     mx2 = h2max(mx2, __shfl_xor_sync(0xffffffffu, mx2, 16));
   }
@@ -334,45 +316,45 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, 
     pos[u] = 8 * j + BITS * u;
     sc[u] = __int_as_float((127 + pos[u]) << 23);
   }
-  const uint32_t lo_sel = j ? 0x1054u : 0x5410u, hi_sel = j ? 0x3276u : 0x7632u;
-  // half-words (Pl, hw, g): channel 64 hf + 32 Pl + 8 (hw NU + u) + g sits
-  // in pair m = g / 2 of chunk i = 4 Pl + hw NU + u, low half for even g
-  uint32_t part[2][WH][8];
+  // words of channel block (Pl, hw): channel 64 hf + 32 Pl + 8 (hw NU + u) +
+  // g sits in pair m = g / 2 of chunk i = 4 Pl + hw NU + u, low half for even g
+#pragma unroll 1
+  for (int ph = 0; ph < 2 * WH; ++ph) {  // (Pl, hw)
+    const int Pl = ph / WH, hw = ph % WH;
+    uint32_t xa[NU][4], xb[NU][4];
 #pragma unroll
-  for (int Pl = 0; Pl < 2; ++Pl)
+    for (int u = 0; u < NU; ++u) {
+      const int i = 4 * Pl + hw * NU + u;
+      const uint4 a = *reinterpret_cast<const uint4 *>(rowa + 16 * i);
+      const uint4 b = *reinterpret_cast<const uint4 *>(rowb + 16 * i);
+      xa[u][0] = a.x; xa[u][1] = a.y; xa[u][2] = a.z; xa[u][3] = a.w;
+      xb[u][0] = b.x; xb[u][1] = b.y; xb[u][2] = b.z; xb[u][3] = b.w;
+    }
+    const int w = (2 * (2 * hf + Pl) + kt) * WH + hw;
 #pragma unroll
-    for (int hw = 0; hw < WH; ++hw)
+    for (int m = 0; m < 4; ++m) {
+      uint32_t ve[NU], vo[NU];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint32_t ve[NU], vo[NU];
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-          const int w = 4 * (4 * Pl + hw * NU + u) + m;
-          ve[u] = __byte_perm(xa[w], xb[w], lo_sel);  // channel 2m (+ base): (token 2p, token 2p + 1)
-          vo[u] = __byte_perm(xa[w], xb[w], hi_sel);  // channel 2m + 1
-        }
-        bool ne, no;
-        part[Pl][hw][2 * m] = pack_pairs<NU>(ve, pq.rcp, pq.c, sc, pq.thr, ne);
-        part[Pl][hw][2 * m + 1] = pack_pairs<NU>(vo, pq.rcp, pq.c, sc, pq.thr, no);
-        if (__any_sync(0xffffffffu, ne || no)) {
-          if (ne) part[Pl][hw][2 * m] = pack_pairs_exact<BITS, NU>(ve, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
-          if (no) part[Pl][hw][2 * m + 1] = pack_pairs_exact<BITS, NU>(vo, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
-        }
+      for (int u = 0; u < NU; ++u) {
+        ve[u] = __byte_perm(xa[u][m], xb[u][m], lo_sel);  // channel 2m (+ base): (token 2p, token 2p + 1)
+        vo[u] = __byte_perm(xa[u][m], xb[u][m], hi_sel);  // channel 2m + 1
       }
-  // lane L ^ 4 holds the other token octet of the same words: keep rows
-  // g = 4j .. 4j+3, hand over the others
-#pragma unroll
-  for (int Pl = 0; Pl < 2; ++Pl)
-#pragma unroll
-    for (int hw = 0; hw < WH; ++hw)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t mine = j ? part[Pl][hw][4 + k] : part[Pl][hw][k];
-        const uint32_t send = j ? part[Pl][hw][k] : part[Pl][hw][4 + k];
-        const uint32_t w = mine | __shfl_xor_sync(0xffffffffu, send, 4);
-        const int P = 2 * hf + Pl;
-        *reinterpret_cast<uint32_t *>(codes + word_offset((2 * P + kt) * WH + hw, 4 * (4 * j + k) + q)) = w;
+      bool ne, no;
+      uint32_t pe = pack_pairs<NU>(ve, pq.rcp, pq.c, sc, pq.thr, ne);
+      uint32_t po = pack_pairs<NU>(vo, pq.rcp, pq.c, sc, pq.thr, no);
+      if (__any_sync(0xffffffffu, ne || no)) {
+        if (ne) pe = pack_pairs_exact<BITS, NU>(ve, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
+        if (no) po = pack_pairs_exact<BITS, NU>(vo, pq.lo0, pq.sc0, pq.lo1, pq.sc1, pos);
       }
+      pe |= __shfl_xor_sync(0xffffffffu, pe, 4);
+      po |= __shfl_xor_sync(0xffffffffu, po, 4);
+      // rows g = 2m, 2m + 1 are stored by the lane of octet j = g / 4
+      if ((m >> 1) == j) {
+        *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * (2 * m) + q)) = pe;
+        *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * (2 * m + 1) + q)) = po;
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ kernel
