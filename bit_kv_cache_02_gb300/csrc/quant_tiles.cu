@@ -29,8 +29,10 @@
 // builds its half, one shuffle ORs in the partner's, and one of the two
 // stores the word.  Codes use the reciprocal filter with the exact IEEE
 // fallback of quant_common.cuh, so they equal the oracle's bit for bit.  The
-// finished tile (codes, then its scales and mins) is staged in shared memory
-// and written by two bulk copies.
+// lanes store the finished words and the slice scales and mins straight into
+// the group block (a tile's code words and metadata together cover whole
+// 32-byte sectors, which L2 merges before they reach HBM), so a warp needs
+// shared memory only for its ring.
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -41,15 +43,12 @@ constexpr int kSlotBytes = kG * kRowPad;    // 8704
 #define KVQ_TILE_RING 2
 #endif
 
-template <int BITS>
-struct TileSmem {  // one warp's shared memory
-  static constexpr int CT = code_tile_bytes(BITS);  // packed codes of one tile
-  static constexpr int NS = KVQ_TILE_RING;          // ring slots
-  static constexpr int STAGE = NS * kSlotBytes;     // codes, then scales and mins
-  static constexpr int BAR = STAGE + CT + 4 * 2 * kD;
+struct TileSmem {  // one warp's shared memory: the ring, then its mbarriers
+  static constexpr int NS = KVQ_TILE_RING;  // ring slots
+  static constexpr int BAR = NS * kSlotBytes;
   static constexpr int BYTES = (BAR + 8 * NS + 127) / 128 * 128;
   static constexpr int WARPS = 232448 / BYTES < 16 ? 232448 / BYTES : 16;  // warps per CTA (one CTA per SM)
-  static_assert(kSlotBytes % 16 == 0 && STAGE % 16 == 0 && (STAGE + CT) % 16 == 0, "bulk copies need 16 B");
+  static_assert(kSlotBytes % 16 == 0 && kRowPad % 16 == 0, "bulk copies need 16-byte alignment");
 };
 
 // The flush of sequence s in this append: groups ng starting at stream
@@ -118,7 +117,7 @@ __device__ __forceinline__ uint32_t pack_pairs(const uint32_t (&x)[NF], f2x rcp,
     const f2x y = f2_fma(f2_pack(xf.x, xf.y), rcp, c);
     const f2x r = f2_sub(f2_add(y, magic), magic);  // rne(y), exact
     const float2 e = f2_unpack(f2_sub(y, r));
-    emax = fmaxf(emax, fmaxf(fabsf(e.x), fabsf(e.y)));
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(emax) : "f"(emax), "f"(e.x), "f"(e.y));  // max of |.|
     acc = f2_fma(r, f2_pack(sc[f], sc[f]), acc);
   }
   near = emax > thr;
@@ -176,7 +175,7 @@ __device__ __forceinline__ PairQ pair_q(float lo0, float hi0, float lo1, float h
 // memory: fully unrolled, the key and value code no longer fit the
 // instruction cache.
 template <int BITS>
-__device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
+__device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int lane) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int kt = lane >> 2, j = (lane >> 1) & 1, q0 = 2 * (lane & 1);
@@ -212,8 +211,10 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
     qa = pair_q(la.x, ha.x, la.y, ha.y, levels);
     qb = pair_q(lb.x, hb.x, lb.y, hb.y, levels);
   }
-  reinterpret_cast<float4 *>(meta)[lane] = make_float4(qa.sc0, qa.sc1, qb.sc0, qb.sc1);
-  reinterpret_cast<float4 *>(meta + kD)[lane] = make_float4(qa.lo0, qa.lo1, qb.lo0, qb.lo1);
+  if (blk) {
+    reinterpret_cast<float4 *>(blk + off_ks(BITS))[lane] = make_float4(qa.sc0, qa.sc1, qb.sc0, qb.sc1);
+    reinterpret_cast<float4 *>(blk + off_km(BITS))[lane] = make_float4(qa.lo0, qa.lo1, qb.lo0, qb.lo1);
+  }
   float sc[NU];
   int pos[NU];
 #pragma unroll
@@ -221,7 +222,7 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
     pos[u] = 8 * j + BITS * u;
     sc[u] = __int_as_float((127 + pos[u]) << 23);
   }
-#pragma unroll 1
+#pragma unroll 2
   for (int wg = 0; wg < 8 * WH; ++wg) {  // (hw, g)
     const int hw = wg >> 3, g = wg & 7;
     uint32_t va[NU], vb[NU];
@@ -240,7 +241,8 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
     }
     pa |= __shfl_xor_sync(0xffffffffu, pa, 2);
     pb |= __shfl_xor_sync(0xffffffffu, pb, 2);
-    if ((g >> 2) == j) {
+    if ((g >> 2) == j && blk) {
+      uint8_t *codes = blk + off_kc(BITS);
       const int w = kt * WH + hw;
       *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0)) = pa;
       *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0 + 1)) = pb;
@@ -259,7 +261,7 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *codes, fl
 // reads over the eight bank groups; the byte permutes that pair a channel's
 // two tokens undo the order.
 template <int BITS>
-__device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, float *meta, int lane) {
+__device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, int lane) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int p = lane & 15, hf = lane >> 4;
@@ -305,9 +307,9 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, 
     const float2 lo = h2_to_f2_pos0(mn2), hi = h2_to_f2_pos0(mx2);
     pq = pair_q(lo.x, hi.x, lo.y, hi.y, levels);
   }
-  if (hf == 0) {
-    reinterpret_cast<float2 *>(meta)[p] = make_float2(pq.sc0, pq.sc1);
-    reinterpret_cast<float2 *>(meta + kG)[p] = make_float2(pq.lo0, pq.lo1);
+  if (hf == 0 && blk) {
+    reinterpret_cast<float2 *>(blk + off_vs(BITS))[p] = make_float2(pq.sc0, pq.sc1);
+    reinterpret_cast<float2 *>(blk + off_vm(BITS))[p] = make_float2(pq.lo0, pq.lo1);
   }
   float sc[NU];
   int pos[NU];
@@ -349,7 +351,8 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, 
       pe |= __shfl_xor_sync(0xffffffffu, pe, 4);
       po |= __shfl_xor_sync(0xffffffffu, po, 4);
       // rows g = 2m, 2m + 1 are stored by the lane of octet j = g / 4
-      if ((m >> 1) == j) {
+      if ((m >> 1) == j && blk) {
+        uint8_t *codes = blk + off_vc(BITS);
         *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * (2 * m) + q)) = pe;
         *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * (2 * m + 1) + q)) = po;
       }
@@ -363,15 +366,14 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *codes, 
 // NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
 // flushed) tiles, ordered (sequence, KV head, group, keys / values).
 template <int BITS>
-__global__ void __launch_bounds__(TileSmem<BITS>::WARPS * 32, 1)
+__global__ void __launch_bounds__(TileSmem::WARPS * 32, 1)
     quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int *__restrict__ new_len, int max_new) {
-  using TS = TileSmem<BITS>;
-  constexpr int NS = TS::NS, CT = TS::CT, BB = block_bytes(BITS);
+  using TS = TileSmem;
+  constexpr int NS = TS::NS, BB = block_bytes(BITS);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *base = smem + warp * TS::BYTES;
-  uint8_t *stage = base + TS::STAGE;                          // codes [CT], then scales and mins
   uint64_t *full = reinterpret_cast<uint64_t *>(base + TS::BAR);
   if (lane == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
@@ -449,30 +451,14 @@ __global__ void __launch_bounds__(TileSmem<BITS>::WARPS * 32, 1)
       ok = false;
       break;
     }
-    if (lane == 0) bulk_wait_read();  // the previous tile's bulk stores have left the stage
-    __syncwarp();
     const uint8_t *tile = base + slot * kSlotBytes;
-    float *meta = reinterpret_cast<float *>(stage + CT);
+    uint8_t *blk = group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB);  // null: a bad table entry
+    if (!blk && cp.kind == 0 && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
     if (cp.kind == 0)
-      key_tile<BITS>(tile, stage, meta, lane);
+      key_tile<BITS>(tile, blk, lane);
     else
-      value_tile<BITS>(tile, stage, meta, lane);
-    fence_proxy_async();  // this lane's stage writes, before the bulk copies read them
-    __syncwarp();
-    if (lane == 0) {
-      uint8_t *blk = group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB);
-      if (blk) {
-        if (cp.kind == 0) {
-          bulk_s2g(blk + off_kc(BITS), stage, CT);
-          bulk_s2g(blk + off_ks(BITS), meta, 4 * 2 * kD);
-        } else {
-          bulk_s2g(blk + off_vc(BITS), stage, CT);
-          bulk_s2g(blk + off_vs(BITS), meta, 4 * 2 * kG);
-        }
-      } else if (cp.kind == 0) {
-        set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
-      }
-    }
+      value_tile<BITS>(tile, blk, lane);
+    __syncwarp();  // every lane's reads of the slot are done before it is refilled
     ++cseq;
     top_up();
     if (u + 1 < ub) next_tile(cp, geo, new_len, max_new);
@@ -481,7 +467,6 @@ __global__ void __launch_bounds__(TileSmem<BITS>::WARPS * 32, 1)
     if (lane == 0) set_status(geo.status, KVQ_STATUS_TIMEOUT);
     for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
   }
-  if (lane == 0) bulk_wait_all();
 }
 
 // One CTA per SM; false when this geometry is not served here (the caller
@@ -489,7 +474,7 @@ __global__ void __launch_bounds__(TileSmem<BITS>::WARPS * 32, 1)
 template <int BITS>
 static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                   int max_new, cudaStream_t stream) {
-  using TS = TileSmem<BITS>;
+  using TS = TileSmem;
   static int sms[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
