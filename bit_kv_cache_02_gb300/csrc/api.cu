@@ -151,7 +151,8 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads, i
 }
 
 static int decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
-                       uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
+                       uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream,
+                       bool zero_counters) {
   int e = check_buffers(cache);
   if (e) return e;
   if (!q || !out || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
@@ -168,14 +169,14 @@ static int decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16
   if (!aligned(workspace, 256)) return KVQ_ERR_ALIGNMENT;
   uint64_t n = 0;
   cudaError_t ce = kvq::launch_decode(geo, num_q_heads, reinterpret_cast<const __half *>(q), softmax_scale,
-                                      reinterpret_cast<__half *>(out), workspace, plan, max_len,
+                                      reinterpret_cast<__half *>(out), workspace, plan, max_len, zero_counters,
                                       static_cast<cudaStream_t>(stream), &n);
   return from_cuda(ce, n);
 }
 
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
                    uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
-  return decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream);
+  return decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream, false);
 }
 
 
@@ -214,9 +215,9 @@ int kvq_set_wait_test(int64_t limit_cycles, int32_t wait_before_fetch) {
 
 namespace kvq {
 
-int decode_attn_checked(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
-                        uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
-  return ::decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream);
+int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                         uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream) {
+  return ::decode_attn(cache, num_q_heads, q, softmax_scale, out, workspace, workspace_bytes, max_len, stream, true);
 }
 
 }  // namespace kvq

@@ -119,7 +119,8 @@ DecodePlan plan_decode(const Geo &geo, int Hq, int max_len) {
   p.pass_slot0 = kMaxDecodeWarps + pairs;
   const size_t slots = p.pass_slot0 + pairs * p.tail_passes;
   p.off_ml = align256(slots * gq * kD * sizeof(float));
-  p.off_base = p.off_ml + align256(slots * gq * sizeof(float2));
+  p.off_cnt = p.off_ml + align256(slots * gq * sizeof(float2));
+  p.off_base = p.off_cnt + align256(pairs * sizeof(int));
   p.off_hdr = p.off_base + align256((static_cast<size_t>(geo.S) + 1) * sizeof(long long));
   p.off_rope = p.off_hdr + 256;
   p.off_off = p.off_rope + align256(static_cast<size_t>(p.n_base) * 64 * sizeof(float2));
@@ -128,8 +129,8 @@ DecodePlan plan_decode(const Geo &geo, int Hq, int max_len) {
 }
 
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
-                          void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
-                          uint64_t *launches) {
+                          void *workspace, const DecodePlan &p, int max_len, bool zero_counters,
+                          cudaStream_t stream, uint64_t *launches) {
   DecodeArgs a;
   a.geo = geo;
   a.Hq = Hq;
@@ -139,6 +140,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   a.part_o = reinterpret_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float2 *>(ws + p.off_ml);
+  a.counters = reinterpret_cast<int *>(ws + p.off_cnt);
   // batches of up to kInlinePlanSeqs sequences are planned inside the decode
   // kernel; larger ones by a one-CTA plan kernel
   const bool inline_plan = geo.S <= kInlinePlanSeqs;
@@ -153,6 +155,9 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
   cudaError_t e = cudaSuccess;
+  if (zero_counters &&
+      (e = cudaMemsetAsync(a.counters, 0, static_cast<size_t>(geo.S) * geo.H * sizeof(int), stream)) != cudaSuccess)
+    return e;
   if (geo.pre_rope) {
     const int n = (p.n_base + kG) * 64;
     rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(reinterpret_cast<float2 *>(ws + p.off_rope), p.n_base,
@@ -170,7 +175,7 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
     e = launch_paged(a, gq, stream);
   else
     e = geo.bits == 2 ? launch_b<2, false, false, false>(a, gq, stream) : launch_b<4, false, false, false>(a, gq, stream);
-  *launches += inline_plan ? 2 : 3;  // (plan,) decode, merge
+  *launches += inline_plan ? 1 : 2;
   return e;
 }
 

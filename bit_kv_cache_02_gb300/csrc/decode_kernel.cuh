@@ -16,10 +16,9 @@
 // copies completing on per-slot mbarriers, fetching across pair boundaries
 // so the next pair's first groups are in flight while the current one ends.
 // It leaves a partial (max, sum, unnormalized output) per query head for
-// each pair it touches; a small merge kernel launched right behind it
-// combines each pair's partials with a log-sum-exp and writes the fp16
-// output.  No CTA-wide synchronization happens after start-up, and no warp
-// waits on another.
+// each pair it touches; the warp that completes a pair's partial count
+// merges them with a log-sum-exp and writes the fp16 output.  No CTA-wide
+// synchronization happens after start-up.
 
 // Scores over a group use mma.sync m16n8k16 with the 32 tokens as M, the
 // channels as K and the query as N: the A operand comes straight from the
@@ -55,6 +54,7 @@ struct DecodeArgs {
   float zscale;             // softmax scale * log2(e)
   float *part_o;            // [slots][GQ][D] unnormalized partial outputs
   float2 *part_ml;          // [slots][GQ] (max, sum) in log2 units
+  int *counters;            // [S][Hkv] partials finished: zero on entry, left zero on exit
   long long *base;          // [S + 1] first work unit of each sequence (plan kernel), or
                             // null when the decode kernel plans by itself
   PlanHeader *plan;         // total work units (plan kernel)
@@ -606,7 +606,6 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     fence_mbar_init();
   }
   __syncthreads();  // the only CTA-wide barrier: from here each warp runs alone
-  griddep_launch_dependents();  // the merge kernel may start its CTAs as these retire
 
   const int NW = a.nw, gw = blockIdx.x * kWarps + warp;
   if (gw >= NW) return;
@@ -803,6 +802,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     __syncwarp();  // the previous pair's reads of q_s are done
     for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
     __syncwarp();
+    int npart = 0;
 
     // ------------------ window / sink passes whose first unit is ours
     for (int k = 0; k < tp; ++k) {
@@ -922,6 +922,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
         *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
         if (lane == 0) a.part_ml[slot * GQ + hh] = make_float2(mh[hh], lh[hh]);
       }
+      ++npart;
     }
 
     // ------------------------------------------- packed groups of our range
@@ -1282,8 +1283,53 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
       }
       if (SP) __syncwarp();
       if (head_valid && g == 0) a.part_ml[slot * GQ + q] = make_float2(m_run, l_run);
+      ++npart;
     }
 
+    // ---- the warp completing the pair's count merges its partials; lane
+    // 0's acq_rel add publishes this warp's partials (ordered before it by
+    // the warp barrier) and observes every other warp's
+    __syncwarp();
+    const Touching tw = touching_warps(P0, P1, W, NW);
+    const int expect = tp + tw.n;
+    int last = 0;
+    if (lane == 0) last = atom_add_acq_rel(&a.counters[pair], npart) + npart == expect;
+    if (__shfl_sync(kFull, last, 0)) {
+      __threadfence();
+      if (lane == 0) a.counters[pair] = 0;  // ready for the next call
+      for (int hh = 0; hh < GQ; ++hh) {
+        float M = -INFINITY;
+        for (int k = lane; k < tp; k += 32)
+          M = fmaxf(M, __ldcg(&a.part_ml[(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k) * GQ + hh]).x);
+        for (int i = lane; i < tw.n; i += 32)
+          M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(tw.at(i)) + pair) * GQ + hh]).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accg = acc;  // window passes, groups
+        auto add = [&](size_t sl, float4 &to) {
+          const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
+          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
+          const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+          Ls = fmaf(ml.y, wgt, Ls);
+          to.x = fmaf(ov.x, wgt, to.x);
+          to.y = fmaf(ov.y, wgt, to.y);
+          to.z = fmaf(ov.z, wgt, to.z);
+          to.w = fmaf(ov.w, wgt, to.w);
+        };
+        if (M != -INFINITY) {
+          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k, acc);
+#pragma unroll 4
+          for (int i = 0; i < tw.n; ++i) add(static_cast<size_t>(tw.at(i)) + pair, accg);
+        }
+        if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
+        acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);
+        const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
+        __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
+        op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      }
+    }
     if (P1 >= ub) break;
     if (++h == H) {
       h = 0;
@@ -1298,88 +1344,6 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     // valid cache blocks, so they complete; the wait keeps its own default
     // bound (about two seconds) whatever limit gave up above
     for (; cseq < fseq; ++cseq) mbar_wait_bounded(&full[cseq % NS], (cseq / NS) & 1);
-  }
-}
-
-// ------------------------------------------------------------------- merge
-//
-// The log-sum-exp merge of every pair's partial results, one warp per
-// (sequence, KV head), launched right after the decode kernel as its
-// programmatic dependent: its CTAs take the SMs as the decode CTAs retire and
-// wait there until the decode grid has completed.  Separate from the decode
-// kernel so that no decode warp waits on a cross-warp count at a pair's end
-// or merges on the critical path.  The partials of pair (s, h): one per
-// window pass (slot pass_slot0 + pair * tail_passes + k, k < tp) and one per
-// warp whose unit range meets the pair's [P0, P1) (slot warp + pair), each
-// an unnormalized output row and its (max, sum) in log2 units per query
-// head.  Lane L holds channels 4L .. 4L+3.
-template <int GQ, bool ROT>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a) {
-  griddep_wait();
-  const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int S = a.geo.S, H = a.geo.H;
-  if (pair >= S * H) return;
-  const int s = pair / H, h = pair - s * H;
-  Split spl;
-  int tp, ng;
-  const int u = seq_units(a, s, spl, tp, ng);
-  if (u == 0) return;  // nothing to attend: the row was zeroed by the plan
-  long long W, sbase;
-  if (a.base) {
-    W = a.plan->total;
-    sbase = a.base[s];
-  } else {  // the prefix the decode kernel derived: units per head of all sequences / of those before s
-    long long tot = 0, before = 0;
-    for (int s2 = lane; s2 < S; s2 += 32) {
-      Split sp2;
-      int tp2, ng2;
-      const int v = seq_units(a, s2, sp2, tp2, ng2);
-      tot += v;
-      before += s2 < s ? v : 0;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      tot += __shfl_xor_sync(kFull, tot, off);
-      before += __shfl_xor_sync(kFull, before, off);
-    }
-    W = tot * H;
-    sbase = before * H;
-  }
-  const long long P0 = sbase + static_cast<long long>(h) * u, P1 = P0 + u;
-  const Touching tw = touching_warps(P0, P1, W, a.nw);
-  const size_t pass0 = a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes;
-  const size_t orow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * kD;
-  for (int hh = 0; hh < GQ; ++hh) {
-    float M = -INFINITY;
-    for (int k = lane; k < tp; k += 32) M = fmaxf(M, __ldcg(&a.part_ml[(pass0 + k) * GQ + hh]).x);
-    for (int i = lane; i < tw.n; i += 32)
-      M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(tw.at(i)) + pair) * GQ + hh]).x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    float Ls = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accg = acc;  // window passes, groups
-    auto add = [&](size_t sl, float4 &to) {
-      const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
-      const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
-      const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-      Ls = fmaf(ml.y, wgt, Ls);
-      to.x = fmaf(ov.x, wgt, to.x);
-      to.y = fmaf(ov.y, wgt, to.y);
-      to.z = fmaf(ov.z, wgt, to.z);
-      to.w = fmaf(ov.w, wgt, to.w);
-    };
-    if (M != -INFINITY) {
-      for (int k = 0; k < tp; ++k) add(pass0 + k, acc);
-#pragma unroll 4
-      for (int i = 0; i < tw.n; ++i) add(static_cast<size_t>(tw.at(i)) + pair, accg);
-    }
-    if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
-    acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);
-    const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
-    __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
-    op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-    op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
   }
 }
 
@@ -1430,22 +1394,6 @@ static cudaError_t kernel_slots(int &per_sm, int &n_sm, int &bytes_out) {
   return cudaSuccess;
 }
 
-// The merge kernel after a decode launch, as its programmatic dependent.
-template <int GQ, bool ROT>
-static cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.geo.S * a.geo.H + 3) / 4);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<GQ, ROT>, a);
-}
-
 // Warps one launch spreads the work over: every resident warp of the device
 // (one wave of persistent CTAs), at most kMaxDecodeWarps, or the override.
 template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
@@ -1462,8 +1410,7 @@ static cudaError_t launch_t(DecodeArgs a, cudaStream_t stream) {
     if ((e = launch_plan(a, stream)) != cudaSuccess) return e;
   }
   decode_kernel<BITS, GQ, ROPE, KPT, PAGED, ROT, SP><<<(nw + kWarps - 1) / kWarps, kWarps * 32, bytes, stream>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_merge<GQ, ROT>(a, stream);
+  return cudaGetLastError();
 }
 
 template <int BITS, int GQ, bool PAGED, bool ROT, bool SP>

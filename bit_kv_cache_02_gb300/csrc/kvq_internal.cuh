@@ -86,6 +86,13 @@ __host__ __device__ inline Split split_len(int L, int ns, int R) {
   return sp;
 }
 
+// atomicAdd with acquire-release semantics at GPU scope; returns the old value.
+__device__ inline int atom_add_acq_rel(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ inline void set_status(int *status, int bit) {
   if (status) atomicOr(status, bit);
 }
@@ -178,15 +185,6 @@ __device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long lo
   return true;
 }
 
-// Programmatic dependent launch: let the grid launched next on this stream
-// (with the programmatic serialization attribute) start its CTAs, and, in
-// that grid, wait until the previous grid has completed and its memory
-// operations are visible.  Without a dependent launch both are no-ops.
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // 2^x on the special-function unit (approximate, flushes subnormal results
 // to zero; softmax weights that small do not matter).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -237,12 +235,12 @@ constexpr int kMaxDecodeWarps = 2560;
 
 // Workspace plan of one decode call: window passes per (sequence, KV head)
 // at most, RoPE base rows, and the byte offsets of the workspace regions
-// (partial outputs, partial (max, sum), per-sequence work prefix, plan
-// header, RoPE tables), each 256-byte aligned.
+// (partial outputs, partial (max, sum), merge counters, per-sequence work
+// prefix, plan header, RoPE tables), each 256-byte aligned.
 struct DecodePlan {
   int tail_passes, n_base;
   size_t pass_slot0;
-  size_t off_ml, off_base, off_hdr, off_rope, off_off, bytes;
+  size_t off_ml, off_cnt, off_base, off_hdr, off_rope, off_off, bytes;
 };
 
 cudaError_t launch_quant_append(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
@@ -258,12 +256,12 @@ cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half
 cudaError_t launch_dequant(const Geo &geo, float *k_out, float *v_out, cudaStream_t stream, uint64_t *launches);
 DecodePlan plan_decode(const Geo &geo, int Hq, int max_len);
 cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax_scale, __half *out,
-                          void *workspace, const DecodePlan &p, int max_len, cudaStream_t stream,
-                          uint64_t *launches);
-// kv_decode_attn's argument checks and launch, for the entry points built on
-// it (kv_decode_attn_noalloc).
-int decode_attn_checked(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
-                        uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream);
+                          void *workspace, const DecodePlan &p, int max_len, bool zero_counters,
+                          cudaStream_t stream, uint64_t *launches);
+// kv_decode_attn that first clears the workspace's merge counters (for
+// scratch shared by calls of different geometries).
+int decode_attn_clearing(const kvq_cache *cache, int32_t num_q_heads, const uint16_t *q, float softmax_scale,
+                         uint16_t *out, void *workspace, size_t workspace_bytes, int32_t max_len, void *stream);
 int set_decode_warps(int warps);
 // Test aid: cycle limit of the decode kernel's pipeline waits (0: the
 // default) and whether each warp's first wait comes before its first copy.

@@ -39,8 +39,9 @@ extern "C" int kv_decode_attn_noalloc(const kvq_cache *cache, int32_t num_q_head
   if (e != KVQ_OK) return e;
   // Arguments are checked exactly as kv_decode_attn checks them, then a
   // geometry whose workspace exceeds the array gets KVQ_ERR_WORKSPACE; either
-  // way nothing is enqueued.  Every part of the workspace a call reads was
-  // written earlier in the same call, so calls of any geometry can share it.
-  return kvq::decode_attn_checked(cache, num_q_heads, q, softmax_scale, out, scratch, kScratchBytes, max_len,
-                                  stream);
+  // way nothing is enqueued.  The array is shared by calls of every
+  // geometry, so each call clears its own merge counters instead of relying
+  // on the previous call to leave them zero.
+  return kvq::decode_attn_clearing(cache, num_q_heads, q, softmax_scale, out, scratch, kScratchBytes, max_len,
+                                   stream);
 }

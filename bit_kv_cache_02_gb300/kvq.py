@@ -202,7 +202,7 @@ def kv_decode_workspace_bytes(cache: KVCache, num_q_heads: int, max_len: int) ->
 
 
 def alloc_workspace(cache: KVCache, num_q_heads: int, max_len: int):
-    """A torch-allocated workspace for kv_decode_attn (256-byte
+    """A torch-allocated, zero-filled workspace for kv_decode_attn (256-byte
     aligned); it stays valid for calls on caches of this geometry."""
     n = kv_decode_workspace_bytes(cache, num_q_heads, max_len)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=cache.blocks.device)

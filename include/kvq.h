@@ -236,11 +236,12 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  *   out     [S][Hq][D] fp16, written for every row (zeros when seq_len is 0).
  *   workspace, workspace_bytes  device scratch of at least
  *           kv_decode_workspace_bytes(cache, num_q_heads, max_len) bytes,
- *           256-byte aligned, used by the call's kernels only while they run.
- *           It needs no initialization: every part a call reads was written
- *           earlier by the same call, so one workspace can serve calls of
- *           any geometry that fits it, as long as they do not overlap on the
- *           GPU.
+ *           256-byte aligned, owned by the library between calls.  It must
+ *           be zero-filled before its first use with a given cache geometry
+ *           and num_q_heads: the call's merge counters live in it, and every
+ *           call that ends without KVQ_STATUS_TIMEOUT leaves them zero again
+ *           (so no clearing step runs per call).  After a timeout, or before
+ *           reusing it for another geometry, zero it again.
  *   max_len host bound on every seq_len (sizes the RoPE table); a
  *           sequence longer than max_len gets a zero output row and sets
  *           KVQ_STATUS_MAX_LEN.
@@ -249,15 +250,14 @@ int64_t kv_decode_workspace_bytes(const kvq_cache *cache, int32_t num_q_heads,
  * rotate-half RoPE at their absolute position); values likewise.  The work
  * of all (sequence, KV head) pairs -- 32-token passes over the fp16 sink and
  * window, then packed groups -- is cut into equal contiguous ranges, one per
- * warp; the kernel dequantizes in registers, forms scores and runs an
- * online softmax over each range, and the merge kernel combines each pair's
+ * warp; the kernel dequantizes in registers, forms scores, runs an online
+ * softmax over each range, and the last range of a pair to finish merges its
  * partials (log-sum-exp).  Every option of the descriptor is honoured:
  * per-token key scales, outlier entries (each adds q . (x - min) to its
  * token's score, or p (x - min) to its channel's output), the rotation
  * (groups scored with H q, their value sum rotated back), and the block
- * table.  Enqueues the decode kernel and, as its programmatic dependent
- * launch, a merge kernel, plus a plan kernel (work prefix over the
- * sequences) when S > 256 and a RoPE table kernel when pre_rope.
+ * table.  Enqueues the decode kernel, plus a plan kernel (work prefix over
+ * the sequences) when S > 256 and a RoPE table kernel when pre_rope.
  */
 int kv_decode_attn(const kvq_cache *cache, int32_t num_q_heads,
                    const uint16_t *q, float softmax_scale, uint16_t *out,
