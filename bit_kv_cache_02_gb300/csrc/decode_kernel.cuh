@@ -344,6 +344,10 @@ static __device__ __forceinline__ uint32_t key_word(const uint8_t *kc, int t, in
 static_assert(KVQ_RING_RAMP == 0 || KVQ_RING_RAMP >= 2, "the group loop consumes two slots at a time");
 constexpr int kPassUnits = KVQ_PASS_UNITS;
 constexpr int kInlinePlanSeqs = 256;  // larger batches use the plan kernel
+#ifndef KVQ_MERGE_BATCH
+#define KVQ_MERGE_BATCH 8
+#endif
+constexpr int kMergeBatch = KVQ_MERGE_BATCH;  // partials a merge loads at once (more: in a loop)
 
 struct PlanHeader {
   long long total;  // W
@@ -1297,19 +1301,12 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     if (__shfl_sync(kFull, last, 0)) {
       __threadfence();
       if (lane == 0) a.counters[pair] = 0;  // ready for the next call
+      const size_t pass0 = a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes;
       for (int hh = 0; hh < GQ; ++hh) {
         float M = -INFINITY;
-        for (int k = lane; k < tp; k += 32)
-          M = fmaxf(M, __ldcg(&a.part_ml[(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k) * GQ + hh]).x);
-        for (int i = lane; i < tw.n; i += 32)
-          M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(tw.at(i)) + pair) * GQ + hh]).x);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
         float Ls = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), accg = acc;  // window passes, groups
-        auto add = [&](size_t sl, float4 &to) {
-          const float2 ml = __ldcg(&a.part_ml[sl * GQ + hh]);
-          const float4 ov = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
+        auto add = [&](const float2 ml, const float4 ov, float4 &to) {
           const float wgt = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
           Ls = fmaf(ml.y, wgt, Ls);
           to.x = fmaf(ov.x, wgt, to.x);
@@ -1317,10 +1314,44 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           to.z = fmaf(ov.z, wgt, to.z);
           to.w = fmaf(ov.w, wgt, to.w);
         };
-        if (M != -INFINITY) {
-          for (int k = 0; k < tp; ++k) add(a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k, acc);
+        auto slot_of = [&](int i) -> size_t { return i < tp ? pass0 + i : static_cast<size_t>(tw.at(i - tp)) + pair; };
+        const int np = tp + tw.n;
+        if (np <= kMergeBatch) {
+          // every partial's loads issued together: one L2 round trip
+          float2 ml[kMergeBatch];
+          float4 ov[kMergeBatch];
+#pragma unroll
+          for (int i = 0; i < kMergeBatch; ++i) {
+            ml[i] = make_float2(-INFINITY, 0.f);
+            ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < np) {
+              const size_t sl = slot_of(i);
+              ml[i] = __ldcg(&a.part_ml[sl * GQ + hh]);
+              ov[i] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kMergeBatch; ++i) M = fmaxf(M, ml[i].x);
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kMergeBatch; ++i)
+              if (i < np) add(ml[i], ov[i], i < tp ? acc : accg);
+          }
+        } else {
+          for (int k = lane; k < tp; k += 32) M = fmaxf(M, __ldcg(&a.part_ml[(pass0 + k) * GQ + hh]).x);
+          for (int i = lane; i < tw.n; i += 32)
+            M = fmaxf(M, __ldcg(&a.part_ml[(static_cast<size_t>(tw.at(i)) + pair) * GQ + hh]).x);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+          auto add_slot = [&](size_t sl, float4 &to) {
+            add(__ldcg(&a.part_ml[sl * GQ + hh]),
+                __ldcg(reinterpret_cast<const float4 *>(a.part_o + (sl * GQ + hh) * kD) + lane), to);
+          };
+          if (M != -INFINITY) {
+            for (int k = 0; k < tp; ++k) add_slot(pass0 + k, acc);
 #pragma unroll 4
-          for (int i = 0; i < tw.n; ++i) add(static_cast<size_t>(tw.at(i)) + pair, accg);
+            for (int i = 0; i < tw.n; ++i) add_slot(static_cast<size_t>(tw.at(i)) + pair, accg);
+          }
         }
         if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
         acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);
