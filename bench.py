@@ -63,6 +63,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     p.add_argument("--warps", type=int, default=0, help="warps a decode launch cuts its work into (0: library's choice)")
+    p.add_argument("--no-configs", action="store_true", help="skip the decode/quantize roofline of the other workloads")
     return p.parse_args()
 
 
@@ -470,6 +471,74 @@ def run_e2e(kvq, w, caches, layers, k_new, qs, ones, outs, ws, max_len, lens0, w
                            "synchronized"}
 
 
+# ------------------------------------------------- the other workloads
+
+CONFIG_WORKLOADS = ("tiny", "llama3_8b_gqa_2bit", "llama3_8b_gqa_4bit", "long_1m", "kvquant_prerope")
+
+
+def run_config(kvq, name, device, replays, peak):
+    """One workload besides the headline one, timed as the headline is:
+    caches prefilled to the workload's own state (context + its decode
+    tokens), the prefill's kv_quant_append timed per layer with CUDA events,
+    then K replays of a CUDA graph of kv_decode_attn over the layers.  Two
+    layers (each cache larger than L2, so the pair of them is far larger)
+    for multi-layer workloads; the one-layer workloads as they are (the
+    million-token cache is 3.25 GiB; Tiny is launch-bound)."""
+    w = synth.WORKLOADS[name]
+    layers = min(w.layers, 2)
+    state = synth.context_lengths(w).astype(np.int64) + w.decode_tokens
+    capacity = int(state.max()) + 8
+    caches, prefill_s = build_caches(kvq, w, layers, state, capacity, device)
+    qs = [synth.queries(w, l, 0, device=device) for l in range(layers)]
+    outs = [torch.empty_like(q) for q in qs]
+    ws = kvq.alloc_workspace(caches[0], w.q_heads, capacity)
+    for l in range(layers):
+        kvq.kv_decode_attn(caches[l], qs[l], outs[l], ws, capacity)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l in range(layers):
+            kvq.kv_decode_attn(caches[l], qs[l], outs[l], ws, capacity)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    for c in caches:
+        if int(c.status.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(c.status.item())}")
+    call_s = e0.elapsed_time(e1) / 1e3 / (replays * layers)
+    dbytes = decode_bytes(state, w)
+    qbytes = prefill_bytes(state, w)
+    q_s = statistics.median(prefill_s)
+    out = {"state_tokens_mean": float(state.mean()), "layers_timed": layers, "replays": replays,
+           "decode_us": call_s * 1e6, "algorithmic_bytes": dbytes, "achieved_gbs": dbytes / call_s / 1e9,
+           "frac": dbytes / call_s / 1e9 / peak, "context_tokens_per_s_per_layer": float(state.sum()) / call_s,
+           "quantize_us": q_s * 1e6, "quantize_bytes": qbytes, "quantize_frac": qbytes / q_s / 1e9 / peak}
+    del caches, qs, outs, ws, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_configs(args, device, peak):
+    from bit_kv_cache_02_gb300 import build
+    build.build()
+    from bit_kv_cache_02_gb300 import kvq
+    res = {}
+    for name in CONFIG_WORKLOADS:
+        if name == args.workload:
+            continue
+        try:
+            res[name] = run_config(kvq, name, device, max(args.steps, 10), peak)
+        except Exception as e:  # one workload's failure is reported, not fatal
+            res[name] = {"unavailable": f"{type(e).__name__}: {e}"}
+    return res
+
+
 # ------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -687,9 +756,13 @@ def main():
         except Exception as e:  # the single-core figure stands on its own
             cpu["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"}
     r = run_ours(args, w, layers, rank, world, local)
+    peaks, which = measured_peaks()
+    configs = None
+    if not args.no_configs:
+        torch.cuda.empty_cache()
+        configs = run_configs(args, torch.device("cuda", local), float(peaks["hbm_gbs"]))
     if rank != 0:
         return
-    peaks, which = measured_peaks()
     achieved = r["bytes_avg"] / r["attn_avg_s"] / 1e9
     peak = float(peaks["hbm_gbs"])
     traffic = ncu_traffic(f"decode_attn_{w.name}.md", r["bytes_avg"])
@@ -711,6 +784,7 @@ def main():
                      "frac": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9 / peak,
                      "algorithmic_bytes": r["prefill"]["bytes_per_layer"], "traffic": q_traffic,
                      "us": r["prefill"]["seconds_per_layer"] * 1e6},
+        "configs": configs,
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
         "gpu_launches": r["launches"],
