@@ -36,23 +36,36 @@ def _inputs():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "kvq.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libkvq.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+# The debug build: every kernel checks the index arithmetic it does on the
+# device and records KVQ_STATUS_BOUNDS instead of making an access out of
+# range (include/kvq.h).  Same sources, its own objects and library.
+DEBUG_LIB = os.path.join(BUILD, "debug", "libkvq_debug.so")
+
+
+def build_debug(force: bool = False) -> str:
+    return build(force=force, extra_flags=("-DKVQ_DEBUG_BOUNDS",), lib=DEBUG_LIB,
+                 build_dir=os.path.join(BUILD, "debug"))
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB, build_dir: str = BUILD) -> str:
+    """Compile and link libkvq.so (or `lib`, from objects in `build_dir`);
+    returns its path."""
+    if not force and up_to_date(lib):
+        return lib
+    BUILD_ = build_dir
+    os.makedirs(BUILD_, exist_ok=True)
     cc = nvcc()
     inc = ["-I", os.path.join(ROOT, "include")]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(BUILD_, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, *inc, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -152,6 +152,8 @@ cudaError_t launch_decode(const Geo &geo, int Hq, const __half *q, float softmax
   a.max_len = max_len;
   a.wait_limit = g_wait_limit ? g_wait_limit : kWaitLimitCycles;
   a.wait_before_fetch = g_wait_before_fetch;
+  a.n_slots = p.pass_slot0 + static_cast<size_t>(geo.S) * geo.H * p.tail_passes;
+  a.n_base = p.n_base;
   a.rope_base = reinterpret_cast<const float2 *>(ws + p.off_rope);
   a.rope_off = reinterpret_cast<const float2 *>(ws + p.off_off);
   cudaError_t e = cudaSuccess;

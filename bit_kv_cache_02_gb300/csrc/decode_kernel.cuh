@@ -64,6 +64,8 @@ struct DecodeArgs {
   int max_len;              // host bound on seq_len the plan was sized for
   long long wait_limit;     // SM cycles a ring wait may last before it gives up
   int wait_before_fetch;    // test aid: first ring wait before any copy is issued
+  size_t n_slots;           // partial slots in the workspace (bounds checks)
+  int n_base;               // rows of rope_base (bounds checks)
   const float2 *rope_base;  // [n_base][64]: cos, sin of (num_sink + 32 r) * omega_i
   const float2 *rope_off;   // [32][64]: cos, sin of delta * omega_i
 };
@@ -772,10 +774,15 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           const unsigned pb = static_cast<unsigned>(geo.table[blk]);
           blk = pb < static_cast<unsigned>(geo.num_blocks) ? pb : 0u;
         }
-        const uint8_t *src = geo.blocks + blk * BB;
-        fence_proxy_async();  // generic reads of the slot before the async write
-        mbar_arrive_expect_tx(&full[slot], BB);
-        bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
+        // (a skipped copy leaves its wait to give up: the warp then stops)
+        if (KVQ_IN_BOUNDS(geo.status, fg, geo.max_groups) &&
+            KVQ_IN_BOUNDS(geo.status, blk, PAGED ? static_cast<size_t>(geo.num_blocks)
+                                                 : static_cast<size_t>(S) * H * geo.max_groups)) {
+          const uint8_t *src = geo.blocks + blk * BB;
+          fence_proxy_async();  // generic reads of the slot before the async write
+          mbar_arrive_expect_tx(&full[slot], BB);
+          bulk_g2s(ring + slot * BB, src, BB, &full[slot]);
+        }
       }
       ++fseq;
       if (++fg >= fg_end) fetch_next_pair();
@@ -804,7 +811,9 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
     const int pair = s * H + h;
     const size_t orow0 = (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * GQ) * kD;
     __syncwarp();  // the previous pair's reads of q_s are done
-    for (int i = lane; i < GQ * kD; i += 32) q_s[i] = __half2float(a.q[orow0 + i]);
+    for (int i = lane; i < GQ * kD; i += 32)
+      q_s[i] = KVQ_IN_BOUNDS(geo.status, orow0 + i, static_cast<size_t>(S) * a.Hq * kD) ? __half2float(a.q[orow0 + i])
+                                                                                        : 0.f;
     __syncwarp();
     int npart = 0;
 
@@ -826,11 +835,11 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
         const __half *kp;
         if (i < spl.nsink) {
           pos = i;
-          kp = geo.k_sink + (sh * geo.ns + i) * kD;
+          kp = geo.k_sink + (KVQ_IN_BOUNDS(geo.status, i, geo.ns) ? (sh * geo.ns + i) * kD : 0);
         } else {
           const int slot = i - spl.nsink;
           pos = spl.nsink + spl.Lq + slot;
-          kp = geo.k_res + (sh * geo.R + slot) * kD;
+          kp = geo.k_res + (KVQ_IN_BOUNDS(geo.status, slot, geo.R) ? (sh * geo.R + slot) * kD : 0);
         }
         const int sidx = pos - geo.ns;  // stream index (negative for the sink)
         // the key row in flight at once (in two halves for four query heads,
@@ -856,7 +865,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           for (int e = 0; e < 8; ++e) {
             const int ch = 8 * c + e;
             float k1 = __half2float(ha[e]), k2 = __half2float(hb[e]);
-            if (ROPE && sidx >= 0) {
+            if (ROPE && sidx >= 0 && KVQ_IN_BOUNDS(geo.status, sidx >> 5, a.n_base)) {
               const float2 bs = a.rope_base[static_cast<size_t>(sidx >> 5) * 64 + ch];
               const float2 of = roff_s[(sidx & 31) * kRopeOffStride + ch];
               const float cs = bs.x * of.x - bs.y * of.y;
@@ -902,7 +911,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
           if (tb + uu < nt) {
             const __half *vp = it < spl.nsink ? geo.v_sink + (sh * geo.ns + it) * kD
                                               : geo.v_res + (sh * geo.R + (it - spl.nsink)) * kD;
-            raw[uu] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
+            if (KVQ_IN_BOUNDS(geo.status, it < spl.nsink ? it : it - spl.nsink, it < spl.nsink ? geo.ns : geo.R))
+              raw[uu] = *reinterpret_cast<const uint2 *>(vp + 4 * lane);
           }
         }
 #pragma unroll
@@ -922,6 +932,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
       const size_t slot = a.pass_slot0 + static_cast<size_t>(pair) * a.tail_passes + k;
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) {
+        if (!KVQ_IN_BOUNDS(geo.status, slot, a.n_slots)) break;
         float *po = a.part_o + (slot * GQ + hh) * kD;
         *reinterpret_cast<float4 *>(po + 4 * lane) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
         if (lane == 0) a.part_ml[slot * GQ + hh] = make_float2(mh[hh], lh[hh]);
@@ -1135,7 +1146,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
 #pragma unroll
             for (int r2 = 0; r2 < 2; ++r2) {
               const int i = lane + 32 * r2;
-              const float2 b0 = a.rope_base[static_cast<size_t>(gi) * 64 + i];  // (cos, sin) of p0 theta_i
+              const float2 b0 = KVQ_IN_BOUNDS(geo.status, gi, a.n_base) ? a.rope_base[static_cast<size_t>(gi) * 64 + i]
+                                                                         : make_float2(1.f, 0.f);  // (cos, sin) of p0 theta_i
               const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
 #pragma unroll
               for (int hh = 0; hh < GQ; ++hh) {
@@ -1257,7 +1269,8 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
         l_run += __shfl_xor_sync(kFull, l_run, off);
         mu_run += __shfl_xor_sync(kFull, mu_run, off);
       }
-      const size_t slot = static_cast<size_t>(gw) + pair;
+      const size_t slot = KVQ_IN_BOUNDS(geo.status, static_cast<size_t>(gw) + pair, a.pass_slot0)
+                              ? static_cast<size_t>(gw) + pair : 0;
       const float mu_c[2] = {__shfl_sync(kFull, mu_run, (2 * q) & 31), __shfl_sync(kFull, mu_run, (2 * q + 1) & 31)};
       // the value weights' low parts sit in columns 4 .. 7, two lanes up:
       // fold them in.  (A rotating cache leaves this partial in the rotated
@@ -1356,6 +1369,7 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
         if (ROT) accg = hadamard_lane4(accg, lane);  // the groups' values back from H x / D: x = H y
         acc = make_float4(acc.x + accg.x, acc.y + accg.y, acc.z + accg.z, acc.w + accg.w);
         const float inv = M == -INFINITY ? 0.f : 1.f / Ls;
+        if (!KVQ_IN_BOUNDS(geo.status, orow0 + static_cast<size_t>(hh) * kD, static_cast<size_t>(S) * a.Hq * kD)) break;
         __half2 *op = reinterpret_cast<__half2 *>(a.out + orow0 + static_cast<size_t>(hh) * kD) + 2 * lane;
         op[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
         op[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);

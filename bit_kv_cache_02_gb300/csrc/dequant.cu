@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
       if (geo.rot) {
         rows[t][d] = kx;
         rows[kG + t][d] = vx;
-      } else {
+      } else if (KVQ_IN_BOUNDS(geo.status, p0 + t, geo.capacity)) {
         ko[static_cast<size_t>(p0 + t) * kD + d] = kx;
         vo[static_cast<size_t>(p0 + t) * kD + d] = vx;
       }
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
       __syncthreads();
       for (int idx = threadIdx.x; idx < kG * kD; idx += blockDim.x) {
         const int t = idx / kD, d = idx % kD;
+        if (!KVQ_IN_BOUNDS(geo.status, p0 + t, geo.capacity)) continue;
         ko[static_cast<size_t>(p0 + t) * kD + d] = rows[t][d];
         vo[static_cast<size_t>(p0 + t) * kD + d] = rows[kG + t][d];
       }
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(Geo geo, float *__restrict
         kp = geo.k_res + (sh * geo.R + slot) * kD;
         vp = geo.v_res + (sh * geo.R + slot) * kD;
       }
+      if (!KVQ_IN_BOUNDS(geo.status, pos, geo.capacity)) continue;
       ko[static_cast<size_t>(pos) * kD + d] = __half2float(kp[d]);
       vo[static_cast<size_t>(pos) * kD + d] = __half2float(vp[d]);
     }

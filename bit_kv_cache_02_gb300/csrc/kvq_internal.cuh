@@ -97,6 +97,23 @@ __device__ inline void set_status(int *status, int bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Index checks of debug builds (compiled with -DKVQ_DEBUG_BOUNDS): an index
+// outside [0, n) records KVQ_STATUS_BOUNDS and the guarded access is skipped,
+// without a trap; release builds compile the checks away.  They cover the
+// index arithmetic the kernels do on the device (block, window, sink,
+// partial-slot, query, output and table rows), the part no host-side
+// validation can see.
+__device__ inline bool in_bounds(int *status, long long i, long long n) {
+  if (i >= 0 && i < n) return true;
+  set_status(status, KVQ_STATUS_BOUNDS);
+  return false;
+}
+#ifdef KVQ_DEBUG_BOUNDS
+#define KVQ_IN_BOUNDS(status, i, n) ::kvq::in_bounds((status), static_cast<long long>(i), static_cast<long long>(n))
+#else
+#define KVQ_IN_BOUNDS(status, i, n) true
+#endif
+
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ inline uint32_t smem_u32(const void *p) {

@@ -62,8 +62,10 @@ __device__ __forceinline__ void load_group(GroupRegs &r, const Geo &geo, const G
   const int p = threadIdx.x >> 4, c8 = threadIdx.x & 15;
   const size_t sh = static_cast<size_t>(g.s) * geo.H + g.h;
   if (g.i0 >= g.n0) {  // the whole group is new input (every prefill group)
-    const __half *pk = k_new + (sh * max_new + (g.i0 + 2 * p + geo.ns - g.L0)) * kD + c8 * 8;
-    const __half *pv = v_new + (sh * max_new + (g.i0 + 2 * p + geo.ns - g.L0)) * kD + c8 * 8;
+    const int j = g.i0 + 2 * p + geo.ns - g.L0;
+    if (!KVQ_IN_BOUNDS(geo.status, j + 1, max_new) || !KVQ_IN_BOUNDS(geo.status, j, max_new)) return;
+    const __half *pk = k_new + (sh * max_new + j) * kD + c8 * 8;
+    const __half *pv = v_new + (sh * max_new + j) * kD + c8 * 8;
     r.k[0] = *reinterpret_cast<const uint4 *>(pk);
     r.k[1] = *reinterpret_cast<const uint4 *>(pk + kD);
     r.v[0] = *reinterpret_cast<const uint4 *>(pv);
@@ -75,10 +77,12 @@ __device__ __forceinline__ void load_group(GroupRegs &r, const Geo &geo, const G
     const int i = g.i0 + 2 * p + t;
     const __half *pk, *pv;
     if (i < g.n0) {
+      if (!KVQ_IN_BOUNDS(geo.status, i - g.Lq0, geo.R)) continue;
       const size_t off = (sh * geo.R + (i - g.Lq0)) * kD;
       pk = geo.k_res + off;
       pv = geo.v_res + off;
     } else {
+      if (!KVQ_IN_BOUNDS(geo.status, i + geo.ns - g.L0, max_new)) continue;
       const size_t off = (sh * max_new + (i + geo.ns - g.L0)) * kD;
       pk = k_new + off;
       pv = v_new + off;
@@ -497,7 +501,8 @@ __device__ __forceinline__ void quantize_group(QuantSmem &sm, const GroupRegs &r
   fence_proxy_async();  // this thread's block writes, before the bulk copy reads them
   __syncthreads();
   if (tid == 0) {
-    uint8_t *dst = group_block(geo, s, h, i0 / kG, block_bytes(BITS, KPT, SP));
+    uint8_t *dst = KVQ_IN_BOUNDS(geo.status, i0 / kG, geo.max_groups) ? group_block(geo, s, h, i0 / kG, block_bytes(BITS, KPT, SP))
+                                                                      : nullptr;
     if (dst)
       bulk_s2g(dst, sm.blk, block_bytes(BITS, KPT, SP));
     else
@@ -596,9 +601,11 @@ __device__ __forceinline__ void copy_tail(const Geo &geo, int s, int h0, int h1,
       dv = geo.v_sink + (sh * geo.ns + pos) * kD;
     } else {
       const int slot = pos - geo.ns - Lq1;
+      if (!KVQ_IN_BOUNDS(geo.status, slot, geo.R)) continue;
       dk = geo.k_res + (sh * geo.R + slot) * kD;
       dv = geo.v_res + (sh * geo.R + slot) * kD;
     }
+    if (!KVQ_IN_BOUNDS(geo.status, j, max_new)) continue;
     const size_t src = (sh * max_new + j) * kD + c8 * 8;
     reinterpret_cast<uint4 *>(dk)[c8] = *reinterpret_cast<const uint4 *>(k_new + src);
     reinterpret_cast<uint4 *>(dv)[c8] = *reinterpret_cast<const uint4 *>(v_new + src);
@@ -667,8 +674,8 @@ __global__ void __launch_bounds__(kQuantThreads, 4) step_append_kernel(Geo geo, 
             dv = geo.v_sink + (sh * geo.ns + pos) * kD;
           } else {
             const int slot = pos - geo.ns - Lq1;
-            dk = geo.k_res + (sh * geo.R + slot) * kD;
-            dv = geo.v_res + (sh * geo.R + slot) * kD;
+            dk = geo.k_res + (sh * geo.R + (KVQ_IN_BOUNDS(geo.status, slot, geo.R) ? slot : 0)) * kD;
+            dv = geo.v_res + (sh * geo.R + (KVQ_IN_BOUNDS(geo.status, slot, geo.R) ? slot : 0)) * kD;
           }
           reinterpret_cast<uint4 *>(dk)[pc] = pk;
           reinterpret_cast<uint4 *>(dv)[pc] = pv;
@@ -780,6 +787,9 @@ __global__ void __launch_bounds__(256) append_tail_split_kernel(Geo geo, const _
         const int k = idx / C16, c8 = idx % C16;
         const int j = k < j_sink_end ? k : j_win + (k - j_sink_end);
         const int pos = L0 + j;
+        if (!KVQ_IN_BOUNDS(geo.status, pos < geo.ns ? pos : pos - geo.ns - Lq1, pos < geo.ns ? geo.ns : geo.R) ||
+            !KVQ_IN_BOUNDS(geo.status, j, max_new))
+          continue;
         const size_t row = pos < geo.ns ? sh * geo.ns + pos : sh * geo.R + (pos - geo.ns - Lq1);
         dk[u] = reinterpret_cast<uint4 *>((pos < geo.ns ? geo.k_sink : geo.k_res) + row * kD) + c8;
         dv[u] = reinterpret_cast<uint4 *>((pos < geo.ns ? geo.v_sink : geo.v_res) + row * kD) + c8;

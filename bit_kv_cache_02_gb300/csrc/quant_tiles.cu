@@ -429,13 +429,16 @@ __global__ void __launch_bounds__(TileSmem::WARPS * 32, 1)
       const uint32_t slot = fseq % NS;
       const size_t sh = static_cast<size_t>(fp.s) * H + fp.h;
       const int i = fp.f.Lq0 + kG * fp.g + lane;  // stream index of row `lane`
-      const __half *src = i < fp.f.n0
+      const bool from_window = i < fp.f.n0;
+      const __half *src = from_window
                               ? (fp.kind ? geo.v_res : geo.k_res) + (sh * geo.R + (i - fp.f.Lq0)) * kD
                               : (fp.kind ? v_new : k_new) + (sh * max_new + (i + geo.ns - fp.f.L0)) * kD;
       fence_proxy_async();  // this lane's reads of the slot, before the copy that overwrites it
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], kG * kD * 2);
       __syncwarp();
-      bulk_g2s(base + slot * kSlotBytes + lane * kRowPad, src, kD * 2, &full[slot]);
+      // (a skipped row leaves the tile's wait to give up)
+      if (KVQ_IN_BOUNDS(geo.status, from_window ? i - fp.f.Lq0 : i + geo.ns - fp.f.L0, from_window ? geo.R : max_new))
+        bulk_g2s(base + slot * kSlotBytes + lane * kRowPad, src, kD * 2, &full[slot]);
       ++fseq;
       ++fu;
       if (fu < ub) next_tile(fp, geo, new_len, max_new);
@@ -452,7 +455,9 @@ __global__ void __launch_bounds__(TileSmem::WARPS * 32, 1)
       break;
     }
     const uint8_t *tile = base + slot * kSlotBytes;
-    uint8_t *blk = group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB);  // null: a bad table entry
+    uint8_t *blk = KVQ_IN_BOUNDS(geo.status, cp.f.Lq0 / kG + cp.g, geo.max_groups)
+                       ? group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB)  // null: a bad table entry
+                       : nullptr;
     if (!blk && cp.kind == 0 && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
     if (cp.kind == 0)
       key_tile<BITS>(tile, blk, lane);

@@ -15,7 +15,9 @@ from ctypes import c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# KVQ_LIB_PATH selects another build of the same library (the bounds-checking
+# debug build of build.build_debug); by default the in-tree release build.
+LIB_PATH = os.environ.get("KVQ_LIB_PATH") or os.path.join(_HERE, "libkvq.so")
 
 KVQ_OK = 0
 KVQ_STATUS_CAPACITY = 1
@@ -23,6 +25,7 @@ KVQ_STATUS_BAD_LEN = 2
 KVQ_STATUS_TIMEOUT = 4
 KVQ_STATUS_MAX_LEN = 8
 KVQ_STATUS_BAD_BLOCK = 16
+KVQ_STATUS_BOUNDS = 32
 BUF_BLOCKS, BUF_K_RES, BUF_V_RES, BUF_K_SINK, BUF_V_SINK, BUF_SEQ_LEN, BUF_BLOCK_TABLE = range(7)
 
 EXPORTED = (

@@ -60,6 +60,9 @@ extern "C" {
 #define KVQ_STATUS_BAD_BLOCK  16  /* a block-table entry outside [0, num_blocks):
                                      its group was not written (append) or pool
                                      block 0 was read in its place (decode)   */
+#define KVQ_STATUS_BOUNDS     32  /* builds compiled with KVQ_DEBUG_BOUNDS only:
+                                     an index computed on the device fell
+                                     outside its buffer; the access was skipped */
 
 /* which buffer for kvq_buffer_bytes() */
 #define KVQ_BUF_BLOCKS   0
