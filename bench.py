@@ -135,7 +135,7 @@ def kernel_source_hash(names=("decode_kernel.cuh", "kvq_internal.cuh")):
     return h.hexdigest()[:16]
 
 
-QUANT_SOURCES = ("quant.cu", "kvq_internal.cuh")
+QUANT_SOURCES = ("quant.cu", "quant_tiles.cu", "quant_common.cuh", "kvq_internal.cuh")
 
 
 def ncu_traffic(profile, algorithmic_bytes, sources=("decode_kernel.cuh", "kvq_internal.cuh")):
@@ -517,7 +517,7 @@ def run_config(kvq, name, device, replays, peak):
     q_s = statistics.median(prefill_s)
     out = {"state_tokens_mean": float(state.mean()), "layers_timed": layers, "replays": replays,
            "decode_us": call_s * 1e6, "algorithmic_bytes": dbytes, "achieved_gbs": dbytes / call_s / 1e9,
-           "frac": dbytes / call_s / 1e9 / peak, "context_tokens_per_s_per_layer": float(state.sum()) / call_s,
+           "frac": dbytes / call_s / 1e9 / peak, "traffic": ncu_traffic(f"decode_attn_{name}.md", dbytes), "context_tokens_per_s_per_layer": float(state.sum()) / call_s,
            "quantize_us": q_s * 1e6, "quantize_bytes": qbytes, "quantize_frac": qbytes / q_s / 1e9 / peak}
     del caches, qs, outs, ws, g
     torch.cuda.empty_cache()
