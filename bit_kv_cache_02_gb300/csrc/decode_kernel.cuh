@@ -84,16 +84,23 @@ struct DecodeArgs {
 #define KVQ_DECODE_RING_4BIT 2
 #endif
 
+// Pre-RoPE keys at 2-bit with one query head per KV head score through a
+// per-group table of each channel pair's 16 possible (X, Y) values: rows of
+// 16 float2 padded to kTabStride bytes (the padding keeps the table's
+// 16-byte stores and its reads conflict free).
+constexpr int kTabStride = 136;
+
 template <int BITS, int GQ, bool ROPE, bool KPT, bool SP = false>
 struct WarpSmem {
+  static constexpr bool TAB = ROPE && BITS == 2 && GQ == 1 && !KPT;
   static constexpr int BB = block_bytes(BITS, KPT, SP);
-  static constexpr int NS = ROPE ? (BITS == 2 ? 3 : 2)
+  static constexpr int NS = TAB ? 2 : ROPE ? (BITS == 2 ? 3 : 2)
                             : SP ? ((BITS == 2 && GQ != 2) ? 3 : 2)
                                  : (BITS == 2 ? KVQ_DECODE_RING_2BIT : KVQ_DECODE_RING_4BIT);
   static constexpr int BAR_OFF = NS * BB;
   static constexpr int Q_OFF = (BAR_OFF + NS * 8 + 15) / 16 * 16;
   static constexpr int COEF_OFF = Q_OFF + GQ * kD * 4;            // [GQ][64] float4, then [GQ][64] float2
-  static constexpr int SP_OFF = COEF_OFF + (ROPE ? GQ * 64 * 24 : 0);
+  static constexpr int SP_OFF = COEF_OFF + (TAB ? 64 * kTabStride : ROPE ? GQ * 64 * 24 : 0);
   static constexpr int SP_FLOATS = SP ? GQ * (2 * kG + kD) : 0;
   static constexpr int BYTES = (SP_OFF + SP_FLOATS * 4 + 127) / 128 * 128;
   static_assert(BB % 16 == 0, "bulk copies need 16-byte multiples");
@@ -578,10 +585,76 @@ struct CtaShape {
   static constexpr int kQuads = ROPE ? 3 : (GQ == 4 ? KVQ_DECODE_MIN_BLOCKS_GQ4 : KVQ_DECODE_MIN_BLOCKS);
   static constexpr int kExtra = ROPE ? kG * kRopeOffStride * 8 : 0;  // the in-group rotation table
   static constexpr int kFit = (232448 - kExtra) / WS::BYTES;         // largest opt-in shared memory
-  static constexpr int W = KVQ_DECODE_ONE_CTA ? (4 * kQuads < kFit ? 4 * kQuads : kFit) : 4;
-  static constexpr int MIN_BLOCKS = KVQ_DECODE_ONE_CTA ? 1 : kQuads;
+  // the table kernel: two CTAs of six warps share the SM (12 warps, as the
+  // other pre-RoPE kernels), each CTA one copy of the rotation table
+  static constexpr int W = WS::TAB ? 6 : KVQ_DECODE_ONE_CTA ? (4 * kQuads < kFit ? 4 * kQuads : kFit) : 4;
+  static constexpr int MIN_BLOCKS = WS::TAB ? 2 : KVQ_DECODE_ONE_CTA ? 1 : kQuads;
   static constexpr int BYTES = W * WS::BYTES + kExtra;
+  static_assert(!WS::TAB || MIN_BLOCKS * (BYTES + 1024) <= 233472, "two table CTAs must fit an SM");
 };
+
+// Pre-RoPE score of token t = lane through a per-group table (2-bit codes,
+// one query head per KV head).  With (a, b) the query rotated back to the
+// group's first position, row i of the table holds for every code pair (c1
+// of channel i, c2 of channel i + 64), at entry c1 + 4 c2,
+//   X = c1 (a s_i) + c2 (b s_{i+64}) + (a m_i + b m_{i+64}),
+//   Y = c1 (b s_i) - c2 (a s_{i+64}) + (b m_i - a m_{i+64}),
+// so a token's channel pair costs one 4-bit index, one table load and its
+// in-group offset rotation (cos, sin): score += cos X + sin Y.  The values
+// and their order of operations are those of the coefficient form.  b0[r]:
+// (cos, sin) of the first position's angle for channel pair lane + 32 r.
+static __device__ __forceinline__ float tab_group_dot(const uint8_t *blk, const float *q_s, const float2 (&b0)[2],
+                                                      float *tab, const float2 *roff_s, int lane) {
+  constexpr int RS = kTabStride / 4;  // row stride in floats
+  const float *ks = reinterpret_cast<const float *>(blk + off_ks(2));
+  const float *km = reinterpret_cast<const float *>(blk + off_km(2));
+#pragma unroll
+  for (int r2 = 0; r2 < 2; ++r2) {
+    const int i = lane + 32 * r2;
+    const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
+    const float qa = q_s[i], qb = q_s[i + 64];
+    const float av = fmaf(qa, b0[r2].x, qb * b0[r2].y), bv = fmaf(qb, b0[r2].x, -qa * b0[r2].y);
+    const float cx = av * s1, cy = bv * s2, cz = bv * s1, cw = -av * s2;
+    const float c0x = fmaf(av, m1, bv * m2), c0y = fmaf(bv, m1, -av * m2);
+    float2 *row = reinterpret_cast<float2 *>(tab + i * RS);
+#pragma unroll
+    for (int c2 = 0; c2 < 4; ++c2) {
+      const float ix = fmaf(float(c2), cy, c0x), iy = fmaf(float(c2), cw, c0y);
+#pragma unroll
+      for (int c1 = 0; c1 < 4; ++c1) row[c1 + 4 * c2] = make_float2(fmaf(float(c1), cx, ix), fmaf(float(c1), cz, iy));
+    }
+  }
+  __syncwarp();
+  const int t = lane, uu = (t >> 3) & 3;
+  const uint8_t *kc = blk + off_kc(2);
+  float dot = 0.f;
+#pragma unroll 1
+  for (int qq = 0; qq < 4; ++qq) {
+    // this token's words of lane 4 (t % 8) + qq: word kt holds channels
+    // 16 kt + 8 j + 2 qq + e at bits 16 e + 8 j + 2 (t / 8)
+    const uint4 *lw = reinterpret_cast<const uint4 *>(kc) + (4 * (t & 7) + qq);
+    const uint4 w0 = lw[0], w1 = lw[32];
+    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      // byte 2 e + j of comb: the index c1 + 4 c2 of channel pair 16 kt + 8 j + 2 qq + e
+      const uint32_t lo = (wv[kt] >> (2 * uu)) & 0x03030303u;
+      const uint32_t hi = (wv[kt + 4] >> (2 * uu)) & 0x03030303u;
+      const uint32_t comb = lo | (hi << 2);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 16 * kt + 8 * j + 2 * qq + e;
+          const uint32_t k = (comb >> (8 * (2 * e + j))) & 15u;
+          const float2 xy = *reinterpret_cast<const float2 *>(tab + i * RS + 2 * k);
+          const float2 cs = roff_s[t * kRopeOffStride + i];
+          dot = fmaf(cs.x, xy.x, fmaf(cs.y, xy.y, dot));
+        }
+    }
+  }
+  return dot;
+}
 
 template <int BITS, int GQ, bool ROPE, bool KPT, bool PAGED, bool ROT, bool SP>
 __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, CtaShape<BITS, GQ, ROPE, KPT, SP>::MIN_BLOCKS)
@@ -1143,64 +1216,74 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
             const float *vs = reinterpret_cast<const float *>(blk + off_vs(BITS));
             const float *vm = reinterpret_cast<const float *>(blk + off_vm(BITS));
             const uint8_t *kc = blk + off_kc(BITS);
-#pragma unroll
-            for (int r2 = 0; r2 < 2; ++r2) {
-              const int i = lane + 32 * r2;
-              const float2 b0 = KVQ_IN_BOUNDS(geo.status, gi, a.n_base) ? a.rope_base[static_cast<size_t>(gi) * 64 + i]
-                                                                         : make_float2(1.f, 0.f);  // (cos, sin) of p0 theta_i
-              const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
-#pragma unroll
-              for (int hh = 0; hh < GQ; ++hh) {
-                const float qa = q_s[hh * kD + i], qb = q_s[hh * kD + i + 64];
-                const float av = fmaf(qa, b0.x, qb * b0.y), bv = fmaf(qb, b0.x, -qa * b0.y);
-                coef[hh * 64 + i] = make_float4(av * s1, bv * s2, bv * s1, -av * s2);
-                coef0[hh * 64 + i] = make_float2(fmaf(av, m1, bv * m2), fmaf(bv, m1, -av * m2));
-              }
-            }
-            __syncwarp();
             const int t = lane;
             const int tau = t >> 3, uu = tau % (8 / BITS);
             float dot[GQ];
 #pragma unroll
             for (int hh = 0; hh < GQ; ++hh) dot[hh] = 0.f;
-#pragma unroll 1
-            for (int qq = 0; qq < 4; ++qq) {
-              // this token's words of lane 4 (t % 8) + qq: word kt (2-bit) or
-              // 2 kt + tau / 2 (4-bit) holds channels 16 kt + 8 j + 2 qq + e
-              constexpr int WPL = BITS * 4;  // words per lane
-              const uint4 *lw = reinterpret_cast<const uint4 *>(kc) + (4 * (t & 7) + qq);
-              uint32_t wv[WPL];
+            if constexpr (WS::TAB) {
+              float2 b0[2];
 #pragma unroll
-              for (int m = 0; m < WPL / 4; ++m) {
-                const uint4 c4 = lw[32 * m];
-                wv[4 * m] = c4.x;
-                wv[4 * m + 1] = c4.y;
-                wv[4 * m + 2] = c4.z;
-                wv[4 * m + 3] = c4.w;
+              for (int r2 = 0; r2 < 2; ++r2)  // (cos, sin) of p0 theta_i
+                b0[r2] = KVQ_IN_BOUNDS(geo.status, gi, a.n_base)
+                             ? a.rope_base[static_cast<size_t>(gi) * 64 + lane + 32 * r2]
+                             : make_float2(1.f, 0.f);
+              dot[0] = tab_group_dot(blk, q_s, b0, reinterpret_cast<float *>(ring + WS::COEF_OFF), roff_s, lane);
+            } else {
+#pragma unroll
+              for (int r2 = 0; r2 < 2; ++r2) {
+                const int i = lane + 32 * r2;
+                const float2 b0 = KVQ_IN_BOUNDS(geo.status, gi, a.n_base) ? a.rope_base[static_cast<size_t>(gi) * 64 + i]
+                                                                           : make_float2(1.f, 0.f);  // (cos, sin) of p0 theta_i
+                const float s1 = ks[i], s2 = ks[i + 64], m1 = km[i], m2 = km[i + 64];
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) {
+                  const float qa = q_s[hh * kD + i], qb = q_s[hh * kD + i + 64];
+                  const float av = fmaf(qa, b0.x, qb * b0.y), bv = fmaf(qb, b0.x, -qa * b0.y);
+                  coef[hh * 64 + i] = make_float4(av * s1, bv * s2, bv * s1, -av * s2);
+                  coef0[hh * 64 + i] = make_float2(fmaf(av, m1, bv * m2), fmaf(bv, m1, -av * m2));
+                }
               }
+              __syncwarp();
+#pragma unroll 1
+              for (int qq = 0; qq < 4; ++qq) {
+                // this token's words of lane 4 (t % 8) + qq: word kt (2-bit) or
+                // 2 kt + tau / 2 (4-bit) holds channels 16 kt + 8 j + 2 qq + e
+                constexpr int WPL = BITS * 4;  // words per lane
+                const uint4 *lw = reinterpret_cast<const uint4 *>(kc) + (4 * (t & 7) + qq);
+                uint32_t wv[WPL];
 #pragma unroll
-              for (int kt = 0; kt < 4; ++kt) {
-                const uint32_t wa = BITS == 2 ? wv[kt] : ((tau >> 1) ? wv[2 * kt + 1] : wv[2 * kt]);
-                const uint32_t wb = BITS == 2 ? wv[kt + 4] : ((tau >> 1) ? wv[2 * (kt + 4) + 1] : wv[2 * (kt + 4)]);
+                for (int m = 0; m < WPL / 4; ++m) {
+                  const uint4 c4 = lw[32 * m];
+                  wv[4 * m] = c4.x;
+                  wv[4 * m + 1] = c4.y;
+                  wv[4 * m + 2] = c4.z;
+                  wv[4 * m + 3] = c4.w;
+                }
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+                for (int kt = 0; kt < 4; ++kt) {
+                  const uint32_t wa = BITS == 2 ? wv[kt] : ((tau >> 1) ? wv[2 * kt + 1] : wv[2 * kt]);
+                  const uint32_t wb = BITS == 2 ? wv[kt + 4] : ((tau >> 1) ? wv[2 * (kt + 4) + 1] : wv[2 * (kt + 4)]);
 #pragma unroll
-                  for (int e = 0; e < 2; ++e) {
-                    const int i = 16 * kt + 8 * j + 2 * qq + e;
-                    const int sh = 16 * e + 8 * j + BITS * uu;
-                    // code -> fp32 on the FMA pipe: the field under 2^23
-                    const float c1 = __uint_as_float(((wa >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
-                    const float c2 = __uint_as_float(((wb >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
-                    const float2 cs = roff_s[t * kRopeOffStride + i];
+                  for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int hh = 0; hh < GQ; ++hh) {
-                      const float4 cf = coef[hh * 64 + i];
-                      const float2 c0 = coef0[hh * 64 + i];
-                      const float X = fmaf(c1, cf.x, fmaf(c2, cf.y, c0.x));
-                      const float Y = fmaf(c1, cf.z, fmaf(c2, cf.w, c0.y));
-                      dot[hh] = fmaf(cs.x, X, fmaf(cs.y, Y, dot[hh]));
+                    for (int e = 0; e < 2; ++e) {
+                      const int i = 16 * kt + 8 * j + 2 * qq + e;
+                      const int sh = 16 * e + 8 * j + BITS * uu;
+                      // code -> fp32 on the FMA pipe: the field under 2^23
+                      const float c1 = __uint_as_float(((wa >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                      const float c2 = __uint_as_float(((wb >> sh) & ((1u << BITS) - 1u)) | 0x4B000000u) - 8388608.f;
+                      const float2 cs = roff_s[t * kRopeOffStride + i];
+#pragma unroll
+                      for (int hh = 0; hh < GQ; ++hh) {
+                        const float4 cf = coef[hh * 64 + i];
+                        const float2 c0 = coef0[hh * 64 + i];
+                        const float X = fmaf(c1, cf.x, fmaf(c2, cf.y, c0.x));
+                        const float Y = fmaf(c1, cf.z, fmaf(c2, cf.w, c0.y));
+                        dot[hh] = fmaf(cs.x, X, fmaf(cs.y, Y, dot[hh]));
+                      }
                     }
-                  }
+                }
               }
             }
             const float vsc = vs[t], vmn = vm[t];
