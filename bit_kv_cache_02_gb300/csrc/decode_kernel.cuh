@@ -362,9 +362,9 @@ struct PlanHeader {
   long long total;  // W
 };
 
-// Units of sequence s per KV head (0 when there is nothing to attend).
-static __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Split &spl, int &tp, int &ng) {
-  const int L = a.geo.seq_len[s];
+// Units per KV head of a sequence of length L (0 when there is nothing to
+// attend), and of sequence s.
+static __device__ __forceinline__ int len_units(const DecodeArgs &a, int L, Split &spl, int &tp, int &ng) {
   tp = ng = 0;
   spl.nsink = spl.Lq = spl.r = 0;
   if (L <= 0 || L > a.geo.capacity || L > a.max_len) return 0;
@@ -372,6 +372,9 @@ static __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Spli
   ng = spl.Lq / kG;
   tp = (spl.nsink + spl.r + 31) / 32;
   return kPassUnits * tp + ng;
+}
+static __device__ __forceinline__ int seq_units(const DecodeArgs &a, int s, Split &spl, int &tp, int &ng) {
+  return len_units(a, a.geo.seq_len[s], spl, tp, ng);
 }
 
 // L2 prefetch of one line (no register, no wait).
@@ -697,7 +700,35 @@ __global__ void __launch_bounds__(CtaShape<BITS, GQ, ROPE, KPT, SP>::W * 32, Cta
   // large ones read the plan kernel's prefix.
   long long W, ua, ub, sbase = 0;
   int s_first = 0;
-  if (a.base == nullptr) {
+  if (a.base == nullptr && S <= 32) {
+    // up to 32 sequences: one read of seq_len (lane s holds sequence s)
+    // serves the empty rows, the total and the prefix
+    const int Ls = lane < S ? geo.seq_len[lane] : 0;
+    for (int s2 = gw; s2 < S; s2 += NW) {  // rows of sequences with nothing to attend
+      const int L = __shfl_sync(kFull, Ls, s2);
+      if (L > 0 && L <= geo.capacity && L <= a.max_len) continue;
+      if (lane == 0 && L > a.max_len) set_status(geo.status, KVQ_STATUS_MAX_LEN);
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<size_t>(s2) * a.Hq * kD);
+      for (int i = lane; i < a.Hq * kD / 8; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    Split spl;
+    int tp, ng;
+    const long long v = lane < S ? len_units(a, Ls, spl, tp, ng) : 0;
+    long long incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long t = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += t;
+    }
+    W = __shfl_sync(kFull, incl, 31) * H;
+    ua = gw * W / NW;
+    ub = (gw + 1) * W / NW;
+    if (ua >= ub) return;
+    // the first sequence whose units end past ua (one exists: ua < W)
+    const int idx = __ffs(__ballot_sync(kFull, lane < S && incl * H > ua)) - 1;
+    s_first = idx;
+    sbase = __shfl_sync(kFull, incl - v, idx) * H;
+  } else if (a.base == nullptr) {
     for (int s2 = gw; s2 < S; s2 += NW) {  // rows of sequences with nothing to attend
       const int L = geo.seq_len[s2];
       if (L > 0 && L <= geo.capacity && L <= a.max_len) continue;
