@@ -588,9 +588,10 @@ def test_split_sizes_agree_variants(kvq, variant, warps):
     assert int(cache.status.item()) == 0
 
 
-@pytest.mark.parametrize("S", [200, 300])
+@pytest.mark.parametrize("S", [20, 32, 33, 200, 300])
 def test_many_sequences_with_empty_and_overlong(kvq, S):
-    """Batches planned inside the decode kernel (S <= 256) and by the plan
+    """Batches planned inside the decode kernel from one read of seq_len
+    (S <= 32) or by chunks of 32 sequences (S <= 256), and by the plan
     kernel (S > 256): ragged lengths with empty sequences and sequences
     longer than max_len, whose rows come back zero with
     KVQ_STATUS_MAX_LEN set."""
