@@ -445,6 +445,27 @@ def test_paged_bad_table_entry_sets_status(kvq):
     _attn_close(out[:1], orc.attention(q)[:1])          # sequence 0 is unaffected
 
 
+@pytest.mark.parametrize("S,H,cap", [(1, 2, (1 << 22) + 64), (1, 512, 400)])
+def test_appends_past_the_length_bits(kvq, S, H, cap):
+    """The one-kernel step append and the split tail count arrivals in the
+    bits of seq_len above 22 length bits, so caches of capacity >= 2^22 or
+    with 512 KV heads append through the flush and the one-CTA-per-sequence
+    tail instead: a prefill, one-token appends across a window flush and a
+    chunk leave the oracle's bytes, and attention matches."""
+    T = 300
+    k, v = _rand_kv(S, H, T, seed=H + 7)
+    cache = kvq.KVCache(S, H, cap, bits=2, num_sink=1)
+    orc = oracle.OracleCache(S, H, 400, 2, num_sink=1)  # the oracle only needs room for T tokens
+    pos = 0
+    for step in [150] + [1] * 40 + [110]:
+        sl = np.full(S, step, np.int32)
+        _append(kvq, cache, orc, k[:, :, pos:pos + step], v[:, :, pos:pos + step], sl)
+        pos += step
+    _compare_state(cache, orc)
+    q = _rand_q(S, H, seed=3)
+    _attn_close(_attend(kvq, cache, q, 400), orc.attention(q))
+
+
 def test_decode_step_flush_then_attend(kvq):
     """A window holding R-1 tokens plus one appended token flushes; attention
     then reads only quantized groups."""
