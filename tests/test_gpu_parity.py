@@ -466,6 +466,25 @@ def test_appends_past_the_length_bits(kvq, S, H, cap):
     _attn_close(_attend(kvq, cache, q, 400), orc.attention(q))
 
 
+def test_prefill_of_more_sequences_than_the_tile_kernel_takes(kvq):
+    """The tile kernel flushes batches of up to 2048 sequences; a prefill of
+    2100 ragged sequences goes through the one-group-per-CTA flush kernel
+    and leaves the oracle's bytes, and decode (planned by the plan kernel)
+    matches."""
+    S, H, T = 2100, 1, 70
+    rng = np.random.default_rng(2100)
+    lens = rng.integers(0, T + 1, S).astype(np.int32)
+    k, v = _rand_kv(S, H, T, seed=2101)
+    cache, orc = _build(kvq, S, H, T + 8, 2, R=32)  # up to two groups flushed per sequence
+    _append(kvq, cache, orc, k, v, lens)
+    _compare_state(cache, orc)
+    q = _rand_q(S, H, seed=4)
+    got = _attend(kvq, cache, q, T)
+    keep = lens > 0
+    assert (got[~keep] == 0).all()
+    _attn_close(got[keep], orc.attention(q)[keep])
+
+
 def test_decode_step_flush_then_attend(kvq):
     """A window holding R-1 tokens plus one appended token flushes; attention
     then reads only quantized groups."""
