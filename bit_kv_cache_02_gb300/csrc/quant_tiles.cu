@@ -12,9 +12,10 @@
 // value tile, next group, ...) of every (sequence, KV head) is cut into one
 // contiguous range per warp.  The 32 token rows of a tile reach shared memory
 // through one 256-byte bulk copy per lane (rows from the fp16 window or the
-// new tokens alike), into a ring of slots whose rows are padded to 272 bytes
-// so that both read patterns below are free of bank conflicts; the next tiles
-// are in flight while the current one is quantized.
+// new tokens alike), into the warp's slot (a ring of one by default), whose
+// rows are padded to 272 bytes so that both read patterns below are free of
+// bank conflicts.  A warp's next tile is copied once the current one is
+// packed; the 20 to 24 warps of an SM hide that latency from one another.
 //
 //   key tile:   lane L owns channels 4L .. 4L+3 of all 32 tokens: their
 //               min/max are lane-local, and the lane packs the codes of its
@@ -39,16 +40,33 @@ namespace kvq {
 
 constexpr int kRowPad = 272;                // bytes per token row in a ring slot (256 + 16)
 constexpr int kSlotBytes = kG * kRowPad;    // 8704
+// Ring slots per warp, and warps per CTA (one CTA per SM) at each bit width.
+// One slot measured fastest: the slot is refilled only once its tile is
+// packed, but the smaller shared memory lets 20 (2-bit) or 24 (4-bit) warps
+// share an SM, which hide each other's copy latency and fixed-latency
+// stalls better than 13 warps with two slots each (the register budget that
+// the warp count leaves decides between 20 and 24).
 #ifndef KVQ_TILE_RING
-#define KVQ_TILE_RING 2
+#define KVQ_TILE_RING 1
+#endif
+#ifndef KVQ_TILE_WARPS_2BIT
+#define KVQ_TILE_WARPS_2BIT 20
+#endif
+#ifndef KVQ_TILE_WARPS_4BIT
+#define KVQ_TILE_WARPS_4BIT 24
 #endif
 
 struct TileSmem {  // one warp's shared memory: the ring, then its mbarriers
   static constexpr int NS = KVQ_TILE_RING;  // ring slots
   static constexpr int BAR = NS * kSlotBytes;
   static constexpr int BYTES = (BAR + 8 * NS + 127) / 128 * 128;
-  static constexpr int WARPS = 232448 / BYTES < 16 ? 232448 / BYTES : 16;  // warps per CTA (one CTA per SM)
   static_assert(kSlotBytes % 16 == 0 && kRowPad % 16 == 0, "bulk copies need 16-byte alignment");
+};
+
+template <int BITS>
+struct TileShape {
+  static constexpr int WANT = BITS == 2 ? KVQ_TILE_WARPS_2BIT : KVQ_TILE_WARPS_4BIT;
+  static constexpr int WARPS = 232448 / TileSmem::BYTES < WANT ? 232448 / TileSmem::BYTES : WANT;
 };
 
 // The flush of sequence s in this append: groups ng starting at stream
@@ -362,11 +380,11 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
 
 // ------------------------------------------------------------------ kernel
 
-// Persistent CTAs of WARPS independent warps (one CTA per SM).  Warp gw of
+// Persistent CTAs of TileShape<BITS>::WARPS independent warps (one CTA per SM).  Warp gw of
 // NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
 // flushed) tiles, ordered (sequence, KV head, group, keys / values).
 template <int BITS>
-__global__ void __launch_bounds__(TileSmem::WARPS * 32, 1)
+__global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
     quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int *__restrict__ new_len, int max_new) {
   using TS = TileSmem;
@@ -380,7 +398,8 @@ __global__ void __launch_bounds__(TileSmem::WARPS * 32, 1)
     fence_mbar_init();
   }
   __syncwarp();
-  const int NW = gridDim.x * TS::WARPS, gw = blockIdx.x * TS::WARPS + warp;
+  constexpr int kWarps = TileShape<BITS>::WARPS;
+  const int NW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
   const int S = geo.S, H = geo.H;
 
   // ---- the line: U tiles in all; the first tile of this warp's range
@@ -487,13 +506,13 @@ static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __h
   int n_sm = dev < 64 ? sms[dev] : 0;
   if (n_sm == 0) {
     if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  TS::WARPS * TS::BYTES)) != cudaSuccess)
+                                  TileShape<BITS>::WARPS * TS::BYTES)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev < 64) sms[dev] = n_sm;
   }
-  quant_tiles_kernel<BITS><<<n_sm, TS::WARPS * 32, TS::WARPS * TS::BYTES, stream>>>(geo, k_new, v_new, new_len,
-                                                                                   max_new);
+  constexpr int kWarps = TileShape<BITS>::WARPS;
+  quant_tiles_kernel<BITS><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new, new_len, max_new);
   return cudaGetLastError();
 }
 
