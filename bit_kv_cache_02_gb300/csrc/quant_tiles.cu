@@ -3,7 +3,8 @@
 // Source: "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
 // second paragraph (keys quantized per channel over groups of 32 tokens,
 // values per token, asymmetric min/scale codes) and third paragraph (the
-// window of newest tokens is quantized in blocks when it fills).
+// window of newest tokens is quantized in blocks when it fills); keys
+// grouped per token are the baseline the first paragraph contrasts with.
 //
 // Each group block is made of two independent halves: the key tile (32
 // tokens x 128 channels, one (scale, min) per channel) and the value tile
@@ -268,6 +269,135 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int 
   }
 }
 
+// ------------------------------------------------------ key tile, per token
+//
+// Keys grouped per token (the ablation of per-channel keys): the tile's
+// slices are its 32 tokens, each over the 128 channels.  Lane L still owns
+// channels 4L .. 4L+3 of every token and packs them as key_tile does; a
+// token's min and max are reduced across the warp (a reduce-scatter leaves
+// token t's with lane t, which forms its scale, min and filter constants),
+// and the packing loop fetches each token's constants from its lane.
+
+// Codes of NF fp16 pairs into one word as pack_pairs, with the filter
+// constants of pair f's slice in (rcp[f], c[f]) (both halves of a pair lie
+// in one slice).
+template <int NF>
+__device__ __forceinline__ uint32_t pack_pairs_tok(const uint32_t (&x)[NF], const float (&rcp)[NF],
+                                                   const float (&c)[NF], const float (&sc)[NF], float thr,
+                                                   bool &near) {
+  const f2x magic = f2_pack(kMagic, kMagic);
+  f2x acc = f2_pack(kPackBase, kPackBase);
+  float emax = 0.f;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x[f]));
+    const f2x y = f2_fma(f2_pack(xf.x, xf.y), f2_pack(rcp[f], rcp[f]), f2_pack(c[f], c[f]));
+    const f2x r = f2_sub(f2_add(y, magic), magic);  // rne(y), exact
+    const float2 e = f2_unpack(f2_sub(y, r));
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(emax) : "f"(emax), "f"(e.x), "f"(e.y));
+    acc = f2_fma(r, f2_pack(sc[f], sc[f]), acc);
+  }
+  near = emax > thr;
+  const float2 a = f2_unpack(acc);
+  return __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x5410);
+}
+
+// The same word by the IEEE subtract and divide, pair f in slice (lo[f], scl[f]).
+template <int BITS, int NF>
+__device__ __noinline__ uint32_t pack_pairs_tok_exact(const uint32_t (&x)[NF], const float (&lo)[NF],
+                                                      const float (&scl)[NF], const int (&pos)[NF]) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x[f]));
+    w |= exact_code<BITS>(xf.x, lo[f], scl[f]) << pos[f];
+    w |= exact_code<BITS>(xf.y, lo[f], scl[f]) << (16 + pos[f]);
+  }
+  return w;
+}
+
+template <int BITS>
+__device__ __forceinline__ void key_tile_kpt(const uint8_t *tile, uint8_t *blk, int lane) {
+  constexpr int NU = 8 / BITS, WH = 4 / NU;
+  const float levels = float((1 << BITS) - 1);
+  const int kt = lane >> 2, j = (lane >> 1) & 1, q0 = 2 * (lane & 1);
+  const uint8_t *col = tile + 8 * lane;  // this lane's 8 bytes of token row t at col + t * kRowPad
+  // (min, -max) of this lane's four channels of every token as an fp16 pair,
+  // then the warp's: after the exchanges at distances 16, 8, 4, 2, 1 lane t
+  // holds token t's
+  uint32_t part[kG];
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(col + t * kRowPad);
+    const uint32_t mn = h2min(w.x, w.y), nmx = h2max(w.x, w.y) ^ 0x80008000u;  // -max: the sign bits
+    part[t] = h2min(__byte_perm(mn, nmx, 0x5410), __byte_perm(mn, nmx, 0x7632));
+  }
+#pragma unroll
+  for (int d = kG / 2; d >= 1; d >>= 1) {
+    const bool up = lane & d;
+#pragma unroll
+    for (int i = 0; i < d; ++i) {
+      const uint32_t send = up ? part[i] : part[i + d];
+      const uint32_t keep = up ? part[i + d] : part[i];
+      part[i] = h2min(keep, __shfl_xor_sync(0xffffffffu, send, d));
+    }
+  }
+  const float2 ex = h2_to_f2_pos0(part[0]);  // (min, -max) of token `lane`
+  const float lo = ex.x, hi = __fadd_rn(-ex.y, 0.f);
+  const float scale = __fdiv_rn(__fsub_rn(hi, lo), levels);
+  const SliceQ sq = make_slice(lo, scale, levels);
+  if (blk) {
+    reinterpret_cast<float *>(blk + off_ks(BITS))[lane] = scale;
+    reinterpret_cast<float *>(blk + off_km(BITS, true))[lane] = lo;
+  }
+  float sc[NU];
+  int pos[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    pos[u] = 8 * j + BITS * u;
+    sc[u] = __int_as_float((127 + pos[u]) << 23);
+  }
+#pragma unroll 2
+  for (int wg = 0; wg < 8 * WH; ++wg) {  // (hw, g)
+    const int hw = wg >> 3, g = wg & 7;
+    uint32_t va[NU], vb[NU];
+    float rc[NU], cc[NU];
+    float tol = 0.f;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const int tok = 8 * (hw * NU + u) + g;
+      const uint2 w = *reinterpret_cast<const uint2 *>(col + tok * kRowPad);
+      va[u] = w.x;
+      vb[u] = w.y;
+      rc[u] = __shfl_sync(0xffffffffu, sq.rcp, tok);
+      cc[u] = __shfl_sync(0xffffffffu, sq.c, tok);
+      tol = fmaxf(tol, __shfl_sync(0xffffffffu, sq.tol, tok));
+    }
+    bool na, nb;
+    uint32_t pa = pack_pairs_tok<NU>(va, rc, cc, sc, 0.5f - tol, na);
+    uint32_t pb = pack_pairs_tok<NU>(vb, rc, cc, sc, 0.5f - tol, nb);
+    if (__any_sync(0xffffffffu, na || nb)) {
+      float lou[NU], scu[NU];
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const int tok = 8 * (hw * NU + u) + g;
+        lou[u] = __shfl_sync(0xffffffffu, lo, tok);
+        scu[u] = __shfl_sync(0xffffffffu, scale, tok);
+      }
+      if (na) pa = pack_pairs_tok_exact<BITS, NU>(va, lou, scu, pos);
+      if (nb) pb = pack_pairs_tok_exact<BITS, NU>(vb, lou, scu, pos);
+    }
+    pa |= __shfl_xor_sync(0xffffffffu, pa, 2);
+    pb |= __shfl_xor_sync(0xffffffffu, pb, 2);
+    if ((g >> 2) == j && blk) {
+      uint8_t *codes = blk + off_kc(BITS);
+      const int w = kt * WH + hw;
+      *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0)) = pa;
+      *reinterpret_cast<uint32_t *>(codes + word_offset(w, 4 * g + q0 + 1)) = pb;
+    }
+  }
+}
+
 // -------------------------------------------------------------- value tile
 //
 // Lane L: tokens 2p, 2p+1 (p = L % 16) over channels 64 hf .. 64 hf + 63
@@ -278,7 +408,7 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int 
 // the order (2p + j, 2p + 1 - j), which spreads each quarter warp's 16-byte
 // reads over the eight bank groups; the byte permutes that pair a channel's
 // two tokens undo the order.
-template <int BITS>
+template <int BITS, bool KPT>
 __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, int lane) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
@@ -326,8 +456,8 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
     pq = pair_q(lo.x, hi.x, lo.y, hi.y, levels);
   }
   if (hf == 0 && blk) {
-    reinterpret_cast<float2 *>(blk + off_vs(BITS))[p] = make_float2(pq.sc0, pq.sc1);
-    reinterpret_cast<float2 *>(blk + off_vm(BITS))[p] = make_float2(pq.lo0, pq.lo1);
+    reinterpret_cast<float2 *>(blk + off_vs(BITS, KPT))[p] = make_float2(pq.sc0, pq.sc1);
+    reinterpret_cast<float2 *>(blk + off_vm(BITS, KPT))[p] = make_float2(pq.lo0, pq.lo1);
   }
   float sc[NU];
   int pos[NU];
@@ -383,12 +513,12 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
 // Persistent CTAs of TileShape<BITS>::WARPS independent warps (one CTA per SM).  Warp gw of
 // NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
 // flushed) tiles, ordered (sequence, KV head, group, keys / values).
-template <int BITS>
+template <int BITS, bool KPT>
 __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
     quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int *__restrict__ new_len, int max_new) {
   using TS = TileSmem;
-  constexpr int NS = TS::NS, BB = block_bytes(BITS);
+  constexpr int NS = TS::NS, BB = block_bytes(BITS, KPT);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *base = smem + warp * TS::BYTES;
@@ -478,10 +608,14 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
                        ? group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB)  // null: a bad table entry
                        : nullptr;
     if (!blk && cp.kind == 0 && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
-    if (cp.kind == 0)
-      key_tile<BITS>(tile, blk, lane);
-    else
-      value_tile<BITS>(tile, blk, lane);
+    if (cp.kind == 0) {
+      if (KPT)
+        key_tile_kpt<BITS>(tile, blk, lane);
+      else
+        key_tile<BITS>(tile, blk, lane);
+    } else {
+      value_tile<BITS, KPT>(tile, blk, lane);
+    }
     __syncwarp();  // every lane's reads of the slot are done before it is refilled
     ++cseq;
     top_up();
@@ -493,37 +627,38 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
   }
 }
 
-// One CTA per SM; false when this geometry is not served here (the caller
-// then uses the general flush kernel).
-template <int BITS>
+// One CTA per SM (the attribute is set once per instantiation and device).
+template <int BITS, bool KPT>
 static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                   int max_new, cudaStream_t stream) {
   using TS = TileSmem;
+  constexpr int kWarps = TileShape<BITS>::WARPS;
   static int sms[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int n_sm = dev < 64 ? sms[dev] : 0;
   if (n_sm == 0) {
-    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  TileShape<BITS>::WARPS * TS::BYTES)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS, KPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kWarps * TS::BYTES)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev < 64) sms[dev] = n_sm;
   }
-  constexpr int kWarps = TileShape<BITS>::WARPS;
-  quant_tiles_kernel<BITS><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new, new_len, max_new);
+  quant_tiles_kernel<BITS, KPT><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new, new_len,
+                                                                                  max_new);
   return cudaGetLastError();
 }
 
-bool flush_tiles_serves(const Geo &geo) {
-  return !geo.kpt && !geo.rot && !geo.sparse && geo.S <= kTileFlushMaxSeqs;
-}
+bool flush_tiles_serves(const Geo &geo) { return !geo.rot && !geo.sparse && geo.S <= kTileFlushMaxSeqs; }
 
 cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                int max_new, cudaStream_t stream) {
-  return geo.bits == 2 ? launch_tiles_t<2>(geo, k_new, v_new, new_len, max_new, stream)
-                       : launch_tiles_t<4>(geo, k_new, v_new, new_len, max_new, stream);
+  if (geo.bits == 2)
+    return geo.kpt ? launch_tiles_t<2, true>(geo, k_new, v_new, new_len, max_new, stream)
+                   : launch_tiles_t<2, false>(geo, k_new, v_new, new_len, max_new, stream);
+  return geo.kpt ? launch_tiles_t<4, true>(geo, k_new, v_new, new_len, max_new, stream)
+                 : launch_tiles_t<4, false>(geo, k_new, v_new, new_len, max_new, stream);
 }
 
 }  // namespace kvq
