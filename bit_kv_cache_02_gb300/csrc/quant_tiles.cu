@@ -269,6 +269,65 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int 
   }
 }
 
+// ------------------------------------------------------- rotation pre-pass
+//
+// Walsh-Hadamard rotation of every token row of a tile in place, fp16(H x /
+// 128) ("2-Bit KV Cache Quantization: Memory You Save, Recall You Risk",
+// "Method map: three ways to shrink the cache"; H the Sylvester matrix):
+// the fast transform in fp32 with strides 1, 2, ..., 64 in that order, one
+// IEEE add or subtract per butterfly, the exact scale 1/128 and one fp16
+// rounding, before the tile is quantized.  Four lanes share a row, lane r +
+// 8 q holding channels 32 q .. 32 q + 31 of row r of each pass of 8 rows:
+// strides 1 to 16 are butterflies inside a lane, strides 32 and 64 pair lane
+// L with L ^ 8 and L ^ 16.  (A quarter warp reads 8 rows at one offset, so
+// the 272-byte row padding keeps the reads and writes conflict free.)
+__device__ __forceinline__ void rotate_tile(uint8_t *tile, int lane) {
+  const int r = lane & 7, q = lane >> 3;
+#pragma unroll 1
+  for (int pass = 0; pass < kG / 8; ++pass) {
+    uint4 *p = reinterpret_cast<uint4 *>(tile + (8 * pass + r) * kRowPad + 64 * q);
+    float f[32];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 w = p[k];
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&wv[i]));
+        f[8 * k + 2 * i] = t.x;
+        f[8 * k + 2 * i + 1] = t.y;
+      }
+    }
+#pragma unroll
+    for (int st = 1; st < 32; st <<= 1)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (!(i & st)) {
+          const float a = f[i], b = f[i + st];
+          f[i] = __fadd_rn(a, b);
+          f[i + st] = __fsub_rn(a, b);
+        }
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {
+      const bool upper = (lane & m) != 0;  // this lane holds the b of each butterfly
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, f[i], m);
+        f[i] = upper ? __fsub_rn(o, f[i]) : __fadd_rn(f[i], o);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t wv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        wv[i] = h2_as_u32(__floats2half2_rn(f[8 * k + 2 * i] * 0.0078125f, f[8 * k + 2 * i + 1] * 0.0078125f));
+      p[k] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+  }
+  __syncwarp();  // the rotated rows are read by other lanes next
+}
+
 // ------------------------------------------------------ key tile, per token
 //
 // Keys grouped per token (the ablation of per-channel keys): the tile's
@@ -513,7 +572,7 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
 // Persistent CTAs of TileShape<BITS>::WARPS independent warps (one CTA per SM).  Warp gw of
 // NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
 // flushed) tiles, ordered (sequence, KV head, group, keys / values).
-template <int BITS, bool KPT>
+template <int BITS, bool KPT, bool ROT>
 __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
     quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int *__restrict__ new_len, int max_new) {
@@ -603,11 +662,12 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
       ok = false;
       break;
     }
-    const uint8_t *tile = base + slot * kSlotBytes;
+    uint8_t *tile = base + slot * kSlotBytes;
     uint8_t *blk = KVQ_IN_BOUNDS(geo.status, cp.f.Lq0 / kG + cp.g, geo.max_groups)
                        ? group_block(geo, cp.s, cp.h, cp.f.Lq0 / kG + cp.g, BB)  // null: a bad table entry
                        : nullptr;
     if (!blk && cp.kind == 0 && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
+    if (ROT) rotate_tile(tile, lane);
     if (cp.kind == 0) {
       if (KPT)
         key_tile_kpt<BITS>(tile, blk, lane);
@@ -628,7 +688,7 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
 }
 
 // One CTA per SM (the attribute is set once per instantiation and device).
-template <int BITS, bool KPT>
+template <int BITS, bool KPT, bool ROT>
 static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                   int max_new, cudaStream_t stream) {
   using TS = TileSmem;
@@ -639,26 +699,33 @@ static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __h
   if (e != cudaSuccess) return e;
   int n_sm = dev < 64 ? sms[dev] : 0;
   if (n_sm == 0) {
-    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS, KPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS, KPT, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kWarps * TS::BYTES)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev < 64) sms[dev] = n_sm;
   }
-  quant_tiles_kernel<BITS, KPT><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new, new_len,
-                                                                                  max_new);
+  quant_tiles_kernel<BITS, KPT, ROT><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new,
+                                                                                       new_len, max_new);
   return cudaGetLastError();
 }
 
-bool flush_tiles_serves(const Geo &geo) { return !geo.rot && !geo.sparse && geo.S <= kTileFlushMaxSeqs; }
+template <int BITS>
+static cudaError_t launch_tiles_b(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
+                                  int max_new, cudaStream_t stream) {
+  if (geo.kpt)
+    return geo.rot ? launch_tiles_t<BITS, true, true>(geo, k_new, v_new, new_len, max_new, stream)
+                   : launch_tiles_t<BITS, true, false>(geo, k_new, v_new, new_len, max_new, stream);
+  return geo.rot ? launch_tiles_t<BITS, false, true>(geo, k_new, v_new, new_len, max_new, stream)
+                 : launch_tiles_t<BITS, false, false>(geo, k_new, v_new, new_len, max_new, stream);
+}
+
+bool flush_tiles_serves(const Geo &geo) { return !geo.sparse && geo.S <= kTileFlushMaxSeqs; }
 
 cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                int max_new, cudaStream_t stream) {
-  if (geo.bits == 2)
-    return geo.kpt ? launch_tiles_t<2, true>(geo, k_new, v_new, new_len, max_new, stream)
-                   : launch_tiles_t<2, false>(geo, k_new, v_new, new_len, max_new, stream);
-  return geo.kpt ? launch_tiles_t<4, true>(geo, k_new, v_new, new_len, max_new, stream)
-                 : launch_tiles_t<4, false>(geo, k_new, v_new, new_len, max_new, stream);
+  return geo.bits == 2 ? launch_tiles_b<2>(geo, k_new, v_new, new_len, max_new, stream)
+                       : launch_tiles_b<4>(geo, k_new, v_new, new_len, max_new, stream);
 }
 
 }  // namespace kvq
