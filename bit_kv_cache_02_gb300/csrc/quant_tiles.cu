@@ -182,6 +182,120 @@ __device__ __forceinline__ PairQ pair_q(float lo0, float hi0, float lo1, float h
   return p;
 }
 
+// -------------------------------------------------- dense-and-sparse slices
+//
+// Blocks with outlier entries ("KV cache quantization", "What they report":
+// dense-and-sparse quantization isolating outliers per vector): the outlier
+// of a slice is its first element of largest magnitude, kept exactly in the
+// slice's 32-bit entry (fp16 bits, index at bit 16); min and scale come from
+// the other elements and the outlier's code is 0.  Before a tile's
+// statistics, the pass below records every slice's outlier and overwrites
+// it in the tile with a neighbour of its slice, so the unchanged statistics
+// see the other elements only; once the slice's min is known, the owner lane
+// writes that min in its place, which the unchanged packing codes 0.  Keys
+// are per channel here (per-token keys with outlier entries use the general
+// flush kernel).
+
+// First row of largest magnitude per channel as fp16 (2 x 16-bit lanes):
+// min over rows of (match ? row : 32), exact in fp16.
+__device__ __forceinline__ uint32_t h2_first_match(uint32_t mag, uint32_t best, float pos, uint32_t idx) {
+  const __half2 eq = __heq2(*reinterpret_cast<const __half2 *>(&mag), *reinterpret_cast<const __half2 *>(&best));
+  const __half2 cand = __hfma2(eq, __float2half2_rn(pos - 32.f), __float2half2_rn(32.f));
+  return h2min(idx, h2_as_u32(cand));
+}
+
+struct KeyOutliers {
+  int row[4];  // outlier row of channels 4L .. 4L+3 of this lane
+};
+
+__device__ __forceinline__ KeyOutliers key_outliers_tile(uint8_t *tile, uint8_t *blk, int bits, int lane) {
+  uint8_t *col = tile + 8 * lane;
+  uint32_t ma = 0u, mb = 0u;  // magnitudes of channels (4L, 4L+1) and (4L+2, 4L+3)
+#pragma unroll 8
+  for (int t = 0; t < kG; ++t) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(col + t * kRowPad);
+    ma = h2max(ma, w.x & 0x7FFF7FFFu);
+    mb = h2max(mb, w.y & 0x7FFF7FFFu);
+  }
+  const uint32_t none = h2_as_u32(__float2half2_rn(32.f));
+  uint32_t ia = none, ib = none;
+#pragma unroll 8
+  for (int t = 0; t < kG; ++t) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(col + t * kRowPad);
+    ia = h2_first_match(w.x & 0x7FFF7FFFu, ma, float(t), ia);
+    ib = h2_first_match(w.y & 0x7FFF7FFFu, mb, float(t), ib);
+  }
+  const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&ia));
+  const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&ib));
+  KeyOutliers o;
+  o.row[0] = static_cast<int>(fa.x);
+  o.row[1] = static_cast<int>(fa.y);
+  o.row[2] = static_cast<int>(fb.x);
+  o.row[3] = static_cast<int>(fb.y);
+  uint32_t e[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint16_t *x = reinterpret_cast<uint16_t *>(col + o.row[c] * kRowPad) + c;
+    e[c] = static_cast<uint32_t>(*x) | (static_cast<uint32_t>(o.row[c]) << 16);
+    const int nb = o.row[c] < kG - 1 ? o.row[c] + 1 : o.row[c] - 1;
+    *x = reinterpret_cast<const uint16_t *>(col + nb * kRowPad)[c];
+  }
+  if (blk) reinterpret_cast<uint4 *>(blk + off_ksp(bits))[lane] = make_uint4(e[0], e[1], e[2], e[3]);
+  return o;
+}
+
+struct ValOutliers {
+  int ch[2];     // channel (0 .. 127) of the outlier of rows a, b of this lane
+  bool own[2];   // whether this lane's channel half holds it
+};
+
+// Lane (p, hf) of value_tile: rows a = 2p + j and b = 2p + 1 - j, channels
+// 64 hf .. 64 hf + 63; the other channel half is lane L ^ 16's, whose
+// channels come later in slice order (it wins only a strictly larger
+// magnitude).
+__device__ __forceinline__ ValOutliers value_outliers_tile(uint8_t *tile, uint8_t *blk, int bits, int lane) {
+  const int p = lane & 15, hf = lane >> 4, j = (p >> 2) & 1;
+  const int rows[2] = {2 * p + j, 2 * p + 1 - j};
+  const uint32_t none = h2_as_u32(__float2half2_rn(32.f));
+  ValOutliers o;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    uint8_t *row = tile + rows[r] * kRowPad + 128 * hf;
+    uint32_t m2 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 w = reinterpret_cast<const uint4 *>(row)[i];
+      m2 = h2max(h2max(m2, w.x & 0x7FFF7FFFu), h2max(w.y & 0x7FFF7FFFu, h2max(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+    }
+    const float2 mf = __half22float2(*reinterpret_cast<const __half2 *>(&m2));
+    const float m = fmaxf(mf.x, mf.y);  // this half's largest magnitude
+    const uint32_t mh = h2_as_u32(__float2half2_rn(m));
+    // first word whose even (low) and whose odd (high) channel matches
+    uint32_t iw = none;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 w = reinterpret_cast<const uint4 *>(row)[i];
+      iw = h2_first_match(w.x & 0x7FFF7FFFu, mh, float(4 * i), iw);
+      iw = h2_first_match(w.y & 0x7FFF7FFFu, mh, float(4 * i + 1), iw);
+      iw = h2_first_match(w.z & 0x7FFF7FFFu, mh, float(4 * i + 2), iw);
+      iw = h2_first_match(w.w & 0x7FFF7FFFu, mh, float(4 * i + 3), iw);
+    }
+    const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&iw));
+    const int c_in = min(2 * static_cast<int>(wf.x), 2 * static_cast<int>(wf.y) + 1);  // channel within the half
+    const float om = __shfl_xor_sync(0xffffffffu, m, 16);
+    o.own[r] = hf == 0 ? m >= om : m > om;
+    o.ch[r] = 64 * hf + c_in;
+    if (o.own[r]) {
+      uint16_t *x = reinterpret_cast<uint16_t *>(row) + c_in;
+      if (blk)
+        reinterpret_cast<uint32_t *>(blk + off_vsp(bits))[rows[r]] =
+            static_cast<uint32_t>(*x) | (static_cast<uint32_t>(64 * hf + c_in) << 16);
+      *x = reinterpret_cast<const uint16_t *>(row)[c_in < 63 ? c_in + 1 : c_in - 1];
+    }
+  }
+  return o;
+}
+
 // ---------------------------------------------------------------- key tile
 //
 // Lane L: channels 4L .. 4L+3, i.e. k-tile kt = L / 4, channel octet j =
@@ -193,8 +307,8 @@ __device__ __forceinline__ PairQ pair_q(float lo0, float hi0, float lo1, float h
 // octet j = g / 4.  The loops stay rolled and re-read the tile from shared
 // memory: fully unrolled, the key and value code no longer fit the
 // instruction cache.
-template <int BITS>
-__device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int lane) {
+template <int BITS, bool SP>
+__device__ __forceinline__ void key_tile(uint8_t *tile, uint8_t *blk, int lane, const KeyOutliers &ko) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int kt = lane >> 2, j = (lane >> 1) & 1, q0 = 2 * (lane & 1);
@@ -233,6 +347,12 @@ __device__ __forceinline__ void key_tile(const uint8_t *tile, uint8_t *blk, int 
   if (blk) {
     reinterpret_cast<float4 *>(blk + off_ks(BITS))[lane] = make_float4(qa.sc0, qa.sc1, qb.sc0, qb.sc1);
     reinterpret_cast<float4 *>(blk + off_km(BITS))[lane] = make_float4(qa.lo0, qa.lo1, qb.lo0, qb.lo1);
+  }
+  if constexpr (SP) {  // each outlier becomes its channel's min: code 0
+    const float lo4[4] = {qa.lo0, qa.lo1, qb.lo0, qb.lo1};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      reinterpret_cast<__half *>(tile + 8 * lane + ko.row[c] * kRowPad)[c] = __float2half_rn(lo4[c]);
   }
   float sc[NU];
   int pos[NU];
@@ -467,8 +587,8 @@ __device__ __forceinline__ void key_tile_kpt(const uint8_t *tile, uint8_t *blk, 
 // the order (2p + j, 2p + 1 - j), which spreads each quarter warp's 16-byte
 // reads over the eight bank groups; the byte permutes that pair a channel's
 // two tokens undo the order.
-template <int BITS, bool KPT>
-__device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, int lane) {
+template <int BITS, bool KPT, bool SP>
+__device__ __forceinline__ void value_tile(uint8_t *tile, uint8_t *blk, int lane, const ValOutliers &vo) {
   constexpr int NU = 8 / BITS, WH = 4 / NU;
   const float levels = float((1 << BITS) - 1);
   const int p = lane & 15, hf = lane >> 4;
@@ -517,6 +637,14 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
   if (hf == 0 && blk) {
     reinterpret_cast<float2 *>(blk + off_vs(BITS, KPT))[p] = make_float2(pq.sc0, pq.sc1);
     reinterpret_cast<float2 *>(blk + off_vm(BITS, KPT))[p] = make_float2(pq.lo0, pq.lo1);
+  }
+  if constexpr (SP) {  // each outlier this lane holds becomes its token's min: code 0
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int tok = r == 0 ? 2 * p + j : 2 * p + 1 - j;
+      if (vo.own[r])
+        reinterpret_cast<__half *>(tile + tok * kRowPad)[vo.ch[r]] = __float2half_rn(tok == 2 * p ? pq.lo0 : pq.lo1);
+    }
   }
   float sc[NU];
   int pos[NU];
@@ -572,12 +700,12 @@ __device__ __forceinline__ void value_tile(const uint8_t *tile, uint8_t *blk, in
 // Persistent CTAs of TileShape<BITS>::WARPS independent warps (one CTA per SM).  Warp gw of
 // NW takes tiles [gw U / NW, (gw + 1) U / NW) of the line of U = 2 x (groups
 // flushed) tiles, ordered (sequence, KV head, group, keys / values).
-template <int BITS, bool KPT, bool ROT>
+template <int BITS, bool KPT, bool ROT, bool SP>
 __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
     quant_tiles_kernel(Geo geo, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
                        const int *__restrict__ new_len, int max_new) {
   using TS = TileSmem;
-  constexpr int NS = TS::NS, BB = block_bytes(BITS, KPT);
+  constexpr int NS = TS::NS, BB = block_bytes(BITS, KPT, SP);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *base = smem + warp * TS::BYTES;
@@ -669,12 +797,16 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
     if (!blk && cp.kind == 0 && lane == 0) set_status(geo.status, KVQ_STATUS_BAD_BLOCK);
     if (ROT) rotate_tile(tile, lane);
     if (cp.kind == 0) {
-      if (KPT)
+      KeyOutliers ko = {};
+      if constexpr (SP) ko = key_outliers_tile(tile, blk, BITS, lane);
+      if constexpr (KPT)
         key_tile_kpt<BITS>(tile, blk, lane);
       else
-        key_tile<BITS>(tile, blk, lane);
+        key_tile<BITS, SP>(tile, blk, lane, ko);
     } else {
-      value_tile<BITS, KPT>(tile, blk, lane);
+      ValOutliers vo = {};
+      if constexpr (SP) vo = value_outliers_tile(tile, blk, BITS, lane);
+      value_tile<BITS, KPT, SP>(tile, blk, lane, vo);
     }
     __syncwarp();  // every lane's reads of the slot are done before it is refilled
     ++cseq;
@@ -688,7 +820,7 @@ __global__ void __launch_bounds__(TileShape<BITS>::WARPS * 32, 1)
 }
 
 // One CTA per SM (the attribute is set once per instantiation and device).
-template <int BITS, bool KPT, bool ROT>
+template <int BITS, bool KPT, bool ROT, bool SP>
 static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                   int max_new, cudaStream_t stream) {
   using TS = TileSmem;
@@ -699,13 +831,13 @@ static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __h
   if (e != cudaSuccess) return e;
   int n_sm = dev < 64 ? sms[dev] : 0;
   if (n_sm == 0) {
-    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS, KPT, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(quant_tiles_kernel<BITS, KPT, ROT, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kWarps * TS::BYTES)) != cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev < 64) sms[dev] = n_sm;
   }
-  quant_tiles_kernel<BITS, KPT, ROT><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new,
+  quant_tiles_kernel<BITS, KPT, ROT, SP><<<n_sm, kWarps * 32, kWarps * TS::BYTES, stream>>>(geo, k_new, v_new,
                                                                                        new_len, max_new);
   return cudaGetLastError();
 }
@@ -713,14 +845,18 @@ static cudaError_t launch_tiles_t(const Geo &geo, const __half *k_new, const __h
 template <int BITS>
 static cudaError_t launch_tiles_b(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                   int max_new, cudaStream_t stream) {
+  // (outlier entries come with neither per-token keys here nor the rotation)
+  if (geo.sparse) return launch_tiles_t<BITS, false, false, true>(geo, k_new, v_new, new_len, max_new, stream);
   if (geo.kpt)
-    return geo.rot ? launch_tiles_t<BITS, true, true>(geo, k_new, v_new, new_len, max_new, stream)
-                   : launch_tiles_t<BITS, true, false>(geo, k_new, v_new, new_len, max_new, stream);
-  return geo.rot ? launch_tiles_t<BITS, false, true>(geo, k_new, v_new, new_len, max_new, stream)
-                 : launch_tiles_t<BITS, false, false>(geo, k_new, v_new, new_len, max_new, stream);
+    return geo.rot ? launch_tiles_t<BITS, true, true, false>(geo, k_new, v_new, new_len, max_new, stream)
+                   : launch_tiles_t<BITS, true, false, false>(geo, k_new, v_new, new_len, max_new, stream);
+  return geo.rot ? launch_tiles_t<BITS, false, true, false>(geo, k_new, v_new, new_len, max_new, stream)
+                 : launch_tiles_t<BITS, false, false, false>(geo, k_new, v_new, new_len, max_new, stream);
 }
 
-bool flush_tiles_serves(const Geo &geo) { return !geo.sparse && geo.S <= kTileFlushMaxSeqs; }
+bool flush_tiles_serves(const Geo &geo) {
+  return !(geo.sparse && (geo.kpt || geo.rot)) && geo.S <= kTileFlushMaxSeqs;
+}
 
 cudaError_t launch_flush_tiles(const Geo &geo, const __half *k_new, const __half *v_new, const int *new_len,
                                int max_new, cudaStream_t stream) {
