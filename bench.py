@@ -309,7 +309,8 @@ def run_ours(args, w, layers, rank, world, local):
     pre = prefill_lengths(w, max(W, 1) + pool)
     capacity = int(pre.max()) + max(W, 1) + pool + K + 64   # room for the end-to-end steps too
     caches, prefill_s = build_caches(kvq, w, layers, pre, capacity, device)
-    prefill = {"seconds_per_layer": statistics.median(prefill_s), "bytes_per_layer": prefill_bytes(pre, w)}
+    prefill = {"seconds_per_layer": statistics.median(prefill_s), "bytes_per_layer": prefill_bytes(pre, w),
+               "seconds_min_max": (min(prefill_s), max(prefill_s))}
 
     S, Hq = w.seqs, w.q_heads
     k_new = [[synth.kv_tokens(w, l, 1, device=device, stream_id=1 + p) for l in range(layers)] for p in range(pool)]
@@ -789,7 +790,8 @@ def main():
                      "unit": "GB/s", "peak": peak,
                      "frac": r["prefill"]["bytes_per_layer"] / r["prefill"]["seconds_per_layer"] / 1e9 / peak,
                      "algorithmic_bytes": r["prefill"]["bytes_per_layer"], "traffic": q_traffic,
-                     "us": r["prefill"]["seconds_per_layer"] * 1e6},
+                     "us": r["prefill"]["seconds_per_layer"] * 1e6,
+                     "us_min_max_over_layers": [round(x * 1e6, 1) for x in r["prefill"]["seconds_min_max"]]},
         "configs": configs,
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
