@@ -35,6 +35,13 @@
 // the group block (a tile's code words and metadata together cover whole
 // 32-byte sectors, which L2 merges before they reach HBM), so a warp needs
 // shared memory only for its ring.
+//
+// Options, as template flags of the kernel: keys grouped per token
+// (key_tile_kpt), the Walsh-Hadamard rotation of the rows in place before a
+// tile is quantized (rotate_tile), and dense-and-sparse blocks (an outlier
+// pass before the statistics).  Per-token keys with outlier entries, and
+// batches of more than kTileFlushMaxSeqs sequences, use the general flush
+// kernel.
 #include "quant_common.cuh"
 
 namespace kvq {
