@@ -466,15 +466,16 @@ def test_appends_past_the_length_bits(kvq, S, H, cap):
     _attn_close(_attend(kvq, cache, q, 400), orc.attention(q))
 
 
-def test_prefill_of_more_sequences_than_the_tile_kernel_takes(kvq):
-    """The tile kernel flushes batches of up to 2048 sequences; a prefill of
-    2100 ragged sequences goes through the one-group-per-CTA flush kernel
-    and leaves the oracle's bytes, and decode (planned by the plan kernel)
-    matches."""
-    S, H, T = 2100, 1, 70
-    rng = np.random.default_rng(2100)
+@pytest.mark.parametrize("S", [2048, 2100])
+def test_prefill_at_and_past_the_tile_kernel_batch_limit(kvq, S):
+    """The tile kernel flushes batches of up to 2048 sequences (its largest
+    line); a prefill of 2100 ragged sequences goes through the
+    one-group-per-CTA flush kernel.  Both leave the oracle's bytes, and
+    decode (planned by the plan kernel) matches."""
+    H, T = 1, 70
+    rng = np.random.default_rng(S)
     lens = rng.integers(0, T + 1, S).astype(np.int32)
-    k, v = _rand_kv(S, H, T, seed=2101)
+    k, v = _rand_kv(S, H, T, seed=S + 1)
     cache, orc = _build(kvq, S, H, T + 8, 2, R=32)  # up to two groups flushed per sequence
     _append(kvq, cache, orc, k, v, lens)
     _compare_state(cache, orc)
